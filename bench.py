@@ -1,0 +1,460 @@
+#!/usr/bin/env python3
+"""Benchmark of the NVFP4 routed-MoE expert path on one GB300 (or N independent replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+One step = one pass of the whole hot path over one batch: moe_quantize_input,
+moe_plan and moe_grouped_fp4_forward (permute, GEMM1 + SwiGLU/ReLU^2 + NVFP4
+requant, GEMM2, finalize). Inputs (BF16 hidden states, routing) and the prepared
+NVFP4 weights are resident in HBM; L2 is flushed between steps (a 256 MB write
+outside the timed events). Rank 0 prints one JSON line.
+
+--impl reference times the CPU oracle (oracle/) on the machine's host cores on a
+bounded sample of the same workload (this repository's reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import moe_inputs as mi  # noqa: E402
+
+METRIC = "MoE layer tokens/s; % of NVFP4-TC/HBM roofline (decode T=8, prefill 4k)"
+NV = 0.5 + 1.0 / 16.0      # NVFP4 bytes per element: packed E2M1 + one E4M3 scale per 16
+FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense ratio (GB300): FP4 tensor rate / BF16 tensor rate
+
+
+def workload_name(cfg) -> str:
+    s = f"{cfg.name}: T={cfg.M} H={cfg.H} I={cfg.I} E={cfg.E} top_k={cfg.top_k} {cfg.act}"
+    if cfg.num_local is not None:
+        s += f" local={cfg.local_offset}..{cfg.local_offset + cfg.El - 1}"
+    if cfg.skew:
+        s += f" zipf={cfg.skew}"
+    return s
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# --------------------------------------------------------------------------- algorithmic work
+def kernel_work(cfg, ids):
+    """Per-launch algorithmic bytes and FLOPs of each kernel of one step (no padding rows)."""
+    l = ids.astype(np.int64) - cfg.local_offset
+    valid = (l >= 0) & (l < cfg.El)
+    R = int(valid.sum())
+    active = int(np.unique(l[valid]).size)
+    M, H, I, N1, k = cfg.M, cfg.H, cfg.I, cfg.N1, cfg.top_k
+    w = {
+        "quantize": {"bytes": M * H * 2 + M * H * NV + M * 4, "flops": 0.0},
+        "plan": {"bytes": M * k * 4 * 2 + cfg.El * 8, "flops": 0.0},
+        "permute": {"bytes": 2 * R * H * NV, "flops": 0.0},
+        "gemm1": {"bytes": active * N1 * H * NV + R * H * NV + R * I * NV + cfg.El * 4,
+                  "flops": 2.0 * R * H * N1},
+        "gemm2": {"bytes": active * H * I * NV + R * I * NV + R * H * 2 + cfg.El * 4,
+                  "flops": 2.0 * R * I * H},
+        "finalize": {"bytes": R * H * 2 + M * k * 8 + M * H * 2, "flops": 0.0},
+    }
+    step = mi.algorithmic_work(cfg, ids, finalize=True)
+    return w, step, R, active
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- GPU arm
+def setup_gpu(cfg, dev):
+    import torch
+
+    import nvfp4_routed_moe_sort_gb300 as pkg
+    x = mi.hidden_bf16(cfg, dev)
+    ids, tw = mi.routing(cfg)
+    q1, q2 = [], []
+    # draw and quantise one expert at a time (the BF16 stacks of the large configs are 22 GB)
+    El = cfg.El
+    d1 = torch.empty(El, cfg.N1, cfg.H // 2, dtype=torch.uint8, device=dev)
+    s1 = torch.empty(El, cfg.N1, cfg.H // 16, dtype=torch.uint8, device=dev)
+    a1 = torch.empty(El, dtype=torch.float32, device=dev)
+    d2 = torch.empty(El, cfg.H, cfg.I // 2, dtype=torch.uint8, device=dev)
+    s2 = torch.empty(El, cfg.H, cfg.I // 16, dtype=torch.uint8, device=dev)
+    a2 = torch.empty(El, dtype=torch.float32, device=dev)
+    scratch = torch.empty(1, dtype=torch.float32, device=dev)
+    for l in range(El):
+        w1 = mi.expert_w1_bf16(cfg, l, dev)
+        pkg.moe_quantize_weights(w1.view(torch.int16)[None], d1[l:l + 1], s1[l:l + 1], a1[l:l + 1], scratch)
+        del w1
+        w2 = mi.expert_w2_bf16(cfg, l, dev)
+        pkg.moe_quantize_weights(w2.view(torch.int16)[None], d2[l:l + 1], s2[l:l + 1], a2[l:l + 1], scratch)
+        del w2
+    layer = pkg.NVFP4RoutedMoE(d1, s1, a1, d2, s2, a2, activation=cfg.act, num_experts=cfg.E,
+                               local_expert_offset=cfg.local_offset, fc2_input_scale=cfg.fc2_input_scale,
+                               scale_mode=cfg.scale_mode)
+    torch.cuda.synchronize()
+    return layer, x, ids, tw
+
+
+def traffic_from_profiles(kernel: str, workload: str):
+    """dram bytes per launch of `kernel` from the committed ncu summary, if the kernel's
+    source is unchanged since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    ent = d.get(workload, {}).get(kernel)
+    if not ent:
+        return None
+    src = os.path.join(ROOT, "nvfp4_routed_moe_sort_gb300", "csrc", ent.get("source", "gemm.cu"))
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if h != ent.get("source_sha"):
+        return None
+    return ent["dram_bytes_per_launch"]
+
+
+def run_gpu(args, cfg, rank, world):
+    import torch
+
+    dev = torch.device(f"cuda:{int(os.environ.get('LOCAL_RANK', 0))}")
+    torch.cuda.set_device(dev)
+    from nvfp4_routed_moe_sort_gb300.build import build
+    build()
+    layer, x, ids, tw = setup_gpu(cfg, dev)
+    ids_t = torch.from_numpy(ids).to(dev)
+    tw_t = torch.from_numpy(tw).to(dev)
+    M, k = ids.shape
+    b = layer.buffers(M, k, True)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    n_ev = 8
+    K, W = args.steps, args.warmup
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(K + W)]
+
+    def step(e):
+        e[0].record()
+        layer.quantize(x, b)
+        e[1].record()
+        layer.plan(ids_t, b)
+        e[2].record()
+        layer.experts(tw_t, b, True, step_events=e[2:7])
+        e[7].record()
+
+    for i in range(W):
+        flush.zero_()
+        step(evs[i])
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(W, W + K):
+        flush.zero_()
+        step(evs[i])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    clk = clocks.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    assert layer.device_status(M, k, True) == 0, "device status word set"
+    names = ["quantize", "plan", "permute", "gemm1", "gemm2", "finalize"]
+    per = {n: [] for n in names}
+    steps_ms = []
+    for e in evs[W:]:
+        t = [e[i].elapsed_time(e[i + 1]) for i in range(n_ev - 1)]
+        # events: 0 quantize 1 plan 2 [permute 3 gemm1 4 gemm2 5 finalize 6] 7
+        per["quantize"].append(t[0])
+        per["plan"].append(t[1])
+        per["permute"].append(t[2])
+        per["gemm1"].append(t[3])
+        per["gemm2"].append(t[4])
+        per["finalize"].append(t[5])
+        steps_ms.append(e[0].elapsed_time(e[7]))
+    ms = float(np.mean(steps_ms))
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    work, stepw, R, active = kernel_work(cfg, ids)
+    kern_ms = {n: float(np.mean(v)) for n, v in per.items()}
+    dom = max(["gemm1", "gemm2"], key=lambda n: kern_ms[n])
+    peaks = load_peaks()
+    fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
+    t_dom = kern_ms[dom] * 1e-3
+    bytes_dom = work[dom]["bytes"]
+    flops_dom = work[dom]["flops"]
+    hbm_time = bytes_dom / (peaks["hbm_gbs"] * 1e9)
+    tc_time = flops_dom / (fp4_peak * 1e12)
+    if hbm_time >= tc_time:
+        roof = {"bound": "hbm", "achieved": bytes_dom / t_dom / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": flops_dom / t_dom / 1e12, "peak": fp4_peak, "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["kernel"] = dom
+    roof["peak_source"] = (f"{peaks['source']} HBM copy" if roof["bound"] == "hbm"
+                           else f"{peaks['source']} bf16 burst x {FP4_OVER_BF16:g} (nominal FP4/BF16)")
+    roof["traffic"] = traffic_from_profiles(dom, cfg.name)
+    step_roof_s = max(stepw["bytes"] / (peaks["hbm_gbs"] * 1e9), stepw["flops"] / (fp4_peak * 1e12))
+    # end to end through the public API with host buffers
+    e2e = run_e2e(layer, x, ids, tw, dev, max(3, min(K, 50)))
+    launches_per_step = 6 + (2 if M * k > 2048 else 0)
+    res = {
+        "metric": METRIC, "value": world * M / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "nvfp4 (e2m1 x e2m1, e4m3 block scales, fp32 accumulate)", "data": "synthetic",
+        "config": {"workload": workload_name(cfg), "tokens": M, "hidden": cfg.H, "inter": cfg.I,
+                   "experts": cfg.E, "top_k": k, "routed_rows": R, "active_experts": active,
+                   "l2": "flushed between steps (256 MB write outside the timed events)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": roof,
+        "step_roofline": {"frac": step_roof_s / (ms * 1e-3), "bytes": stepw["bytes"], "flops": stepw["flops"],
+                          "note": "whole step: max(bytes/HBM peak, flops/FP4 peak) over measured step time"},
+        "kernels_ms": kern_ms,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk,
+        "wall_s_timed_region": wall,
+    }
+    return res
+
+
+def run_e2e(layer, x, ids, tw, dev, steps):
+    import torch
+    M, k = ids.shape
+    hx = x.cpu().pin_memory()
+    hid = torch.from_numpy(ids).pin_memory()
+    htw = torch.from_numpy(tw).pin_memory()
+    hout = torch.empty(M, x.shape[1], dtype=torch.bfloat16).pin_memory()
+    dx = torch.empty_like(x)
+    did = torch.empty(M, k, dtype=torch.int32, device=dev)
+    dtw = torch.empty(M, k, dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    times = []
+    for i in range(steps + 3):
+        flush.zero_()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        dx.copy_(hx, non_blocking=True)
+        did.copy_(hid, non_blocking=True)
+        dtw.copy_(htw, non_blocking=True)
+        out = layer.forward(dx, did, dtw, do_finalize=True)
+        hout.copy_(out, non_blocking=True)
+        e.record()
+        e.synchronize()
+        if i >= 3:
+            times.append(s.elapsed_time(e))
+    ms = float(np.mean(times))
+    return {"value": M / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": int(hx.numel() * 2 + hid.numel() * 4 + htw.numel() * 4),
+            "d2h_bytes_per_step": int(hout.numel() * 2)}
+
+
+# --------------------------------------------------------------------------- oracle arm
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+class OracleArm:
+    """The CPU oracle on a fixed sample of the workload's tokens (weights prepared once)."""
+
+    def __init__(self, cfg, n_tokens: int):
+        from oracle import moe as O
+        from oracle import quantize as Q
+        self.cfg = cfg
+        self.O = O
+        self.Q = Q
+        dev = "cuda" if _cuda_available() else "cpu"
+        x = mi.hidden_bf16(cfg, dev).float().cpu().numpy()
+        self.ids, self.tw = mi.routing(cfg)
+        self.tokens = list(range(min(n_tokens, cfg.M)))
+        self.x = x[self.tokens]
+        cache = {}
+
+        def load(l):
+            if l not in cache:
+                w1 = mi.expert_w1_bf16(cfg, l, dev).float().cpu().numpy()
+                w2 = mi.expert_w2_bf16(cfg, l, dev).float().cpu().numpy()
+                cache[l] = (Q.quantize_weight(w1), Q.quantize_weight(w2))
+            return cache[l]
+        self.W = O.ExpertWeights(cfg.El, cfg.H, cfg.I, cfg.gated, load)
+        for t in self.tokens:                        # weight preparation is not timed
+            for j in range(cfg.top_k):
+                l = int(self.ids[t, j]) - cfg.local_offset
+                if 0 <= l < cfg.El:
+                    self.W.get(l)
+
+    def step(self):
+        cfg = self.cfg
+        xq, xsf, xs = self.Q.quantize_activations(self.x, cfg.scale_mode)
+        n = len(self.tokens)
+        ids = self.ids[self.tokens]
+        tw = self.tw[self.tokens]
+        return self.O.forward_tokens(list(range(n)), xq, xsf, xs, ids, tw, self.W, cfg.act,
+                                     local_expert_offset=cfg.local_offset,
+                                     fc2_input_scale=cfg.fc2_input_scale)["out"]
+
+
+def _cuda_available() -> bool:
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except Exception:
+        return False
+
+
+def oracle_sample_tokens(cfg) -> int:
+    # about 1-3 s of oracle work per step on a many-core host
+    big = cfg.H * cfg.N1 > 8_000_000
+    return 1 if big else min(cfg.M, 2)
+
+
+def run_reference(args, cfg):
+    arm = OracleArm(cfg, oracle_sample_tokens(cfg))
+    for _ in range(args.warmup):
+        arm.step()
+    times = []
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        arm.step()
+        times.append(time.perf_counter() - t)
+    s = float(np.mean(times))
+    n = len(arm.tokens)
+    v = n / s
+    sample = f"tokens {arm.tokens} of the batch per step (all their routed experts), weights prepared untimed"
+    return {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": s * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64 sums / f32 codecs (CPU oracle)", "data": "synthetic",
+        "config": {"workload": workload_name(cfg), "tokens": cfg.M},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def cpu_baseline(cfg, budget_s: float = 12.0):
+    """The oracle as it stands, on a bounded sample of the workload, on this host's cores."""
+    arm = OracleArm(cfg, oracle_sample_tokens(cfg))
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        arm.step()
+        n += 1
+        if time.perf_counter() - t0 > budget_s or n >= 20:
+            break
+    s = (time.perf_counter() - t0) / n
+    return {"value": len(arm.tokens) / s, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"{n} passes over tokens {arm.tokens} (all their routed experts); weights prepared untimed"}
+
+
+# --------------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="decode_t8", choices=sorted(mi.CONFIGS))
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    cfg = mi.CONFIGS[args.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, cfg)), flush=True)
+        return 0
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group("nccl")
+    res = run_gpu(args, cfg, rank, world)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(cfg)
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,18 @@
+"""NVFP4 routed-MoE expert path for GB300 (sm_103a).
+
+The compute runs in ``libmoe_nvfp4.so`` (C ABI: include/moe_nvfp4.h); this package
+holds its build script, a ctypes binding with the same function names, and a small
+buffer-owning wrapper. Importing it never falls back to another implementation:
+calls raise ``MoEError`` if the library is not built.
+"""
+from . import _lib
+from ._lib import (  # noqa: F401
+    EXPORTED, MOE_ACT_RELU2, MOE_ACT_SWIGLU, MOE_DEV_DUPLICATE_EXPERT, MOE_DEV_TIMEOUT,
+    MOE_SCALE_GLOBAL_ONE, MOE_SCALE_PER_TOKEN, MoEError, WeightsT, lib, make_weights,
+    moe_abi_version, moe_debug_gemm1, moe_finalize, moe_forward_workspace_bytes,
+    moe_forward_workspace_layout, moe_grouped_fp4_forward, moe_plan, moe_plan_capacity,
+    moe_plan_workspace_bytes, moe_prepare_weights, moe_prepared_weights_bytes, moe_quantize_input,
+    moe_quantize_weights, status_string,
+)
+from .build import LIB as LIB_PATH  # noqa: F401
+from .moe import NVFP4RoutedMoE, quantize_weights  # noqa: F401

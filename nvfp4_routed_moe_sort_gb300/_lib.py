@@ -1,0 +1,198 @@
+"""ctypes binding of libmoe_nvfp4.so (the C ABI in include/moe_nvfp4.h).
+
+Argument marshalling only: every function here turns torch tensors into device
+pointers, passes torch's current CUDA stream and raises on a non-OK status. All of
+the path runs in the library's CUDA kernels; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from ctypes import c_float, c_int32, c_int64, c_size_t, c_void_p
+
+from .build import LIB as LIB_PATH
+
+_lib = None
+
+MOE_OK = 0
+MOE_ACT_SWIGLU, MOE_ACT_RELU2 = 0, 1
+MOE_SCALE_GLOBAL_ONE, MOE_SCALE_PER_TOKEN = 0, 1
+MOE_DEV_DUPLICATE_EXPERT, MOE_DEV_TIMEOUT = 1, 2
+
+EXPORTED = [
+    "moe_status_string", "moe_abi_version", "moe_quantize_input", "moe_plan_capacity",
+    "moe_plan_workspace_bytes", "moe_plan", "moe_quantize_weights", "moe_prepared_weights_bytes",
+    "moe_prepare_weights", "moe_forward_workspace_bytes", "moe_forward_workspace_layout",
+    "moe_grouped_fp4_forward", "moe_finalize", "moe_debug_gemm1",
+]
+
+
+class MoEError(RuntimeError):
+    pass
+
+
+class WeightsT(ctypes.Structure):
+    """moe_nvfp4_weights_t"""
+    _fields_ = [
+        ("w1", c_void_p), ("w1_sf", c_void_p), ("w1_alpha", c_void_p),
+        ("w2", c_void_p), ("w2_sf", c_void_p), ("w2_alpha", c_void_p),
+        ("num_local_experts", c_int32), ("hidden", c_int32), ("inter", c_int32),
+        ("activation", c_int32),
+    ]
+
+
+def _declare(lib):
+    P = c_void_p
+    sig = {
+        "moe_status_string": (ctypes.c_char_p, [c_int32]),
+        "moe_abi_version": (c_int32, []),
+        "moe_quantize_input": (c_int32, [P, c_int32, c_int32, c_int64, c_int32, P, P, P, P]),
+        "moe_plan_capacity": (c_size_t, [c_int32, c_int32, c_int32]),
+        "moe_plan_workspace_bytes": (c_size_t, [c_int32, c_int32, c_int32]),
+        "moe_plan": (c_int32, [P, c_int32, c_int32, c_int32, c_int32, c_int32, P, P, P, P, P, c_size_t,
+                               P, P]),
+        "moe_quantize_weights": (c_int32, [P, c_int32, c_int32, c_int32, P, P, P, P, P]),
+        "moe_prepared_weights_bytes": (c_size_t, [ctypes.POINTER(WeightsT)]),
+        "moe_prepare_weights": (c_int32, [ctypes.POINTER(WeightsT), P, c_size_t, P]),
+        "moe_forward_workspace_bytes": (c_size_t, [c_int32, c_int32, ctypes.POINTER(WeightsT), c_int32]),
+        "moe_forward_workspace_layout": (c_int32, [c_int32, c_int32, ctypes.POINTER(WeightsT), c_int32,
+                                                   ctypes.POINTER(c_size_t)]),
+        "moe_grouped_fp4_forward": (c_int32, [P, P, P, c_int32, c_int32, P, P, P, ctypes.POINTER(WeightsT),
+                                              P, c_size_t, P, c_float, c_int32, P, P, P, c_size_t, P,
+                                              ctypes.POINTER(c_void_p), c_int32, P]),
+        "moe_finalize": (c_int32, [P, P, P, c_int32, c_int32, c_int32, P, P]),
+        "moe_debug_gemm1": (c_int32, [P, P, c_int32, c_int32, P, P, P, ctypes.POINTER(WeightsT), P,
+                                      c_size_t, c_int32, P, P, c_size_t, P, P]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise MoEError(f"{LIB_PATH} is missing: build it first (nvfp4_routed_moe_sort_gb300.build, "
+                           "nvcc for sm_103a); there is no fallback path")
+        _lib = ctypes.CDLL(LIB_PATH)
+        _declare(_lib)
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().moe_status_string(code).decode()
+
+
+def _check(code: int, what: str):
+    if code != MOE_OK:
+        raise MoEError(f"{what}: {status_string(code)}")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is not None:
+        return stream if isinstance(stream, int) else stream.cuda_stream
+    import torch
+    return torch.cuda.current_stream().cuda_stream
+
+
+def make_weights(num_local_experts: int, hidden: int, inter: int, activation: int,
+                 w1=None, w1_sf=None, w1_alpha=None, w2=None, w2_sf=None, w2_alpha=None) -> WeightsT:
+    return WeightsT(_ptr(w1), _ptr(w1_sf), _ptr(w1_alpha), _ptr(w2), _ptr(w2_sf), _ptr(w2_alpha),
+                    num_local_experts, hidden, inter, activation)
+
+
+# ---------------------------------------------------------------- entry points
+def moe_abi_version() -> int:
+    return lib().moe_abi_version()
+
+
+def moe_quantize_input(x, mode, xq, xsf, xs, stream=None):
+    M, H = x.shape
+    _check(lib().moe_quantize_input(_ptr(x), M, H, x.stride(0), mode, _ptr(xq), _ptr(xsf), _ptr(xs),
+                                    _stream(stream)), "moe_quantize_input")
+
+
+def moe_plan_capacity(M, top_k, num_local_experts) -> int:
+    return lib().moe_plan_capacity(M, top_k, num_local_experts)
+
+
+def moe_plan_workspace_bytes(M, top_k, num_local_experts) -> int:
+    return lib().moe_plan_workspace_bytes(M, top_k, num_local_experts)
+
+
+def moe_plan(topk_ids, num_experts, local_expert_offset, num_local_experts, counts, padded_offsets,
+             row_to_slot, token_to_row, workspace, dev_status, stream=None):
+    M, k = topk_ids.shape
+    wsb = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().moe_plan(_ptr(topk_ids), M, k, num_experts, local_expert_offset, num_local_experts,
+                          _ptr(counts), _ptr(padded_offsets), _ptr(row_to_slot), _ptr(token_to_row),
+                          _ptr(workspace), wsb, _ptr(dev_status), _stream(stream)), "moe_plan")
+
+
+def moe_quantize_weights(w, data, sf, alpha, amax_scratch, stream=None):
+    E, R, C = w.shape
+    _check(lib().moe_quantize_weights(_ptr(w), E, R, C, _ptr(data), _ptr(sf), _ptr(alpha),
+                                      _ptr(amax_scratch), _stream(stream)), "moe_quantize_weights")
+
+
+def moe_prepared_weights_bytes(w: WeightsT) -> int:
+    return lib().moe_prepared_weights_bytes(ctypes.byref(w))
+
+
+def moe_prepare_weights(w: WeightsT, prepared, stream=None):
+    _check(lib().moe_prepare_weights(ctypes.byref(w), _ptr(prepared), prepared.numel() * prepared.element_size(),
+                                     _stream(stream)), "moe_prepare_weights")
+
+
+def moe_forward_workspace_bytes(M, top_k, w: WeightsT, do_finalize) -> int:
+    return lib().moe_forward_workspace_bytes(M, top_k, ctypes.byref(w), int(do_finalize))
+
+
+def moe_forward_workspace_layout(M, top_k, w: WeightsT, do_finalize) -> list[int]:
+    arr = (c_size_t * 6)()
+    _check(lib().moe_forward_workspace_layout(M, top_k, ctypes.byref(w), int(do_finalize), arr),
+           "moe_forward_workspace_layout")
+    return list(arr)
+
+
+def moe_grouped_fp4_forward(padded_offsets, row_to_slot, token_to_row, xq, xsf, xs, w: WeightsT, prepared,
+                            topk_weights, fc2_input_scale, do_finalize, out, gemm2_out, workspace,
+                            dev_status, step_events=None, stream=None):
+    M, k = token_to_row.shape
+    ev = None
+    nev = 0
+    if step_events:
+        ev = (c_void_p * len(step_events))(*[e.cuda_event for e in step_events])
+        nev = len(step_events)
+    _check(lib().moe_grouped_fp4_forward(
+        _ptr(padded_offsets), _ptr(row_to_slot), _ptr(token_to_row), M, k, _ptr(xq), _ptr(xsf), _ptr(xs),
+        ctypes.byref(w), _ptr(prepared), prepared.numel() * prepared.element_size(), _ptr(topk_weights),
+        float(fc2_input_scale), int(do_finalize), _ptr(out), _ptr(gemm2_out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(dev_status), ev, nev, _stream(stream)),
+        "moe_grouped_fp4_forward")
+
+
+def moe_finalize(gemm2_out, topk_weights, token_to_row, out, stream=None):
+    M, k = token_to_row.shape
+    H = out.shape[1]
+    _check(lib().moe_finalize(_ptr(gemm2_out), _ptr(topk_weights), _ptr(token_to_row), M, k, H, _ptr(out),
+                              _stream(stream)), "moe_finalize")
+
+
+def moe_debug_gemm1(padded_offsets, row_to_slot, M, top_k, xq, xsf, xs, w: WeightsT, prepared, mode,
+                    dbg_out, workspace, dev_status, stream=None):
+    _check(lib().moe_debug_gemm1(
+        _ptr(padded_offsets), _ptr(row_to_slot), M, top_k, _ptr(xq), _ptr(xsf), _ptr(xs), ctypes.byref(w),
+        _ptr(prepared), prepared.numel() * prepared.element_size(), mode, _ptr(dbg_out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream)), "moe_debug_gemm1")

@@ -1,0 +1,125 @@
+// Host-side sizes and buffer layouts shared by the entry points, and the internal launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe_nvfp4.h"
+#include "common.cuh"
+
+namespace moe {
+
+// Problem sizes, with the paddings the kernels need: every GEMM tile reads 256 K values per
+// stage and covers 256 output columns, so K dimensions and per-expert weight rows are padded
+// to 256 (zero data, zero scales).
+struct Dims {
+  int64_t El, H, I, N1;
+  bool gated;
+  int64_t N1p;  // W1 rows per expert in the prepared layout
+  int64_t Hp;   // H padded to 256: GEMM1 K, and W2 rows per expert
+  int64_t Ip;   // I padded to 256: GEMM2 K
+};
+
+inline Dims make_dims(const moe_nvfp4_weights_t* w) {
+  Dims d;
+  d.El = w->num_local_experts;
+  d.H = w->hidden;
+  d.I = w->inter;
+  d.gated = w->activation == MOE_ACT_SWIGLU;
+  d.N1 = d.gated ? 2 * d.I : d.I;
+  d.N1p = roundup64(d.N1, kTileN);
+  d.Hp = roundup64(d.H, kTileK);
+  d.Ip = roundup64(d.I, kTileK);
+  return d;
+}
+
+inline size_t take(size_t& cursor, size_t bytes) {
+  const size_t at = cursor;
+  cursor = static_cast<size_t>(roundup64(static_cast<int64_t>(cursor + bytes), 256));
+  return at;
+}
+
+// Prepared weights: W1 data [El, N1p, H/2], W1 scale tiles [El][N1p/128][Hp/64][512],
+// W2 data [El, Hp, I/2], W2 scale tiles [El][Hp/128][Ip/64][512], alpha1 [El], alpha2 [El].
+struct PreparedLayout {
+  size_t w1, w1sf, w2, w2sf, a1, a2, total;
+};
+
+inline PreparedLayout prepared_layout(const Dims& d) {
+  PreparedLayout L;
+  size_t c = 0;
+  L.w1 = take(c, d.El * d.N1p * d.H / 2);
+  L.w1sf = take(c, d.El * d.N1p * d.Hp / 16);
+  L.w2 = take(c, d.El * d.Hp * d.I / 2);
+  L.w2sf = take(c, d.El * d.Hp * d.Ip / 16);
+  L.a1 = take(c, d.El * 4);
+  L.a2 = take(c, d.El * 4);
+  L.total = c;
+  return L;
+}
+
+// Forward workspace: permuted activations [cap, H/2] + scale tiles [cap/128][Hp/64][512],
+// intermediate [cap, I/2] + scale tiles [cap/128][Ip/64][512], and (finalize only) the
+// BF16 expert rows [cap, H].
+struct WorkspaceLayout {
+  size_t aq, asf, iq, isf, g, total;
+  int64_t cap;
+};
+
+inline int64_t plan_capacity_rows(int64_t M, int64_t top_k, int64_t El) {
+  const int64_t slots = M * top_k;
+  const int64_t segs = slots < El ? slots : El;
+  return roundup64(slots + (kSegAlign - 1) * segs, kSegAlign);
+}
+
+inline WorkspaceLayout workspace_layout(const Dims& d, int64_t M, int64_t top_k, bool finalize) {
+  WorkspaceLayout L;
+  L.cap = plan_capacity_rows(M, top_k, d.El);
+  size_t c = 0;
+  L.aq = take(c, L.cap * d.H / 2);
+  L.asf = take(c, L.cap * d.Hp / 16);
+  L.iq = take(c, L.cap * d.I / 2);
+  L.isf = take(c, L.cap * d.Ip / 16);
+  L.g = finalize ? take(c, L.cap * d.H * 2) : 0;
+  L.total = c;
+  return L;
+}
+
+// GEMM epilogue modes
+enum GemmMode : int {
+  kG1Fused = 0,   // activation + NVFP4 requant of the intermediate
+  kG1Preact = 1,  // FP32 pre-activations (test hook)
+  kG1Act = 2,     // BF16 intermediate (test hook)
+  kG2Rows = 3,    // BF16 expert rows
+};
+
+struct GemmLaunch {
+  int mode;
+  const uint8_t* a;      // [cap, K/2] packed rows in plan order
+  const uint8_t* a_sf;   // [cap/128][Kp/64][512]
+  const uint8_t* b;      // [El * Np, K/2]
+  const uint8_t* b_sf;   // [El][Np/128][Kp/64][512]
+  const float* alpha;    // [El]
+  const float* xs;       // per-token scale (GEMM1)
+  const int32_t* padded_offsets;
+  const int32_t* row_to_slot;
+  int64_t cap, El, K, Kp, N, Np;
+  int top_k, inter;
+  bool gated;
+  float g2;
+  void* out;
+  uint8_t* out_sf;
+  int32_t* dev_status;
+};
+
+moe_status_t launch_gemm(const GemmLaunch& g, cudaStream_t s);
+moe_status_t launch_permute(const int32_t* padded_offsets, int El, const int32_t* row_to_slot, int top_k,
+                            int64_t cap, const uint8_t* xq, const uint8_t* xsf, int H, uint8_t* aq, uint8_t* asf,
+                            cudaStream_t s);
+moe_status_t launch_finalize(const uint16_t* rows, const float* topk_weights, const int32_t* token_to_row, int M,
+                             int top_k, int H, uint16_t* out, cudaStream_t s);
+moe_status_t launch_prepare_matrix(const uint8_t* src, const uint8_t* src_sf, int E, int rows, int rows_p, int K,
+                                   int gated_inter, uint8_t* dst, uint8_t* dst_sf, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,263 @@
+// S2: expert-sorted routing plan (moe_sort), a stable counting sort of the routed slots.
+//
+// Sources: FlashInfer flashinfer.fused_moe.CudnnGroupedGemmNvfp4Config (rows permuted into
+// expert order, each expert segment padded to a multiple of 128 rows; non-local experts
+// masked; distinct topk_ids per token); Megatron-Core flashinfer_routed_nvfp4_moe (-1
+// routing entries contribute zero); FlashInfer flashinfer.fused_moe.FrostLowLatencyConfig
+// (expert ids outside [0, num_experts) mark unrouted slots).
+//
+// Slots s = t*top_k + j are placed in ascending s inside each segment. A block places 1024
+// slots per step: __match_any_sync groups the lanes of a warp that route to the same
+// expert (rank = lower lanes in the group), a 32 x El byte table holds each warp's count
+// per expert for the cross-warp prefix, and a per-expert cursor carries the running row.
+//  - one block (small inputs: one launch): histogram, scan, padding fill and placement;
+//  - several blocks (large inputs: three launches): per-block histograms, one scan block
+//    that turns them into per-block base rows, then per-block placement.
+#include "common.cuh"
+#include "host_util.h"
+
+namespace moe {
+namespace {
+
+constexpr int kPlanThreads = 1024;
+constexpr int kSlotsPerBlock = 2048;
+
+struct PlanSmem {
+  int cnt[kMaxLocalExperts];
+  int cursor[kMaxLocalExperts + 1];
+  uint8_t warp_cnt[32][kMaxLocalExperts];
+};
+
+__device__ __forceinline__ int local_of(int id, int off, int El) {
+  const int l = id - off;
+  return (l >= 0 && l < El) ? l : -1;
+}
+
+// exclusive scan of roundup(cnt[l], 128) by warp 0 into cursor[0..El] (cursor[El] = total)
+__device__ void scan_padded(PlanSmem& sm, int El) {
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
+  const int per = (El + 31) / 32;
+  int sum = 0;
+  for (int i = 0; i < per; ++i) {
+    const int l = lane * per + i;
+    if (l < El) sum += (sm.cnt[l] + kSegAlign - 1) / kSegAlign * kSegAlign;
+  }
+  int incl = sum;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += n;
+  }
+  int run = incl - sum;
+  for (int i = 0; i < per; ++i) {
+    const int l = lane * per + i;
+    if (l < El) {
+      sm.cursor[l] = run;
+      run += (sm.cnt[l] + kSegAlign - 1) / kSegAlign * kSegAlign;
+    }
+  }
+  if (lane == 31) sm.cursor[El] = incl;
+}
+
+// row_to_slot = -1 on the padding rows of every segment and on [total, capacity)
+__device__ void fill_padding(const int* start, const int* cnt, int El, int total, int64_t cap,
+                             int32_t* row_to_slot) {
+  for (int l = threadIdx.x; l < El; l += blockDim.x) {
+    const int b = start[l] + cnt[l];
+    const int e = start[l] + (cnt[l] + kSegAlign - 1) / kSegAlign * kSegAlign;
+    for (int p = b; p < e; ++p) row_to_slot[p] = -1;
+  }
+  for (int64_t p = total + threadIdx.x; p < cap; p += blockDim.x) row_to_slot[p] = -1;
+}
+
+// place slots [begin, end) in order; sm.cursor[l] holds the first free row of expert l
+__device__ void place_range(const int32_t* __restrict__ ids, int64_t begin, int64_t end, int top_k, int off, int El,
+                            PlanSmem& sm, int32_t* __restrict__ row_to_slot, int32_t* __restrict__ token_to_row,
+                            int32_t* dev_status) {
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  for (int64_t base = begin; base < end; base += kPlanThreads) {
+    const int64_t s = base + tid;
+    int l = -1;
+    if (s < end) {
+      const int id = ids[s];
+      l = local_of(id, off, El);
+      if (l >= 0) {
+        const int64_t t0 = s - s % top_k;
+        for (int64_t q = t0; q < s; ++q)
+          if (ids[q] == id) atomicOr(dev_status, MOE_DEV_DUPLICATE_EXPERT);
+      } else {
+        token_to_row[s] = -1;
+      }
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, l);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    const bool leader = l >= 0 && rank == 0;
+    if (leader) sm.warp_cnt[w][l] = static_cast<uint8_t>(__popc(peers));
+    __syncthreads();
+    if (l >= 0) {
+      int prefix = 0;
+      for (int ww = 0; ww < w; ++ww) prefix += sm.warp_cnt[ww][l];
+      const int row = sm.cursor[l] + prefix + rank;
+      row_to_slot[row] = static_cast<int32_t>(s);
+      token_to_row[s] = row;
+    }
+    __syncthreads();
+    if (leader) {
+      atomicAdd(&sm.cursor[l], __popc(peers));
+      sm.warp_cnt[w][l] = 0;
+    }
+    __syncthreads();
+  }
+}
+
+__device__ void zero_tables(PlanSmem& sm, int El) {
+  for (int i = threadIdx.x; i < El; i += blockDim.x) sm.cnt[i] = 0;
+  for (int i = threadIdx.x; i < 32 * kMaxLocalExperts; i += blockDim.x) (&sm.warp_cnt[0][0])[i] = 0;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_single_kernel(
+    const int32_t* __restrict__ ids, int64_t n, int top_k, int off, int El, int64_t cap, int32_t* __restrict__ counts,
+    int32_t* __restrict__ padded_offsets, int32_t* __restrict__ row_to_slot, int32_t* __restrict__ token_to_row,
+    int32_t* dev_status) {
+  __shared__ PlanSmem sm;
+  zero_tables(sm, El);
+  __syncthreads();
+  for (int64_t s = threadIdx.x; s < n; s += blockDim.x) {
+    const int l = local_of(ids[s], off, El);
+    if (l >= 0) atomicAdd(&sm.cnt[l], 1);
+  }
+  __syncthreads();
+  scan_padded(sm, El);
+  __syncthreads();
+  for (int l = threadIdx.x; l <= El; l += blockDim.x) {
+    padded_offsets[l] = sm.cursor[l];
+    if (l < El) counts[l] = sm.cnt[l];
+  }
+  fill_padding(sm.cursor, sm.cnt, El, sm.cursor[El], cap, row_to_slot);
+  __syncthreads();
+  place_range(ids, 0, n, top_k, off, El, sm, row_to_slot, token_to_row, dev_status);
+}
+
+// per-block histograms: hist[b * El + l]
+__global__ void __launch_bounds__(kPlanThreads) plan_hist_kernel(const int32_t* __restrict__ ids, int64_t n, int off,
+                                                                 int El, int32_t* __restrict__ hist) {
+  __shared__ int cnt[kMaxLocalExperts];
+  for (int i = threadIdx.x; i < El; i += blockDim.x) cnt[i] = 0;
+  __syncthreads();
+  const int64_t b0 = static_cast<int64_t>(blockIdx.x) * kSlotsPerBlock;
+  const int64_t b1 = min(n, b0 + kSlotsPerBlock);
+  for (int64_t s = b0 + threadIdx.x; s < b1; s += blockDim.x) {
+    const int l = local_of(ids[s], off, El);
+    if (l >= 0) atomicAdd(&cnt[l], 1);
+  }
+  __syncthreads();
+  for (int l = threadIdx.x; l < El; l += blockDim.x) hist[static_cast<int64_t>(blockIdx.x) * El + l] = cnt[l];
+}
+
+// one block: counts, padded offsets, per-block base rows (in place over hist), padding fill
+__global__ void __launch_bounds__(kPlanThreads) plan_scan_kernel(int32_t* __restrict__ hist, int nb, int El,
+                                                                 int64_t cap, int32_t* __restrict__ counts,
+                                                                 int32_t* __restrict__ padded_offsets,
+                                                                 int32_t* __restrict__ row_to_slot) {
+  __shared__ PlanSmem sm;
+  for (int l = threadIdx.x; l < El; l += blockDim.x) {
+    int run = 0;
+    for (int b = 0; b < nb; ++b) {
+      const int h = hist[static_cast<int64_t>(b) * El + l];
+      hist[static_cast<int64_t>(b) * El + l] = run;
+      run += h;
+    }
+    sm.cnt[l] = run;
+  }
+  __syncthreads();
+  scan_padded(sm, El);
+  __syncthreads();
+  for (int l = threadIdx.x; l <= El; l += blockDim.x) {
+    padded_offsets[l] = sm.cursor[l];
+    if (l < El) {
+      counts[l] = sm.cnt[l];
+      for (int b = 0; b < nb; ++b) hist[static_cast<int64_t>(b) * El + l] += sm.cursor[l];
+    }
+  }
+  fill_padding(sm.cursor, sm.cnt, El, sm.cursor[El], cap, row_to_slot);
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_place_kernel(const int32_t* __restrict__ ids, int64_t n,
+                                                                  int top_k, int off, int El,
+                                                                  const int32_t* __restrict__ base,
+                                                                  int32_t* __restrict__ row_to_slot,
+                                                                  int32_t* __restrict__ token_to_row,
+                                                                  int32_t* dev_status) {
+  __shared__ PlanSmem sm;
+  for (int i = threadIdx.x; i < 32 * kMaxLocalExperts; i += blockDim.x) (&sm.warp_cnt[0][0])[i] = 0;
+  for (int l = threadIdx.x; l < El; l += blockDim.x) sm.cursor[l] = base[static_cast<int64_t>(blockIdx.x) * El + l];
+  __syncthreads();
+  const int64_t b0 = static_cast<int64_t>(blockIdx.x) * kSlotsPerBlock;
+  const int64_t b1 = min(n, b0 + kSlotsPerBlock);
+  place_range(ids, b0, b1, top_k, off, El, sm, row_to_slot, token_to_row, dev_status);
+}
+
+int64_t plan_blocks(int64_t n) { return (n + kSlotsPerBlock - 1) / kSlotsPerBlock; }
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" size_t moe_plan_capacity(int32_t M, int32_t top_k, int32_t num_local_experts) {
+  if (M < 0 || top_k <= 0 || num_local_experts <= 0) return 0;
+  const int64_t slots = static_cast<int64_t>(M) * top_k;
+  const int64_t segs = slots < num_local_experts ? slots : num_local_experts;
+  return static_cast<size_t>(roundup64(slots + (kSegAlign - 1) * segs, kSegAlign));
+}
+
+extern "C" size_t moe_plan_workspace_bytes(int32_t M, int32_t top_k, int32_t num_local_experts) {
+  if (M < 0 || top_k <= 0 || num_local_experts <= 0) return 0;
+  const int64_t n = static_cast<int64_t>(M) * top_k;
+  const int64_t nb = plan_blocks(n);
+  if (nb <= 1) return 0;
+  return static_cast<size_t>(roundup64(nb * num_local_experts * 4, 256));
+}
+
+extern "C" moe_status_t moe_plan(const int32_t* topk_ids, int32_t M, int32_t top_k, int32_t num_experts,
+                                 int32_t local_expert_offset, int32_t num_local_experts, int32_t* counts,
+                                 int32_t* padded_offsets, int32_t* row_to_slot, int32_t* token_to_row,
+                                 void* workspace, size_t workspace_bytes, int32_t* dev_status, moe_stream_t stream) {
+  MOE_CHECK(M >= 0 && top_k >= 1 && num_local_experts >= 1 && num_experts >= 1, MOE_ERR_INVALID_ARGUMENT);
+  MOE_CHECK(local_expert_offset >= 0 && local_expert_offset + num_local_experts <= num_experts,
+            MOE_ERR_INVALID_ARGUMENT);
+  MOE_CHECK(num_local_experts <= kMaxLocalExperts, MOE_ERR_UNSUPPORTED_SHAPE);
+  MOE_CHECK(static_cast<int64_t>(M) * top_k < (int64_t(1) << 30), MOE_ERR_UNSUPPORTED_SHAPE);
+  MOE_CHECK(counts && padded_offsets && dev_status, MOE_ERR_INVALID_ARGUMENT);
+  MOE_CHECK(aligned16(counts) && aligned16(padded_offsets) && aligned16(dev_status), MOE_ERR_MISALIGNED);
+  const int64_t n = static_cast<int64_t>(M) * top_k;
+  const int64_t cap = static_cast<int64_t>(moe_plan_capacity(M, top_k, num_local_experts));
+  if (n > 0) {
+    MOE_CHECK(topk_ids && row_to_slot && token_to_row, MOE_ERR_INVALID_ARGUMENT);
+    MOE_CHECK(aligned16(topk_ids) && aligned16(row_to_slot) && aligned16(token_to_row), MOE_ERR_MISALIGNED);
+  }
+  const size_t need = moe_plan_workspace_bytes(M, top_k, num_local_experts);
+  MOE_CHECK(workspace_bytes >= need, MOE_ERR_WORKSPACE_TOO_SMALL);
+  if (need) {
+    MOE_CHECK(workspace != nullptr, MOE_ERR_INVALID_ARGUMENT);
+    MOE_CHECK(aligned16(workspace), MOE_ERR_MISALIGNED);
+  }
+  cudaStream_t s = as_stream(stream);
+  const int64_t nb = plan_blocks(n);
+  const int off = local_expert_offset, El = num_local_experts;
+  if (nb <= 1) {
+    plan_single_kernel<<<1, kPlanThreads, 0, s>>>(topk_ids, n, top_k, off, El, cap, counts, padded_offsets,
+                                                  row_to_slot, token_to_row, dev_status);
+    return launch_status();
+  }
+  int32_t* hist = static_cast<int32_t*>(workspace);
+  plan_hist_kernel<<<static_cast<unsigned>(nb), kPlanThreads, 0, s>>>(topk_ids, n, off, El, hist);
+  MOE_CHECK(launch_status() == MOE_OK, MOE_ERR_CUDA);
+  plan_scan_kernel<<<1, kPlanThreads, 0, s>>>(hist, static_cast<int>(nb), El, cap, counts, padded_offsets,
+                                              row_to_slot);
+  MOE_CHECK(launch_status() == MOE_OK, MOE_ERR_CUDA);
+  plan_place_kernel<<<static_cast<unsigned>(nb), kPlanThreads, 0, s>>>(topk_ids, n, top_k, off, El, hist,
+                                                                       row_to_slot, token_to_row, dev_status);
+  return launch_status();
+}

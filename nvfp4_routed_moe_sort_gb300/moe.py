@@ -1,0 +1,112 @@
+"""User-facing wrapper: owns the capacity-sized buffers and chains the C-ABI calls.
+
+``NVFP4RoutedMoE.forward`` runs moe_quantize_input -> moe_plan ->
+moe_grouped_fp4_forward on torch's current stream; every step runs in the
+library's kernels. torch only allocates device memory (once per batch shape)
+and supplies the stream.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _lib as L
+
+
+def quantize_weights(w_bf16: torch.Tensor):
+    """BF16 expert stack [E, rows, cols] -> (data [E, rows, cols/2] u8, sf [E, rows, cols/16] u8,
+    alpha [E] f32) with one FP32 global scale per expert (moe_quantize_weights)."""
+    E, R, C = w_bf16.shape
+    dev = w_bf16.device
+    data = torch.empty(E, R, C // 2, dtype=torch.uint8, device=dev)
+    sf = torch.empty(E, R, C // 16, dtype=torch.uint8, device=dev)
+    alpha = torch.empty(E, dtype=torch.float32, device=dev)
+    scratch = torch.empty(E, dtype=torch.float32, device=dev)
+    L.moe_quantize_weights(w_bf16.contiguous().view(torch.int16), data, sf, alpha, scratch)
+    return data, sf, alpha
+
+
+class NVFP4RoutedMoE:
+    """Routed-MoE expert layer on NVFP4 weights (linear boundary layout, on the GPU)."""
+
+    def __init__(self, w1, w1_sf, w1_alpha, w2, w2_sf, w2_alpha, activation: str = "swiglu",
+                 num_experts: int | None = None, local_expert_offset: int = 0,
+                 fc2_input_scale: float = 1.0, scale_mode: str = "per_token"):
+        El, N1, Hh = w1.shape
+        self.El = El
+        self.H = Hh * 2
+        self.I = w2.shape[2] * 2
+        self.act = L.MOE_ACT_SWIGLU if activation == "swiglu" else L.MOE_ACT_RELU2
+        self.num_experts = num_experts if num_experts is not None else El + local_expert_offset
+        self.local_expert_offset = local_expert_offset
+        self.fc2_input_scale = float(fc2_input_scale)
+        self.scale_mode = L.MOE_SCALE_PER_TOKEN if scale_mode == "per_token" else L.MOE_SCALE_GLOBAL_ONE
+        self.device = w1.device
+        self.linear = (w1, w1_sf, w1_alpha, w2, w2_sf, w2_alpha)
+        self.w = L.make_weights(El, self.H, self.I, self.act, w1, w1_sf, w1_alpha, w2, w2_sf, w2_alpha)
+        nbytes = L.moe_prepared_weights_bytes(self.w)
+        self.prepared = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+        L.moe_prepare_weights(self.w, self.prepared)
+        self._bufs = {}
+
+    def refresh(self):
+        """Re-prepare from the (updated) linear weights into the same buffer."""
+        L.moe_prepare_weights(self.w, self.prepared)
+
+    def buffers(self, M: int, top_k: int, do_finalize: bool) -> dict:
+        key = (M, top_k, bool(do_finalize))
+        if key in self._bufs:
+            return self._bufs[key]
+        dev = self.device
+        cap = L.moe_plan_capacity(M, top_k, self.El)
+        b = {
+            "xq": torch.empty(M, self.H // 2, dtype=torch.uint8, device=dev),
+            "xsf": torch.empty(M, self.H // 16, dtype=torch.uint8, device=dev),
+            "xs": torch.empty(M, dtype=torch.float32, device=dev),
+            "counts": torch.empty(self.El, dtype=torch.int32, device=dev),
+            "padded_offsets": torch.empty(self.El + 1, dtype=torch.int32, device=dev),
+            "row_to_slot": torch.empty(max(cap, 1), dtype=torch.int32, device=dev),
+            "token_to_row": torch.empty(M, top_k, dtype=torch.int32, device=dev),
+            "plan_ws": torch.empty(max(L.moe_plan_workspace_bytes(M, top_k, self.El), 16),
+                                   dtype=torch.uint8, device=dev),
+            "ws": torch.empty(max(L.moe_forward_workspace_bytes(M, top_k, self.w, do_finalize), 16),
+                              dtype=torch.uint8, device=dev),
+            "dev_status": torch.zeros(4, dtype=torch.int32, device=dev),
+            "out": torch.empty(M, self.H, dtype=torch.bfloat16, device=dev) if do_finalize else None,
+            "gemm2_out": None if do_finalize else torch.empty(max(cap, 1), self.H, dtype=torch.bfloat16,
+                                                              device=dev),
+            "capacity": cap,
+        }
+        self._bufs[key] = b
+        return b
+
+    def quantize(self, x: torch.Tensor, b: dict):
+        L.moe_quantize_input(x.view(torch.int16), self.scale_mode, b["xq"], b["xsf"], b["xs"])
+
+    def plan(self, topk_ids: torch.Tensor, b: dict):
+        L.moe_plan(topk_ids, self.num_experts, self.local_expert_offset, self.El, b["counts"],
+                   b["padded_offsets"], b["row_to_slot"], b["token_to_row"], b["plan_ws"], b["dev_status"])
+
+    def experts(self, topk_weights: torch.Tensor, b: dict, do_finalize: bool, step_events=None):
+        L.moe_grouped_fp4_forward(b["padded_offsets"], b["row_to_slot"], b["token_to_row"], b["xq"], b["xsf"],
+                                  b["xs"], self.w, self.prepared, topk_weights, self.fc2_input_scale,
+                                  do_finalize, b["out"], b["gemm2_out"], b["ws"], b["dev_status"],
+                                  step_events=step_events)
+
+    def forward(self, x: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor,
+                do_finalize: bool = True, step_events=None):
+        """x [M, H] bf16, topk_ids [M, k] int32, topk_weights [M, k] f32 (all on the GPU).
+
+        Returns out [M, H] bf16, or (gemm2_out [capacity, H], topk_weights, token_to_row)
+        when do_finalize is False. The returned tensors are the layer's reusable buffers.
+        """
+        M, k = topk_ids.shape
+        b = self.buffers(M, k, do_finalize)
+        self.quantize(x, b)
+        self.plan(topk_ids, b)
+        self.experts(topk_weights, b, do_finalize, step_events)
+        if do_finalize:
+            return b["out"]
+        return b["gemm2_out"], topk_weights, b["token_to_row"]
+
+    def device_status(self, M: int, top_k: int, do_finalize: bool) -> int:
+        return int(self.buffers(M, top_k, do_finalize)["dev_status"][0].item())
