@@ -145,13 +145,16 @@ def setup_gpu(cfg, dev):
     d2 = torch.empty(El, cfg.H, cfg.I // 2, dtype=torch.uint8, device=dev)
     s2 = torch.empty(El, cfg.H, cfg.I // 16, dtype=torch.uint8, device=dev)
     a2 = torch.empty(El, dtype=torch.float32, device=dev)
-    scratch = torch.empty(1, dtype=torch.float32, device=dev)
+    scratch = torch.empty(4, dtype=torch.float32, device=dev)
+    alpha = torch.empty(4, dtype=torch.float32, device=dev)   # 16-byte aligned per-call output
     for l in range(El):
         w1 = mi.expert_w1_bf16(cfg, l, dev)
-        pkg.moe_quantize_weights(w1.view(torch.int16)[None], d1[l:l + 1], s1[l:l + 1], a1[l:l + 1], scratch)
+        pkg.moe_quantize_weights(w1.view(torch.int16)[None], d1[l:l + 1], s1[l:l + 1], alpha, scratch)
+        a1[l] = alpha[0]
         del w1
         w2 = mi.expert_w2_bf16(cfg, l, dev)
-        pkg.moe_quantize_weights(w2.view(torch.int16)[None], d2[l:l + 1], s2[l:l + 1], a2[l:l + 1], scratch)
+        pkg.moe_quantize_weights(w2.view(torch.int16)[None], d2[l:l + 1], s2[l:l + 1], alpha, scratch)
+        a2[l] = alpha[0]
         del w2
     layer = pkg.NVFP4RoutedMoE(d1, s1, a1, d2, s2, a2, activation=cfg.act, num_experts=cfg.E,
                                local_expert_offset=cfg.local_offset, fc2_input_scale=cfg.fc2_input_scale,
@@ -194,6 +197,10 @@ def run_gpu(args, cfg, rank, world):
     n_ev = 8
     K, W = args.steps, args.warmup
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(K + W)]
+    for row in evs:          # torch creates the CUDA event on its first record
+        for e in row:
+            e.record()
+    torch.cuda.synchronize()
 
     def step(e):
         e[0].record()

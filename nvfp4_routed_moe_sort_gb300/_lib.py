@@ -173,7 +173,10 @@ def moe_grouped_fp4_forward(padded_offsets, row_to_slot, token_to_row, xq, xsf, 
     ev = None
     nev = 0
     if step_events:
-        ev = (c_void_p * len(step_events))(*[e.cuda_event for e in step_events])
+        handles = [e.cuda_event for e in step_events]
+        if not all(handles):
+            raise MoEError("step_events: torch creates an event on its first record(); record each once first")
+        ev = (c_void_p * len(step_events))(*handles)
         nev = len(step_events)
     _check(lib().moe_grouped_fp4_forward(
         _ptr(padded_offsets), _ptr(row_to_slot), _ptr(token_to_row), M, k, _ptr(xq), _ptr(xsf), _ptr(xs),
