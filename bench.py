@@ -269,7 +269,7 @@ def run_gpu(args, cfg, rank, world):
     roof["traffic"] = traffic_from_profiles(dom, cfg.name)
     step_roof_s = max(stepw["bytes"] / (peaks["hbm_gbs"] * 1e9), stepw["flops"] / (fp4_peak * 1e12))
     # end to end through the public API with host buffers
-    e2e = run_e2e(layer, x, ids, tw, dev, max(3, min(K, 50)))
+    e2e = None if args.no_e2e else run_e2e(layer, x, ids, tw, dev, max(3, min(K, 50)))
     launches_per_step = 6 + (2 if M * k > 2048 else 0)
     res = {
         "metric": METRIC, "value": world * M / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world, "steps": K,
@@ -436,10 +436,19 @@ def main():
     ap.add_argument("--workload", default="decode_t8", choices=sorted(mi.CONFIGS))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer run (profiling)")
+    ap.add_argument("--set", action="append", default=[], metavar="FIELD=VALUE",
+                    help="override a workload field (e.g. E=64 M=1024) for smaller profiling cases")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     cfg = mi.CONFIGS[args.workload]
+    for kv in args.set:
+        k_, v_ = kv.split("=", 1)
+        cur = getattr(cfg, k_)
+        cfg = cfg.with_(**{k_: type(cur)(v_) if cur is not None else int(v_)})
+    if args.set:
+        cfg = cfg.with_(name=cfg.name + "[" + ",".join(args.set) + "]")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
