@@ -144,6 +144,30 @@ MOE_API moe_status_t moe_plan(const int32_t* topk_ids, int32_t M, int32_t top_k,
                       moe_stream_t stream);
 
 /* ----------------------------------------------------------------------------------------
+ * moe_plan_noalloc - the pages have no counterpart of this call; it exists for callers of
+ * this library that cannot allocate device memory: runtimes that hand out all device memory
+ * from one pool reserved at start-up, C hosts with no device allocator, or code that must
+ * not call cudaMalloc because it would synchronise the device mid-stream.
+ * It computes exactly what moe_plan computes, with the same arguments minus the workspace:
+ * the histogram scratch of the multi-block plan lives in a fixed array of
+ * MOE_PLAN_NOALLOC_SCRATCH_BYTES of the library's own device memory, which every GPU that
+ * loads the library holds until the process exits. The call allocates nothing.
+ *  - Size limit: ceil(M * top_k / 2048) * num_local_experts * 4 bytes must not exceed
+ *    MOE_PLAN_NOALLOC_SCRATCH_BYTES (inputs of at most 2048 slots need no scratch at all);
+ *    larger inputs are rejected with MOE_ERR_UNSUPPORTED_SHAPE before anything runs.
+ *  - The first call on each device looks up the array's device address on that device
+ *    (cudaGetSymbolAddress) and caches it; make that first call before any stream capture.
+ *  - Every call on a device shares the one array and leaves its contents behind; nothing in
+ *    it must start at zero, but calls that overlap on the GPU (other streams, other host
+ *    threads) race on it and must be serialised by the caller.
+ * ---------------------------------------------------------------------------------------- */
+#define MOE_PLAN_NOALLOC_SCRATCH_BYTES (1 << 20)
+MOE_API moe_status_t moe_plan_noalloc(const int32_t* topk_ids, int32_t M, int32_t top_k, int32_t num_experts,
+                              int32_t local_expert_offset, int32_t num_local_experts, int32_t* counts,
+                              int32_t* padded_offsets, int32_t* row_to_slot, int32_t* token_to_row,
+                              int32_t* dev_status, moe_stream_t stream);
+
+/* ----------------------------------------------------------------------------------------
  * Weight preparation (off the timed path).
  *
  * moe_quantize_weights - [MCORE] _global_encode_scale / _quantize_expert: one FP32 global

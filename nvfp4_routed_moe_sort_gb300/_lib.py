@@ -23,8 +23,9 @@ EXPORTED = [
     "moe_status_string", "moe_abi_version", "moe_quantize_input", "moe_plan_capacity",
     "moe_plan_workspace_bytes", "moe_plan", "moe_quantize_weights", "moe_prepared_weights_bytes",
     "moe_prepare_weights", "moe_forward_workspace_bytes", "moe_forward_workspace_layout",
-    "moe_grouped_fp4_forward", "moe_finalize", "moe_debug_gemm1",
+    "moe_grouped_fp4_forward", "moe_finalize", "moe_debug_gemm1", "moe_plan_noalloc",
 ]
+MOE_PLAN_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 
 class MoEError(RuntimeError):
@@ -51,6 +52,7 @@ def _declare(lib):
         "moe_plan_workspace_bytes": (c_size_t, [c_int32, c_int32, c_int32]),
         "moe_plan": (c_int32, [P, c_int32, c_int32, c_int32, c_int32, c_int32, P, P, P, P, P, c_size_t,
                                P, P]),
+        "moe_plan_noalloc": (c_int32, [P, c_int32, c_int32, c_int32, c_int32, c_int32, P, P, P, P, P, P]),
         "moe_quantize_weights": (c_int32, [P, c_int32, c_int32, c_int32, P, P, P, P, P]),
         "moe_prepared_weights_bytes": (c_size_t, [ctypes.POINTER(WeightsT)]),
         "moe_prepare_weights": (c_int32, [ctypes.POINTER(WeightsT), P, c_size_t, P]),
@@ -138,6 +140,16 @@ def moe_plan(topk_ids, num_experts, local_expert_offset, num_local_experts, coun
     _check(lib().moe_plan(_ptr(topk_ids), M, k, num_experts, local_expert_offset, num_local_experts,
                           _ptr(counts), _ptr(padded_offsets), _ptr(row_to_slot), _ptr(token_to_row),
                           _ptr(workspace), wsb, _ptr(dev_status), _stream(stream)), "moe_plan")
+
+
+def moe_plan_noalloc(topk_ids, num_experts, local_expert_offset, num_local_experts, counts, padded_offsets,
+                     row_to_slot, token_to_row, dev_status, stream=None):
+    """moe_plan without a workspace, for callers that cannot allocate device memory (its
+    histogram scratch is a fixed 1 MiB array inside the library; see the C header)."""
+    M, k = topk_ids.shape
+    _check(lib().moe_plan_noalloc(_ptr(topk_ids), M, k, num_experts, local_expert_offset, num_local_experts,
+                                  _ptr(counts), _ptr(padded_offsets), _ptr(row_to_slot), _ptr(token_to_row),
+                                  _ptr(dev_status), _stream(stream)), "moe_plan_noalloc")
 
 
 def moe_quantize_weights(w, data, sf, alpha, amax_scratch, stream=None):

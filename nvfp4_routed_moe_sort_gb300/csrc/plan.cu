@@ -261,3 +261,90 @@ extern "C" moe_status_t moe_plan(const int32_t* topk_ids, int32_t M, int32_t top
                                                                        row_to_slot, token_to_row, dev_status);
   return launch_status();
 }
+
+// ---------------------------------------------------------------------------------------
+// moe_plan_noalloc: the same plan for callers that cannot hand the library device scratch.
+//
+// Some callers never allocate device memory after start-up: serving runtimes that carve
+// all memory from one up-front pool, C hosts without a device allocator of their own, or
+// code that must not call cudaMalloc because it would synchronise the device in the middle
+// of a stream's work. For them the per-block expert histograms of the multi-block plan
+// live in a fixed array in the library's own device memory instead of a workspace.
+//
+// The array is file-scope device memory, so every GPU that loads the library holds it
+// (MOE_PLAN_NOALLOC_SCRATCH_BYTES) until the process exits. In host code its name is only
+// a host-side stand-in: the kernels are given the device address that
+// cudaGetSymbolAddress returns, looked up once per device on that device's first call and
+// cached. All calls on a device share the array and it keeps the last call's contents;
+// nothing in it has to start at zero (each call writes every histogram entry it later
+// reads), but calls that overlap on the GPU (two streams, or two threads) race on it.
+// ---------------------------------------------------------------------------------------
+#include <mutex>
+
+namespace moe {
+namespace {
+
+constexpr int64_t kNoAllocScratchInts = MOE_PLAN_NOALLOC_SCRATCH_BYTES / 4;
+static __device__ __align__(256) int32_t g_plan_noalloc_scratch[kNoAllocScratchInts];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+int32_t* g_noalloc_ptr[kMaxDevices] = {};
+
+// device address of the scratch array on the current device (looked up on first use)
+moe_status_t noalloc_scratch(int32_t** out) {
+  int dev = -1;
+  MOE_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_plan_noalloc_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
+    g_noalloc_ptr[dev] = static_cast<int32_t*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status_t moe_plan_noalloc(const int32_t* topk_ids, int32_t M, int32_t top_k, int32_t num_experts,
+                                         int32_t local_expert_offset, int32_t num_local_experts, int32_t* counts,
+                                         int32_t* padded_offsets, int32_t* row_to_slot, int32_t* token_to_row,
+                                         int32_t* dev_status, moe_stream_t stream) {
+  MOE_CHECK(M >= 0 && top_k >= 1 && num_local_experts >= 1 && num_experts >= 1, MOE_ERR_INVALID_ARGUMENT);
+  MOE_CHECK(local_expert_offset >= 0 && local_expert_offset + num_local_experts <= num_experts,
+            MOE_ERR_INVALID_ARGUMENT);
+  MOE_CHECK(num_local_experts <= kMaxLocalExperts, MOE_ERR_UNSUPPORTED_SHAPE);
+  MOE_CHECK(static_cast<int64_t>(M) * top_k < (int64_t(1) << 30), MOE_ERR_UNSUPPORTED_SHAPE);
+  const int64_t n = static_cast<int64_t>(M) * top_k;
+  const int64_t nb = plan_blocks(n);
+  // the histograms must fit the fixed array
+  MOE_CHECK(nb <= 1 || nb * num_local_experts <= kNoAllocScratchInts, MOE_ERR_UNSUPPORTED_SHAPE);
+  MOE_CHECK(counts && padded_offsets && dev_status, MOE_ERR_INVALID_ARGUMENT);
+  MOE_CHECK(aligned16(counts) && aligned16(padded_offsets) && aligned16(dev_status), MOE_ERR_MISALIGNED);
+  if (n > 0) {
+    MOE_CHECK(topk_ids && row_to_slot && token_to_row, MOE_ERR_INVALID_ARGUMENT);
+    MOE_CHECK(aligned16(topk_ids) && aligned16(row_to_slot) && aligned16(token_to_row), MOE_ERR_MISALIGNED);
+  }
+  int32_t* hist = nullptr;
+  moe_status_t st = noalloc_scratch(&hist);
+  if (st != MOE_OK) return st;
+  const int64_t cap = static_cast<int64_t>(moe_plan_capacity(M, top_k, num_local_experts));
+  cudaStream_t s = as_stream(stream);
+  const int off = local_expert_offset, El = num_local_experts;
+  if (nb <= 1) {
+    plan_single_kernel<<<1, kPlanThreads, 0, s>>>(topk_ids, n, top_k, off, El, cap, counts, padded_offsets,
+                                                  row_to_slot, token_to_row, dev_status);
+    return launch_status();
+  }
+  plan_hist_kernel<<<static_cast<unsigned>(nb), kPlanThreads, 0, s>>>(topk_ids, n, off, El, hist);
+  MOE_CHECK(launch_status() == MOE_OK, MOE_ERR_CUDA);
+  plan_scan_kernel<<<1, kPlanThreads, 0, s>>>(hist, static_cast<int>(nb), El, cap, counts, padded_offsets,
+                                              row_to_slot);
+  MOE_CHECK(launch_status() == MOE_OK, MOE_ERR_CUDA);
+  plan_place_kernel<<<static_cast<unsigned>(nb), kPlanThreads, 0, s>>>(topk_ids, n, top_k, off, El, hist,
+                                                                       row_to_slot, token_to_row, dev_status);
+  return launch_status();
+}
