@@ -255,7 +255,7 @@ extern "C" moe_status_t moe_grouped_fp4_forward(const int32_t* padded_offsets, c
   g2.Np = d.Hp;
   g2.top_k = top_k;
   g2.inter = static_cast<int>(d.I);
-  g2.gated = d.gated;
+  g2.gated = false;  // GEMM2 columns are plain output columns
   g2.g2 = fc2_input_scale;
   g2.out = rows_out;
   g2.out_sf = nullptr;

@@ -8,15 +8,18 @@
 // FlashInfer flashinfer.fused_moe.alphamoe_nvfp4_aligned_moe (capacity-sized grid that
 // skips work past the device-side valid extent).
 //
-// One persistent CTA per SM, 192 threads:
+// One persistent CTA per SM, 320 threads:
 //   warp 0       producer: per stage, two 2D TMA tile loads (A: 128 rows x 128 B, B: 256
 //                rows x 128 B, 128-byte swizzle) and three 2 KB bulk copies of 128x4 scale
 //                tiles, all completing on the stage's full barrier;
 //   warp 1       TMEM owner and MMA issuer: per stage, 12 tcgen05.cp of scale tiles into
 //                TMEM and 8 tcgen05.mma.kind::mxf4nvf4 (M=128, N=128, K=64, E2M1 x E2M1
 //                with UE4M3 scales per 16 values, FP32 accumulation in TMEM);
-//   warps 2..5   epilogue: TMEM -> registers (tcgen05.ld), scaling, activation and NVFP4
-//                requantisation (GEMM1) or BF16 rows (GEMM2), stores to global memory.
+//   warps 2..9   epilogue: two warps per TMEM lane quarter, one per column half; each pulls
+//                its 128 accumulator columns into registers (tcgen05.ld) and releases the
+//                accumulator at once, so the next tile's MMAs overlap its scaling,
+//                activation and NVFP4 requantisation (GEMM1) or BF16 rows (GEMM2); warps
+//                whose 32 rows are all padding skip the arithmetic.
 // A work unit is (expert e, 256-column tile nt, 128-row tile mi); units are numbered
 // expert-major, then column tile, then row tile, so CTAs running side by side share an
 // expert's weight tiles in L2. The unit count comes from padded_offsets on the device.
@@ -45,7 +48,8 @@ constexpr uint32_t kStageTx = kStageBytes;
 constexpr int kTmemCols = 512;
 constexpr int kSfCol0 = 256;
 constexpr int kSfColsPerStage = 48;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // producer, MMA, 8 epilogue warps
+constexpr int kEpiThreads = 256;
 constexpr int kSmemExtra = 1024 /*align*/ + 256 /*barriers*/;
 
 static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
@@ -108,103 +112,110 @@ __device__ __forceinline__ uint32_t requant32_store(const float* h, float g2, ui
   return q0 | (q1 << 8);
 }
 
+// Pull this thread's 128 accumulator columns into registers, then hand the accumulator
+// back to the MMA warp so the next tile's MMAs overlap this epilogue's arithmetic.
+// Thread (lane quarter q, half h) owns TMEM lane 32q + lane and, for a gated GEMM1, gate
+// columns [64h, 64h+64) plus the matching up columns [128+64h, ...); otherwise the columns
+// [128h, 128h+128).
 template <int MODE>
-__device__ __forceinline__ void epilogue_unit(const GemmParams& p, uint32_t tmem_row, int e, int nt, int64_t prow,
-                                              int slot) {
+__device__ __forceinline__ void load_acc(const GemmParams& p, uint32_t tmem_row, int half, uint32_t* r,
+                                         uint64_t* acc_empty) {
+  if (MODE != kG2Rows && p.gated) {
+    tmem_ld32_issue(tmem_row + half * 64, r);
+    tmem_ld32_issue(tmem_row + half * 64 + 32, r + 32);
+    tmem_ld32_issue(tmem_row + 128 + half * 64, r + 64);
+    tmem_ld32_issue(tmem_row + 128 + half * 64 + 32, r + 96);
+  } else {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) tmem_ld32_issue(tmem_row + half * 128 + c * 32, r + 32 * c);
+  }
+  tmem_wait_ld<128>(r);
+  tc_fence_before();
+  mbar_arrive(acc_empty);
+}
+
+__device__ __forceinline__ void store_bf16x32(uint16_t* dst, const float* v) {
+  uint32_t w[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) d[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+}
+
+template <int MODE>
+__device__ __forceinline__ void epilogue_compute(const GemmParams& p, uint32_t* r, int half, int e, int nt,
+                                                 int64_t prow, int slot, float xs_t) {
   const bool real = slot >= 0;
   if constexpr (MODE == kG2Rows) {
     const float d2 = __fmul_rn(p.alpha[e], __fdiv_rn(1.0f, p.g2));
-    uint16_t* orow = static_cast<uint16_t*>(p.out) + prow * p.N;
-#pragma unroll 1
-    for (int c = 0; c < kTileN / 32; ++c) {
+    const int col0 = nt * kTileN + half * 128;
+    if (!real || col0 >= p.N) return;
+    uint16_t* orow = static_cast<uint16_t*>(p.out) + prow * p.N + col0;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
       float v[32];
-      tmem_ld32(tmem_row + c * 32, v);
-      const int col0 = nt * kTileN + c * 32;
-      if (real && col0 < p.N) {
-        uint32_t w[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(__fmul_rn(v[2 * i], d2), __fmul_rn(v[2 * i + 1], d2));
-        uint4* dst = reinterpret_cast<uint4*>(orow + col0);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-      }
+      for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(__uint_as_float(r[32 * c + i]), d2);
+      store_bf16x32(orow + 32 * c, v);
     }
   } else {
-    const float xs_t = real ? p.xs[slot / p.top_k] : 0.0f;
+    if (!real) return;
     const float a1 = p.alpha[e];
     const int I = p.inter;
     const int ip16 = static_cast<int>(roundup64(I, kTileK) / 16);  // scale columns of the intermediate
-    // column chunks of 32 intermediate values
-    const int nchunks = p.gated ? 4 : 8;
-    uint32_t sfword = 0;
-#pragma unroll 1
-    for (int c = 0; c < nchunks; ++c) {
-      float h[32];
-      int i0;  // first intermediate column of this chunk
-      if (p.gated) {
-        float g[32], u[32];
-        tmem_ld32(tmem_row + c * 32, g);
-        tmem_ld32(tmem_row + 128 + c * 32, u);
-        i0 = nt * 128 + c * 32;
-        if constexpr (MODE == kG1Preact) {
-          if (real) {
-            float* o = static_cast<float*>(p.out) + prow * (2 * I);
+    // intermediate columns [i0, i0 + nout) come from this thread's registers
+    const int i0 = p.gated ? nt * 128 + half * 64 : nt * kTileN + half * 128;
+    const int nout = p.gated ? 64 : 128;
+    if (i0 >= I) return;
+    if constexpr (MODE == kG1Preact) {
+      const int ld = p.gated ? 2 * I : I;
+      float* o = static_cast<float*>(p.out) + prow * ld;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              o[i0 + i] = __fmul_rn(__fmul_rn(g[i], xs_t), a1);
-              o[I + i0 + i] = __fmul_rn(__fmul_rn(u[i], xs_t), a1);
-            }
-          }
-          continue;
-        }
+      for (int i = 0; i < 128; ++i) {
+        const float y = __fmul_rn(__fmul_rn(__uint_as_float(r[i]), xs_t), a1);
+        if (i < nout) o[i0 + i] = y;                    // gate (or all) columns
+        else if (p.gated) o[I + i0 + i - 64] = y;       // up columns
+      }
+      return;
+    }
+    // activation, 32 intermediate values at a time
+    uint32_t sfw = 0;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      if (c * 32 >= nout) break;
+      float h[32];
+      if (p.gated) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float yg = __fmul_rn(__fmul_rn(g[i], xs_t), a1);
-          const float yu = __fmul_rn(__fmul_rn(u[i], xs_t), a1);
+          const float yg = __fmul_rn(__fmul_rn(__uint_as_float(r[32 * c + i]), xs_t), a1);
+          const float yu = __fmul_rn(__fmul_rn(__uint_as_float(r[64 + 32 * c + i]), xs_t), a1);
           h[i] = bf16_round_f32(__fmul_rn(silu_f32(yg), yu));
         }
       } else {
-        float y[32];
-        tmem_ld32(tmem_row + c * 32, y);
-        i0 = nt * kTileN + c * 32;
-        if (i0 >= I) continue;
-        if constexpr (MODE == kG1Preact) {
-          if (real) {
-            float* o = static_cast<float*>(p.out) + prow * I;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o[i0 + i] = __fmul_rn(__fmul_rn(y[i], xs_t), a1);
-          }
-          continue;
-        }
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float r = fmaxf(__fmul_rn(__fmul_rn(y[i], xs_t), a1), 0.0f);
-          h[i] = bf16_round_f32(__fmul_rn(r, r));
+          const float y = fmaxf(__fmul_rn(__fmul_rn(__uint_as_float(r[32 * c + i]), xs_t), a1), 0.0f);
+          h[i] = bf16_round_f32(__fmul_rn(y, y));
         }
       }
-      if (!real) continue;
+      const int ic = i0 + 32 * c;
       if constexpr (MODE == kG1Act) {
-        uint16_t* o = static_cast<uint16_t*>(p.out) + prow * I + i0;
-        uint32_t w[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(h[2 * i], h[2 * i + 1]);
-        uint4* dst = reinterpret_cast<uint4*>(o);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-      } else if constexpr (MODE == kG1Fused) {
-        uint8_t* dst = static_cast<uint8_t*>(p.out) + prow * (I / 2) + i0 / 2;
+        store_bf16x32(static_cast<uint16_t*>(p.out) + prow * I + ic, h);
+      } else {
+        uint8_t* dst = static_cast<uint8_t*>(p.out) + prow * (I / 2) + ic / 2;
         const uint32_t q2 = requant32_store(h, p.g2, dst);
-        // two 32-column chunks fill one 4-scale group of the 128x4 tile layout
-        sfword |= q2 << (16 * ((i0 >> 5) & 1));
-        if ((i0 >> 5) & 1) {
-          *reinterpret_cast<uint32_t*>(p.out_sf + sf_tile_offset(prow, (i0 >> 4) - 2, ip16)) = sfword;
-          sfword = 0;
+        // two 32-value chunks make one 4-scale group of the 128x4 tile layout
+        if (c & 1) {
+          *reinterpret_cast<uint32_t*>(p.out_sf + sf_tile_offset(prow, (ic >> 4) - 2, ip16)) = sfw | (q2 << 16);
+        } else {
+          sfw = q2;
         }
       }
     }
     if constexpr (MODE == kG1Fused) {
-      // zero the scale columns of the K padding once per row (last column tile)
-      if (real && nt == p.n_tiles - 1) {
+      // zero the scale columns of the K padding once per row (last column tile, first half)
+      if (nt == p.n_tiles - 1 && half == 0) {
         for (int c4 = I / 64; c4 < ip16 / 4; ++c4)
           *reinterpret_cast<uint32_t*>(p.out_sf + sf_tile_offset(prow, 4 * c4, ip16)) = 0u;
       }
@@ -233,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       mbar_init(&empty[s], 1);
     }
     mbar_init(acc_full, 1);
-    mbar_init(acc_empty, 128);
+    mbar_init(acc_empty, kEpiThreads);
     mbar_init(final_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -329,22 +340,24 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     }
   } else {
     const int q = warp & 3;                 // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;       // column half of the tile
     const int r = q * 32 + lane;            // row inside the 128-row tile
     const uint32_t tmem_row = tmem + (static_cast<uint32_t>(q * 32) << 16);
     uint32_t acc_phase = 0;
     for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
-      bool ok = mbar_wait(acc_full, acc_phase, abort_flag, p.dev_status);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
       int e, nt, mi;
       decode_unit(u, s_off, p.El, p.n_tiles, e, nt, mi);
       const int64_t prow = s_off[e] + mi * kTileM + r;
       const int slot = p.row_to_slot[prow];
-      epilogue_unit<MODE>(p, tmem_row, e, nt, prow, slot);
-      tc_fence_before();
-      mbar_arrive(acc_empty);
+      const float xs_t = (MODE != kG2Rows && slot >= 0) ? p.xs[slot / p.top_k] : 0.0f;
+      bool ok = mbar_wait(acc_full, acc_phase, abort_flag, p.dev_status);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t acc[128];
+      load_acc<MODE>(p, tmem_row, half, acc, acc_empty);
       acc_phase ^= 1;
+      if (__any_sync(0xffffffffu, slot >= 0)) epilogue_compute<MODE>(p, acc, half, e, nt, prow, slot, xs_t);
     }
   }
   tc_fence_before();
