@@ -223,8 +223,17 @@ extern "C" moe_status_t moe_grouped_fp4_forward(const int32_t* padded_offsets, c
   const Bufs b = carve(workspace, L);
   if (fin) rows_out = b.g;
   const Prepared pw = prepared_ptrs(prepared, prepared_layout(d));
+  // while the stream is being captured, the marks become external event-record nodes so the
+  // caller can read their timestamps after each graph launch
+  cudaStreamCaptureStatus capturing = cudaStreamCaptureStatusNone;
+  if (num_step_events == 5) MOE_CUDA(cudaStreamIsCapturing(s, &capturing));
   auto mark = [&](int i) -> moe_status_t {
-    if (num_step_events == 5) MOE_CUDA(cudaEventRecord(static_cast<cudaEvent_t>(step_events[i]), s));
+    if (num_step_events != 5) return MOE_OK;
+    cudaEvent_t ev = static_cast<cudaEvent_t>(step_events[i]);
+    if (capturing == cudaStreamCaptureStatusActive)
+      MOE_CUDA(cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal));
+    else
+      MOE_CUDA(cudaEventRecord(ev, s));
     return MOE_OK;
   };
   if ((st = mark(0)) != MOE_OK) return st;

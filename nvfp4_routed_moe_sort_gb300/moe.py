@@ -108,5 +108,35 @@ class NVFP4RoutedMoE:
             return b["out"]
         return b["gemm2_out"], topk_weights, b["token_to_row"]
 
+    def capture(self, x: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor,
+                do_finalize: bool = True, step_events=None) -> torch.cuda.CUDAGraph:
+        """Capture one forward (quantize, plan, permute, GEMM1, GEMM2, finalize) in a CUDA graph.
+
+        The graph reads x, topk_ids and topk_weights at their current addresses and writes the
+        layer's buffers; refill the inputs in place and call ``replay()``. Any routing of the
+        same (M, top_k) replays correctly: the kernels size their work from the device-side
+        plan. ``step_events`` (8 recorded torch events, optional) mark the step boundaries
+        inside the graph: before quantize, plan, permute, gemm1, gemm2, finalize, and the end.
+        """
+        M, k = topk_ids.shape
+        b = self.buffers(M, k, do_finalize)
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):          # warm-up outside the capture
+            self.forward(x, topk_ids, topk_weights, do_finalize)
+        torch.cuda.current_stream().wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            if step_events:
+                step_events[0].record()
+            self.quantize(x, b)
+            if step_events:
+                step_events[1].record()
+            self.plan(topk_ids, b)
+            self.experts(topk_weights, b, do_finalize, step_events[2:7] if step_events else None)
+            if step_events:
+                step_events[7].record()
+        return g
+
     def device_status(self, M: int, top_k: int, do_finalize: bool) -> int:
         return int(self.buffers(M, top_k, do_finalize)["dev_status"][0].item())

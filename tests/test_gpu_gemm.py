@@ -184,3 +184,26 @@ def test_step_events_recorded():
     times = [evs[i].elapsed_time(evs[i + 1]) for i in range(4)]
     assert all(t >= 0 for t in times)
     assert_close_output(bf16_np(b["out"]), p.oracle_forward()["out"], "events")
+
+
+def test_cuda_graph_replay_with_new_routing():
+    # capture once; refill hidden states and routing in place; replay == eager forward
+    cfg = SMALL["swiglu_skew"]
+    p = Problem(cfg)
+    x = p.x.clone()
+    ids = p.ids_t.clone()
+    tw = p.tw_t.clone()
+    g = p.layer.capture(x, ids, tw, True)
+    cfg2 = cfg.with_(seed=99, skew=0.0)
+    ids2, tw2 = mi.routing(cfg2)
+    x.copy_(mi.hidden_bf16(cfg2, DEV))
+    ids.copy_(torch.from_numpy(ids2))
+    tw.copy_(torch.from_numpy(tw2))
+    g.replay()
+    torch.cuda.synchronize()
+    got = bf16_np(p.bufs(True)["out"]).copy()
+    ref = bf16_np(p.layer.forward(x.clone(), ids.clone(), tw.clone()))
+    torch.cuda.synchronize()
+    assert np.array_equal(got, ref)
+    p2 = Problem(cfg2)
+    assert_close_output(got, p2.oracle_forward()["out"], "graph")
