@@ -164,21 +164,21 @@ def setup_gpu(cfg, dev):
 
 
 def traffic_from_profiles(kernel: str, workload: str):
-    """dram bytes per launch of `kernel` from the committed ncu summary, if the kernel's
-    source is unchanged since the counters were taken."""
-    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    """DRAM bytes per launch of `kernel` from the committed ncu summary
+    (profiles/dram_traffic.txt), or None when the kernel's source has changed since the
+    counters were taken (sha256 of gemm.cu followed by common.cuh)."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(p):
         return None
+    csrc = os.path.join(ROOT, "nvfp4_routed_moe_sort_gb300", "csrc")
+    h = hashlib.sha256(open(os.path.join(csrc, "gemm.cu"), "rb").read()
+                       + open(os.path.join(csrc, "common.cuh"), "rb").read()).hexdigest()[:16]
     with open(p) as f:
-        d = json.load(f)
-    ent = d.get(workload, {}).get(kernel)
-    if not ent:
-        return None
-    src = os.path.join(ROOT, "nvfp4_routed_moe_sort_gb300", "csrc", ent.get("source", "gemm.cu"))
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    if h != ent.get("source_sha"):
-        return None
-    return ent["dram_bytes_per_launch"]
+        for ln in f:
+            parts = ln.split()
+            if len(parts) == 5 and not ln.startswith("#") and parts[0] == workload and parts[1] == kernel:
+                return int(parts[2]) if parts[4] == h else None
+    return None
 
 
 def run_gpu(args, cfg, rank, world):
