@@ -26,6 +26,7 @@ moe_status_t check_weights(const moe_nvfp4_weights_t* w) {
 }
 
 struct Bufs {
+  int32_t* sched;
   uint8_t *aq, *asf, *iq, *isf;
   uint16_t* g;
 };
@@ -33,6 +34,7 @@ struct Bufs {
 Bufs carve(void* ws, const WorkspaceLayout& L) {
   uint8_t* b = static_cast<uint8_t*>(ws);
   Bufs r;
+  r.sched = reinterpret_cast<int32_t*>(b + L.sched);
   r.aq = b + L.aq;
   r.asf = b + L.asf;
   r.iq = b + L.iq;
@@ -98,6 +100,7 @@ GemmLaunch gemm1_launch(const Dims& d, const WorkspaceLayout& L, const Bufs& b, 
   g.out = b.iq;
   g.out_sf = b.isf;
   g.dev_status = dev_status;
+  g.tile_counter = b.sched;
   g.mode = kG1Fused;
   return g;
 }
@@ -238,7 +241,7 @@ extern "C" moe_status_t moe_grouped_fp4_forward(const int32_t* padded_offsets, c
   };
   if ((st = mark(0)) != MOE_OK) return st;
   st = launch_permute(padded_offsets, static_cast<int>(d.El), row_to_slot, top_k, L.cap, xq, xsf,
-                      static_cast<int>(d.H), b.aq, b.asf, s);
+                      static_cast<int>(d.H), b.aq, b.asf, b.sched, s);
   if (st != MOE_OK) return st;
   if ((st = mark(1)) != MOE_OK) return st;
   GemmLaunch g1 = gemm1_launch(d, L, b, pw, padded_offsets, row_to_slot, xs, top_k, dev_status);
@@ -269,6 +272,7 @@ extern "C" moe_status_t moe_grouped_fp4_forward(const int32_t* padded_offsets, c
   g2.out = rows_out;
   g2.out_sf = nullptr;
   g2.dev_status = dev_status;
+  g2.tile_counter = b.sched + 1;
   st = launch_gemm(g2, s);
   if (st != MOE_OK) return st;
   if ((st = mark(3)) != MOE_OK) return st;
@@ -299,7 +303,7 @@ extern "C" moe_status_t moe_debug_gemm1(const int32_t* padded_offsets, const int
   const Bufs b = carve(workspace, L);
   const Prepared pw = prepared_ptrs(prepared, prepared_layout(d));
   st = launch_permute(padded_offsets, static_cast<int>(d.El), row_to_slot, top_k, L.cap, xq, xsf,
-                      static_cast<int>(d.H), b.aq, b.asf, s);
+                      static_cast<int>(d.H), b.aq, b.asf, b.sched, s);
   if (st != MOE_OK) return st;
   GemmLaunch g1 = gemm1_launch(d, L, b, pw, padded_offsets, row_to_slot, xs, top_k, dev_status);
   g1.mode = mode == 0 ? kG1Preact : kG1Act;

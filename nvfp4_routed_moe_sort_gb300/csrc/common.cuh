@@ -99,6 +99,15 @@ __device__ __forceinline__ float bf16_round_f32(float x) {
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch: kernels of the path are launched so that the next one may
+// start while this one runs; each kernel lets its dependents launch at entry, does its
+// prologue (no global memory), and waits for its predecessor before touching its outputs.
+// Without the launch attribute both instructions are no-ops.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
 // shared memory, mbarrier, TMA
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -205,6 +214,7 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
                    smem_u32(bar))
                : "memory");
 }
+
 
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of 128 bytes,
 // 8-row groups 1024 bytes apart. `saddr` is the start (the 1024-aligned tile base plus the

@@ -21,8 +21,11 @@
 //                activation and NVFP4 requantisation (GEMM1) or BF16 rows (GEMM2); warps
 //                whose 32 rows are all padding skip the arithmetic.
 // A work unit is (expert e, 256-column tile nt, 128-row tile mi); units are numbered
-// expert-major, then column tile, then row tile, so CTAs running side by side share an
-// expert's weight tiles in L2. The unit count comes from padded_offsets on the device.
+// expert-major, then column tile, then row tile, and claimed in that order from an atomic
+// counter by whichever CTA's producer is free, so the row tiles of one expert stream the
+// same weight tile at the same time and share it in L2. The producer hands each claimed id
+// to the MMA and epilogue warps through a 4-entry shared-memory ring. The unit count comes
+// from padded_offsets on the device.
 // TMEM: columns [0, 256) accumulator (two N=128 halves), [256, 448) scale tiles of the four
 // stages (16 columns of A scales + 32 of B scales each). Every wait is bounded.
 #include <cuda.h>
@@ -51,12 +54,15 @@ constexpr int kSfColsPerStage = 48;
 constexpr int kThreads = 320;  // producer, MMA, 8 epilogue warps
 constexpr int kEpiThreads = 256;
 constexpr int kSmemExtra = 1024 /*align*/ + 256 /*barriers*/;
+constexpr int kUnitRing = 4;      // work-unit ids handed from the producer to the other roles
+constexpr int kRingConsumers = 1 + kEpiThreads / 32;  // MMA thread + one lane per epilogue warp
 
 static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
 static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
 
 struct GemmParams {
-  CUtensorMap tmap_a;
+  CUtensorMap tmap_a;     // 128-row activation boxes
+  CUtensorMap tmap_a32;   // 32-row boxes, for tiles whose real rows all lie in the first 32
   CUtensorMap tmap_b;
   const uint8_t* sfa;
   const uint8_t* sfb;
@@ -67,6 +73,7 @@ struct GemmParams {
   void* out;
   uint8_t* out_sf;
   int32_t* dev_status;
+  int32_t* tile_counter;  // zeroed before the launch (by the permute kernel)
   int32_t El, Kp, nkb, N, Np, n_tiles, top_k, inter, gated;
   float g2;
 };
@@ -232,12 +239,15 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
   uint64_t* acc_full = empty + kStages;
   uint64_t* acc_empty = acc_full + 1;
   uint64_t* final_bar = acc_empty + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(final_bar + 1);
+  uint64_t* unit_full = final_bar + 1;
+  uint64_t* unit_empty = unit_full + kUnitRing;
+  volatile int32_t* unit_ring = reinterpret_cast<volatile int32_t*>(unit_empty + kUnitRing);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(unit_empty + kUnitRing) + kUnitRing;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int32_t* s_off = reinterpret_cast<int32_t*>(smem + kStages * kStageBytes + 256);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int i = threadIdx.x; i <= p.El; i += blockDim.x) s_off[i] = p.padded_offsets[i];
+  pdl_trigger();
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -246,29 +256,56 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, kEpiThreads);
     mbar_init(final_bar, 1);
+    for (int i = 0; i < kUnitRing; ++i) {
+      mbar_init(&unit_full[i], 1);
+      mbar_init(&unit_empty[i], kRingConsumers);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&p.tmap_a);
+    prefetch_tensormap(&p.tmap_a32);
     prefetch_tensormap(&p.tmap_b);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
+  pdl_wait();  // the plan, activations and tile counter come from earlier kernels
+  for (int i = threadIdx.x; i <= p.El; i += blockDim.x) s_off[i] = p.padded_offsets[i];
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int total_units = (s_off[p.El] >> 7) * p.n_tiles;
+  // the producer claims work units and hands their ids to the MMA and epilogue warps
+  auto take_unit = [&](uint32_t& rslot, uint32_t& rphase, bool one_lane) -> int {
+    bool got = mbar_wait(&unit_full[rslot], rphase, abort_flag, p.dev_status);
+    if (!one_lane) got = __all_sync(0xffffffffu, got);
+    if (!got) return -2;
+    const int u = unit_ring[rslot];
+    if (!one_lane) __syncwarp();
+    if (one_lane || lane == 0) mbar_arrive(&unit_empty[rslot]);
+    if (++rslot == kUnitRing) { rslot = 0; rphase ^= 1; }
+    return u;
+  };
 
   if (warp == 0) {
     if (lane == 0) {
       uint32_t stage = 0, phase = 0;
       uint32_t issued_mask = 0, issued_phase = 0;
+      uint32_t rslot = 0, rphase = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+      while (ok) {
+        // claim the next unit (in order, from the global counter) and publish its id
+        if (!mbar_wait(&unit_empty[rslot], rphase ^ 1, abort_flag, p.dev_status)) { ok = false; break; }
+        int u = atomicAdd(p.tile_counter, 1);
+        if (u >= total_units) u = -1;
+        unit_ring[rslot] = u;
+        mbar_arrive(&unit_full[rslot]);
+        if (++rslot == kUnitRing) { rslot = 0; rphase ^= 1; }
+        if (u < 0) break;
         int e, nt, mi;
         decode_unit(u, s_off, p.El, p.n_tiles, e, nt, mi);
         const int row0 = s_off[e] + mi * kTileM;
@@ -277,11 +314,16 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         const uint8_t* sfa = p.sfa + static_cast<int64_t>(row0 >> 7) * kt * 512;
         const uint8_t* sfb0 = p.sfb + (static_cast<int64_t>(e) * (p.Np >> 7) + nt * 2) * kt * 512;
         const uint8_t* sfb1 = sfb0 + kt * 512;
+        // a tile whose row 32 is padding has all its real rows in the first 32 (padding rows
+        // end a segment): load only those; the MMA rows fed by stale shared memory are
+        // padding rows, whose results are never stored
+        const bool short_tile = p.row_to_slot[row0 + 32] < 0;
+        const uint32_t tx = short_tile ? kStageTx - (kABytes - 32 * 128) : kStageTx;
         for (int kb = 0; kb < p.nkb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.dev_status)) { ok = false; break; }
           uint8_t* st = smem + stage * kStageBytes;
-          mbar_arrive_expect_tx(&full[stage], kStageTx);
-          tma_load_2d(st, &p.tmap_a, kb * 128, row0, &full[stage]);
+          mbar_arrive_expect_tx(&full[stage], tx);
+          tma_load_2d(st, short_tile ? &p.tmap_a32 : &p.tmap_a, kb * 128, row0, &full[stage]);
           tma_load_2d(st + kOffB, &p.tmap_b, kb * 128, brow0, &full[stage]);
           bulk_load(st + kOffSfa, sfa + kb * 2048, 2048, &full[stage]);
           bulk_load(st + kOffSfb, sfb0 + kb * 2048, 2048, &full[stage]);
@@ -301,8 +343,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_mxf4nvf4(kTileM, 128);
       uint32_t stage = 0, phase = 0, acc_phase = 0;
+      uint32_t rslot = 0, rphase = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
+      while (ok) {
+        const int u = take_unit(rslot, rphase, true);
+        if (u < 0) break;
         if (!mbar_wait(acc_empty, acc_phase ^ 1, abort_flag, p.dev_status)) { ok = false; break; }
         tc_fence_after();
         for (int kb = 0; kb < p.nkb; ++kb) {
@@ -344,7 +389,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     const int r = q * 32 + lane;            // row inside the 128-row tile
     const uint32_t tmem_row = tmem + (static_cast<uint32_t>(q * 32) << 16);
     uint32_t acc_phase = 0;
-    for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+    uint32_t rslot = 0, rphase = 0;
+    while (true) {
+      const int u = take_unit(rslot, rphase, false);
+      if (u < 0) break;
       int e, nt, mi;
       decode_unit(u, s_off, p.El, p.n_tiles, e, nt, mi);
       const int64_t prow = s_off[e] + mi * kTileM + r;
@@ -401,11 +449,12 @@ bool encode_rows(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t 
 }
 
 template <int MODE>
-moe_status_t launch_mode(const GemmParams& prm, int grid, size_t smem, cudaStream_t s) {
+moe_status_t launch_mode(const GemmParams& prm, int64_t units_max, size_t smem, cudaStream_t s) {
   auto kern = grouped_gemm_kernel<MODE>;
   MOE_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)));
-  kern<<<grid, kThreads, smem, s>>>(prm);
-  return launch_status();
+  // persistent: one CTA per SM, at most one per work unit
+  const int grid = static_cast<int>(units_max < num_sms() ? units_max : num_sms());
+  return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, prm);
 }
 
 }  // namespace
@@ -415,6 +464,7 @@ moe_status_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
   GemmParams prm;
   memset(&prm, 0, sizeof(prm));
   if (!encode_rows(&prm.tmap_a, g.a, g.K / 2, g.cap, kTileM)) return MOE_ERR_CUDA;
+  if (!encode_rows(&prm.tmap_a32, g.a, g.K / 2, g.cap, 32)) return MOE_ERR_CUDA;
   if (!encode_rows(&prm.tmap_b, g.b, g.K / 2, g.El * g.Np, kTileN)) return MOE_ERR_CUDA;
   prm.sfa = g.a_sf;
   prm.sfb = g.b_sf;
@@ -425,6 +475,7 @@ moe_status_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
   prm.out = g.out;
   prm.out_sf = g.out_sf;
   prm.dev_status = g.dev_status;
+  prm.tile_counter = g.tile_counter;
   prm.El = static_cast<int32_t>(g.El);
   prm.Kp = static_cast<int32_t>(g.Kp);
   prm.nkb = static_cast<int32_t>(g.Kp / kTileK);
@@ -436,13 +487,12 @@ moe_status_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
   prm.gated = g.gated ? 1 : 0;
   prm.g2 = g.g2;
   const int64_t units_max = (g.cap / kTileM) * prm.n_tiles;
-  const int grid = static_cast<int>(units_max < num_sms() ? units_max : num_sms());
   const size_t smem = static_cast<size_t>(kStages) * kStageBytes + kSmemExtra + (g.El + 1) * 4;
   switch (g.mode) {
-    case kG1Fused: return launch_mode<kG1Fused>(prm, grid, smem, s);
-    case kG1Preact: return launch_mode<kG1Preact>(prm, grid, smem, s);
-    case kG1Act: return launch_mode<kG1Act>(prm, grid, smem, s);
-    case kG2Rows: return launch_mode<kG2Rows>(prm, grid, smem, s);
+    case kG1Fused: return launch_mode<kG1Fused>(prm, units_max, smem, s);
+    case kG1Preact: return launch_mode<kG1Preact>(prm, units_max, smem, s);
+    case kG1Act: return launch_mode<kG1Act>(prm, units_max, smem, s);
+    case kG2Rows: return launch_mode<kG2Rows>(prm, units_max, smem, s);
     default: return MOE_ERR_INVALID_ARGUMENT;
   }
 }

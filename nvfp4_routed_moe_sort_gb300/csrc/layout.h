@@ -59,11 +59,11 @@ inline PreparedLayout prepared_layout(const Dims& d) {
   return L;
 }
 
-// Forward workspace: permuted activations [cap, H/2] + scale tiles [cap/128][Hp/64][512],
+// Forward workspace: GEMM tile counters (256 B), permuted activations [cap, H/2] + scale tiles [cap/128][Hp/64][512],
 // intermediate [cap, I/2] + scale tiles [cap/128][Ip/64][512], and (finalize only) the
 // BF16 expert rows [cap, H].
 struct WorkspaceLayout {
-  size_t aq, asf, iq, isf, g, total;
+  size_t sched, aq, asf, iq, isf, g, total;
   int64_t cap;
 };
 
@@ -77,6 +77,7 @@ inline WorkspaceLayout workspace_layout(const Dims& d, int64_t M, int64_t top_k,
   WorkspaceLayout L;
   L.cap = plan_capacity_rows(M, top_k, d.El);
   size_t c = 0;
+  L.sched = take(c, 256);  // GEMM tile counters, zeroed by the permute kernel
   L.aq = take(c, L.cap * d.H / 2);
   L.asf = take(c, L.cap * d.Hp / 16);
   L.iq = take(c, L.cap * d.I / 2);
@@ -111,12 +112,13 @@ struct GemmLaunch {
   void* out;
   uint8_t* out_sf;
   int32_t* dev_status;
+  int32_t* tile_counter;
 };
 
 moe_status_t launch_gemm(const GemmLaunch& g, cudaStream_t s);
 moe_status_t launch_permute(const int32_t* padded_offsets, int El, const int32_t* row_to_slot, int top_k,
                             int64_t cap, const uint8_t* xq, const uint8_t* xsf, int H, uint8_t* aq, uint8_t* asf,
-                            cudaStream_t s);
+                            int32_t* tile_counters, cudaStream_t s);
 moe_status_t launch_finalize(const uint16_t* rows, const float* topk_weights, const int32_t* token_to_row, int M,
                              int top_k, int H, uint16_t* out, cudaStream_t s);
 moe_status_t launch_prepare_matrix(const uint8_t* src, const uint8_t* src_sf, int E, int rows, int rows_p, int K,

