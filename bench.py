@@ -196,54 +196,16 @@ def run_gpu(args, cfg, rank, world):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     n_ev = 8
     K, W = args.steps, args.warmup
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]]
-    for row in evs:          # torch creates the CUDA event on its first record
-        for e in row:
-            e.record()
-    torch.cuda.synchronize()
 
-    # eager reference: the same calls launched one by one from the host
-    def eager_step(e):
-        e[0].record()
-        layer.quantize(x, b)
-        e[1].record()
-        layer.plan(ids_t, b)
-        layer.experts(tw_t, b, True, step_events=e[2:7])
-        e[7].record()
-
-    eager = []
-    eager_parts = []
-    for i in range(W + min(K, 20)):
-        flush.zero_()
-        eager_step(evs[0])
-        torch.cuda.synchronize()
-        if i >= W:
-            eager.append(evs[0][0].elapsed_time(evs[0][7]))
-            eager_parts.append([evs[0][j].elapsed_time(evs[0][j + 1]) for j in range(n_ev - 1)])
-    eager_ms = float(np.mean(eager))
-    ep = np.mean(np.array(eager_parts), axis=0)
-    eager_kern = dict(zip(["quantize", "plan", "permute", "gemm1", "gemm2", "finalize"], map(float, ep[:6])))
-    # the timed step: one CUDA-graph replay of the whole path, kernel boundaries marked
-    # by event nodes inside the graph
-    try:
-        gev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n_ev)]
-    except TypeError:
-        gev = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
-    for e in gev:
-        e.record()
-    graph = layer.capture(x, ids_t, tw_t, True, step_events=gev)
+    # the timed step: one CUDA-graph replay of the whole path
+    graph = layer.capture(x, ids_t, tw_t, True)
     for i in range(W):
         flush.zero_()
         graph.replay()
     torch.cuda.synchronize()
-    s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    in_graph_events = True
-    try:
-        gev[0].elapsed_time(gev[n_ev - 1])
-    except Exception:
-        in_graph_events = False
     if world > 1:
         torch.distributed.barrier()
+    s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(dev.index)
     clocks.start()
     torch.cuda.synchronize()
@@ -255,29 +217,38 @@ def run_gpu(args, cfg, rank, world):
         graph.replay()
         e_ev.record()
         e_ev.synchronize()
-        if in_graph_events:
-            step_times.append([gev[j].elapsed_time(gev[j + 1]) for j in range(n_ev - 1)] +
-                              [s_ev.elapsed_time(e_ev)])
-        else:
-            step_times.append([float("nan")] * (n_ev - 1) + [s_ev.elapsed_time(e_ev)])
+        step_times.append(s_ev.elapsed_time(e_ev))
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     clk = clocks.stop()
-    if world > 1:
-        torch.distributed.barrier()
+    # kernel boundaries: the same calls launched eagerly with an event between kernels. A
+    # device-side sleep enqueued first lets the host queue every step before the GPU starts,
+    # so the events bracket device time only (no host gaps).
+    KE = min(K, 50)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(KE)]
+    for row in evs:          # torch creates the CUDA event on its first record
+        for e in row:
+            e.record()
+    for _ in range(W):
+        flush.zero_()
+        layer.forward(x, ids_t, tw_t)
+    torch.cuda.synchronize()
+    torch.cuda._sleep(int(60e6))   # ~30 ms at 2 GHz
+    for e in evs:
+        flush.zero_()
+        e[0].record()
+        layer.quantize(x, b)
+        e[1].record()
+        layer.plan(ids_t, b)
+        layer.experts(tw_t, b, True, step_events=e[2:7])
+        e[7].record()
+    torch.cuda.synchronize()
+    kern_times = [[e[j].elapsed_time(e[j + 1]) for j in range(n_ev - 1)] for e in evs]
+    eager_ms = float(np.mean([e[0].elapsed_time(e[7]) for e in evs]))
     assert layer.device_status(M, k, True) == 0, "device status word set"
     names = ["quantize", "plan", "permute", "gemm1", "gemm2", "finalize"]
-    per = {n: [] for n in names}
-    steps_ms = []
-    for t in step_times:
-        # events: 0 quantize 1 plan 2 [permute 3 gemm1 4 gemm2 5 finalize 6] 7
-        per["quantize"].append(t[0])
-        per["plan"].append(t[1])
-        per["permute"].append(t[2])
-        per["gemm1"].append(t[3])
-        per["gemm2"].append(t[4])
-        per["finalize"].append(t[5])
-        steps_ms.append(t[7])
+    per = {n: [t[c] for t in kern_times] for c, n in enumerate(names)}
+    steps_ms = step_times
     ms = float(np.mean(steps_ms))
     if world > 1:
         tt = torch.tensor([ms], device=dev)
@@ -285,8 +256,6 @@ def run_gpu(args, cfg, rank, world):
         ms = float(tt.item())
     work, stepw, R, active = kernel_work(cfg, ids)
     kern_ms = {n: float(np.mean(v)) for n, v in per.items()}
-    if not in_graph_events:       # per-kernel times from the eager steps instead
-        kern_ms = eager_kern
     dom = max(["gemm1", "gemm2"], key=lambda n: kern_ms[n])
     peaks = load_peaks()
     fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
@@ -320,10 +289,10 @@ def run_gpu(args, cfg, rank, world):
         "step_roofline": {"frac": step_roof_s / (ms * 1e-3), "bytes": stepw["bytes"], "flops": stepw["flops"],
                           "note": "whole step: max(bytes/HBM peak, flops/FP4 peak) over measured step time"},
         "kernels_ms": kern_ms,
-        "timing": "each step is one CUDA-graph replay of the whole path, timed by events on its stream "
-                  + ("(kernel times from event nodes inside the graph); " if in_graph_events else
-                     "(kernel times from eagerly launched steps); ")
-                  + f"the same calls launched eagerly from the host take {eager_ms:.4f} ms",
+        "timing": "each step is one CUDA-graph replay of the whole path, timed by events on its stream; "
+                  "kernel times from the same calls launched eagerly with events between the kernels, "
+                  "queued behind a device sleep so no host gap is timed; "
+                  f"an eager step takes {eager_ms:.4f} ms",
         "eager_ms_per_step": eager_ms,
         "e2e": e2e,
         "gpu_launches": launches_per_step * K,

@@ -91,6 +91,14 @@ __global__ void __launch_bounds__(256) prepare_matrix_kernel(const uint8_t* __re
 
 // out[t, :] = bf16(sum_j w[t,j] * row_j) with FP32 multiply and add kept separate and
 // slots taken in ascending j. Each thread owns 8 consecutive columns of one token.
+// BATCHED (few tokens, latency-bound): the loads of up to kMaxSlots slots are issued
+// together before the ordered accumulation, so a token costs one or two memory round
+// trips, not top_k. Otherwise (many tokens) the plain per-slot loop keeps more threads
+// resident, which hides the latency better.
+constexpr int kMaxSlots = 8;
+constexpr int kBatchedFinalizeMaxTokens = 256;
+
+template <bool BATCHED>
 __global__ void __launch_bounds__(256) finalize_kernel(const uint16_t* __restrict__ rows,
                                                        const float* __restrict__ topk_weights,
                                                        const int32_t* __restrict__ token_to_row, int M, int top_k,
@@ -103,16 +111,45 @@ __global__ void __launch_bounds__(256) finalize_kernel(const uint16_t* __restric
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-  for (int j = 0; j < top_k; ++j) {
-    const int r = token_to_row[static_cast<int64_t>(t) * top_k + j];
-    if (r < 0) continue;
-    const float w = topk_weights[static_cast<int64_t>(t) * top_k + j];
-    const uint4 v = *reinterpret_cast<const uint4*>(rows + static_cast<int64_t>(r) * H + c8 * 8);
-    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+  if constexpr (!BATCHED) {
+    for (int j = 0; j < top_k; ++j) {
+      const int r = token_to_row[static_cast<int64_t>(t) * top_k + j];
+      if (r < 0) continue;
+      const float w = topk_weights[static_cast<int64_t>(t) * top_k + j];
+      const uint4 v = *reinterpret_cast<const uint4*>(rows + static_cast<int64_t>(r) * H + c8 * 8);
+      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      acc[2 * i] = __fadd_rn(acc[2 * i], __fmul_rn(w, __uint_as_float(u[i] << 16)));
-      acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], __fmul_rn(w, __uint_as_float(u[i] & 0xFFFF0000u)));
+      for (int i = 0; i < 4; ++i) {
+        acc[2 * i] = __fadd_rn(acc[2 * i], __fmul_rn(w, __uint_as_float(u[i] << 16)));
+        acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], __fmul_rn(w, __uint_as_float(u[i] & 0xFFFF0000u)));
+      }
+    }
+  }
+  for (int j0 = 0; BATCHED && j0 < top_k; j0 += kMaxSlots) {
+    int r[kMaxSlots];
+#pragma unroll
+    for (int j = 0; j < kMaxSlots; ++j)
+      r[j] = (j0 + j < top_k) ? token_to_row[static_cast<int64_t>(t) * top_k + j0 + j] : -1;
+    float w[kMaxSlots];
+    uint4 v[kMaxSlots];
+#pragma unroll
+    for (int j = 0; j < kMaxSlots; ++j) {
+      w[j] = 0.0f;
+      v[j] = make_uint4(0, 0, 0, 0);
+      if (r[j] >= 0) {
+        w[j] = topk_weights[static_cast<int64_t>(t) * top_k + j0 + j];
+        v[j] = *reinterpret_cast<const uint4*>(rows + static_cast<int64_t>(r[j]) * H + c8 * 8);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kMaxSlots; ++j) {
+      if (r[j] < 0) continue;
+      const uint32_t u[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[2 * i] = __fadd_rn(acc[2 * i], __fmul_rn(w[j], __uint_as_float(u[i] << 16)));
+        acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], __fmul_rn(w[j], __uint_as_float(u[i] & 0xFFFF0000u)));
+      }
     }
   }
   uint32_t o[4];
@@ -146,8 +183,11 @@ moe_status_t launch_finalize(const uint16_t* rows, const float* topk_weights, co
   if (M == 0) return MOE_OK;
   const int threads = 256;
   const int bx = (H / 8 + threads - 1) / threads;
-  return launch_pdl(finalize_kernel, dim3(bx, M), dim3(threads), 0, s, rows, topk_weights, token_to_row, M, top_k,
-                    H, out);
+  if (M <= kBatchedFinalizeMaxTokens)
+    return launch_pdl(finalize_kernel<true>, dim3(bx, M), dim3(threads), 0, s, rows, topk_weights, token_to_row, M,
+                      top_k, H, out);
+  return launch_pdl(finalize_kernel<false>, dim3(bx, M), dim3(threads), 0, s, rows, topk_weights, token_to_row, M,
+                    top_k, H, out);
 }
 
 moe_status_t launch_prepare_matrix(const uint8_t* src, const uint8_t* src_sf, int E, int rows, int rows_p, int K,

@@ -25,7 +25,7 @@ constexpr int kSlotsPerBlock = 2048;
 struct PlanSmem {
   int cnt[kMaxLocalExperts];
   int cursor[kMaxLocalExperts + 1];
-  uint8_t warp_cnt[32][kMaxLocalExperts];
+  alignas(16) uint8_t warp_cnt[32][kMaxLocalExperts];
 };
 
 __device__ __forceinline__ int local_of(int id, int off, int El) {
@@ -60,13 +60,15 @@ __device__ void scan_padded(PlanSmem& sm, int El) {
   if (lane == 31) sm.cursor[El] = incl;
 }
 
-// row_to_slot = -1 on the padding rows of every segment and on [total, capacity)
+// row_to_slot = -1 on the padding rows of every segment (one warp per expert, lanes across
+// its padding rows) and on [total, capacity)
 __device__ void fill_padding(const int* start, const int* cnt, int El, int total, int64_t cap,
                              int32_t* row_to_slot) {
-  for (int l = threadIdx.x; l < El; l += blockDim.x) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  for (int l = warp; l < El; l += nwarps) {
     const int b = start[l] + cnt[l];
     const int e = start[l] + (cnt[l] + kSegAlign - 1) / kSegAlign * kSegAlign;
-    for (int p = b; p < e; ++p) row_to_slot[p] = -1;
+    for (int p = b + lane; p < e; p += 32) row_to_slot[p] = -1;
   }
   for (int64_t p = total + threadIdx.x; p < cap; p += blockDim.x) row_to_slot[p] = -1;
 }
@@ -111,9 +113,14 @@ __device__ void place_range(const int32_t* __restrict__ ids, int64_t begin, int6
   }
 }
 
+__device__ void zero_warp_counts(PlanSmem& sm) {
+  uint4* w = reinterpret_cast<uint4*>(&sm.warp_cnt[0][0]);
+  for (int i = threadIdx.x; i < 32 * kMaxLocalExperts / 16; i += blockDim.x) w[i] = make_uint4(0, 0, 0, 0);
+}
+
 __device__ void zero_tables(PlanSmem& sm, int El) {
   for (int i = threadIdx.x; i < El; i += blockDim.x) sm.cnt[i] = 0;
-  for (int i = threadIdx.x; i < 32 * kMaxLocalExperts; i += blockDim.x) (&sm.warp_cnt[0][0])[i] = 0;
+  zero_warp_counts(sm);
 }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_single_kernel(
@@ -197,7 +204,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_place_kernel(const int32_t*
                                                                   int32_t* dev_status) {
   __shared__ PlanSmem sm;
   pdl_trigger();
-  for (int i = threadIdx.x; i < 32 * kMaxLocalExperts; i += blockDim.x) (&sm.warp_cnt[0][0])[i] = 0;
+  zero_warp_counts(sm);
   pdl_wait();
   for (int l = threadIdx.x; l < El; l += blockDim.x) sm.cursor[l] = base[static_cast<int64_t>(blockIdx.x) * El + l];
   __syncthreads();
