@@ -68,16 +68,31 @@ typedef enum {
 #define MOE_DEV_DUPLICATE_EXPERT 1 /* a token names the same local expert twice ([CUDNN] "distinct experts") */
 #define MOE_DEV_TIMEOUT 2          /* a pipeline wait in a GEMM kernel gave up (bounded spin) */
 
-/* [MCORE] flashinfer_routed_nvfp4_moe(activation_type): squared-ReLU or SwiGLU experts. */
-typedef enum { MOE_ACT_SWIGLU = 0, MOE_ACT_RELU2 = 1 } moe_activation_t;
+/* Expert activations. [MCORE] flashinfer_routed_nvfp4_moe(activation_type): squared-ReLU or
+ * SwiGLU experts; [CUDNN] Activation functions: SwiGLU with default scalars, GeGLU, GELU, ReLU,
+ * SiLU and Identity. Gated kinds (SwiGLU = silu(g)*u, GeGLU = gelu(g)*u) take W1 rows
+ * [gate; up] (N1 = 2I); the others act on each of the I pre-activations (N1 = I).
+ * GELU is x/2 * (1 + erf(x/sqrt(2))); SiLU is x / (1 + exp(-x)). */
+typedef enum {
+  MOE_ACT_SWIGLU = 0,
+  MOE_ACT_RELU2 = 1,
+  MOE_ACT_GEGLU = 2,
+  MOE_ACT_GELU = 3,
+  MOE_ACT_RELU = 4,
+  MOE_ACT_SILU = 5,
+  MOE_ACT_IDENTITY = 6
+} moe_activation_t;
+
+/* Storage of the route weights ([CUDNN] "Routing weights: ... unpacked FP32 / BF16"). */
+typedef enum { MOE_WEIGHTS_F32 = 0, MOE_WEIGHTS_BF16 = 1 } moe_weights_dtype_t;
 
 /* Activation global scale: [CUDNN] "a global scale of one" (prepare_activations) or
  * [MCORE]/[VLLM] one FP32 decode scale per token computed online. */
 typedef enum { MOE_SCALE_GLOBAL_ONE = 0, MOE_SCALE_PER_TOKEN = 1 } moe_act_scale_t;
 
 /* Expert weights in the linear boundary layout of [ALPHA] (gemm1_weights / gemm2_weights):
- *   w1       [El, N1, H/2]  packed E2M1; N1 = 2*I rows [gate; up] for SwiGLU ([MCORE] "MCore
- *                            stores gated FC1 as [gate; up]"), N1 = I for squared-ReLU
+ *   w1       [El, N1, H/2]  packed E2M1; N1 = 2*I rows [gate; up] for SwiGLU / GeGLU ([MCORE]
+ *                            "MCore stores gated FC1 as [gate; up]"), N1 = I otherwise
  *   w1_sf    [El, N1, H/16] E4M3 block scales, row-major ("linear, contiguous")
  *   w1_alpha [El]           FP32 per-expert dequant (global decode scale) of W1
  *   w2       [El, H, I/2]   packed E2M1
@@ -197,10 +212,13 @@ MOE_API moe_status_t moe_prepare_weights(const moe_nvfp4_weights_t* w, void* pre
  *   padded_offsets, row_to_slot, token_to_row  from moe_plan
  *   xq, xsf, xs        activation pack from moe_quantize_input ([M, H/2], [M, H/16], [M])
  *   w, prepared        sizes/activation and the moe_prepare_weights buffer
- *   topk_weights       [M, top_k] FP32 route weights (entries of masked slots are never read)
+ *   topk_weights       [M, top_k] route weights, FP32 or BF16 per topk_weights_dtype (entries of
+ *                      masked slots are never read)
+ *   routed_scaling_factor  finite FP32 scalar applied to each routed contribution ([ALPHA]
+ *                      routed_scaling_factor): the combine uses w' = fp32(w * factor); 1.0 = none
  *   fc2_input_scale    static FP32 encode scale of the intermediate (1.0 = global scale one);
  *                      GEMM2 rows are multiplied by alpha2[e] / fc2_input_scale
- *   do_finalize = 1    out [M, H] BF16 = bf16(sum_j w[t,j] * gemm2 row), ordered FP32
+ *   do_finalize = 1    out [M, H] BF16 = bf16(sum_j w'[t,j] * gemm2 row), ordered FP32
  *                      multiply + add over ascending j ([FROST] ordered combine); gemm2_out
  *                      may be NULL (rows go to the workspace)
  *   do_finalize = 0    gemm2_out [capacity, H] BF16 expert outputs, bf16(y2) in real rows,
@@ -220,7 +238,8 @@ MOE_API moe_status_t moe_grouped_fp4_forward(const int32_t* padded_offsets, cons
                                      const int32_t* token_to_row, int32_t M, int32_t top_k,
                                      const uint8_t* xq, const uint8_t* xsf, const float* xs,
                                      const moe_nvfp4_weights_t* w, const void* prepared,
-                                     size_t prepared_bytes, const float* topk_weights,
+                                     size_t prepared_bytes, const void* topk_weights,
+                                     int32_t topk_weights_dtype, float routed_scaling_factor,
                                      float fc2_input_scale, int32_t do_finalize, uint16_t* out,
                                      uint16_t* gemm2_out, void* workspace, size_t workspace_bytes,
                                      int32_t* dev_status, void* const* step_events,
@@ -229,12 +248,15 @@ MOE_API moe_status_t moe_grouped_fp4_forward(const int32_t* padded_offsets, cons
 /* ----------------------------------------------------------------------------------------
  * S7  moe_finalize - [CUDNN] moe_unpermute; [FROST] "ordered, separate FP32 multiplication
  * and addition"; unrouted slots and their scores are ignored.
- *   gemm2_out    [rows, H] BF16 expert rows;  topk_weights [M, top_k] FP32
+ *   gemm2_out    [rows, H] BF16 expert rows
+ *   topk_weights [M, top_k] route weights, FP32 or BF16 (topk_weights_dtype)
+ *   routed_scaling_factor  finite FP32 scalar, w' = fp32(w * factor) ([ALPHA])
  *   token_to_row [M, top_k] row per slot or -1;  out [M, H] BF16
- * out[t,:] = bf16(acc) with acc = 0; acc = acc + w[t,j]*row for j = 0..top_k-1, row != -1.
+ * out[t,:] = bf16(acc) with acc = 0; acc = acc + w'[t,j]*row for j = 0..top_k-1, row != -1.
  * A token with every slot masked gets a zero row.
  * ---------------------------------------------------------------------------------------- */
-MOE_API moe_status_t moe_finalize(const uint16_t* gemm2_out, const float* topk_weights,
+MOE_API moe_status_t moe_finalize(const uint16_t* gemm2_out, const void* topk_weights,
+                          int32_t topk_weights_dtype, float routed_scaling_factor,
                           const int32_t* token_to_row, int32_t M, int32_t top_k, int32_t H,
                           uint16_t* out, moe_stream_t stream);
 

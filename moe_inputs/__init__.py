@@ -104,7 +104,7 @@ class MoEConfig:
     I: int                 # intermediate size
     E: int                 # global experts
     top_k: int
-    act: str = "swiglu"    # "swiglu" | "relu2"
+    act: str = "swiglu"    # gated: "swiglu", "geglu"; non-gated: "relu2", "gelu", "relu", "silu", "identity"
     scale_mode: str = "per_token"   # "global_one" | "per_token"
     seed: int = 0          # hidden + routing
     weight_seed: int = 0   # expert weights
@@ -112,6 +112,7 @@ class MoEConfig:
     local_offset: int = 0
     num_local: Optional[int] = None
     fc2_input_scale: float = 1.0
+    routed_scaling_factor: float = 1.0
 
     @property
     def El(self) -> int:
@@ -119,7 +120,7 @@ class MoEConfig:
 
     @property
     def gated(self) -> bool:
-        return self.act == "swiglu"
+        return self.act in ("swiglu", "geglu")
 
     @property
     def N1(self) -> int:

@@ -15,9 +15,12 @@ from .build import LIB as LIB_PATH
 _lib = None
 
 MOE_OK = 0
-MOE_ACT_SWIGLU, MOE_ACT_RELU2 = 0, 1
+MOE_ACT_SWIGLU, MOE_ACT_RELU2, MOE_ACT_GEGLU, MOE_ACT_GELU, MOE_ACT_RELU, MOE_ACT_SILU, MOE_ACT_IDENTITY = range(7)
+ACTIVATIONS = {"swiglu": MOE_ACT_SWIGLU, "relu2": MOE_ACT_RELU2, "geglu": MOE_ACT_GEGLU, "gelu": MOE_ACT_GELU,
+               "relu": MOE_ACT_RELU, "silu": MOE_ACT_SILU, "identity": MOE_ACT_IDENTITY}
 MOE_SCALE_GLOBAL_ONE, MOE_SCALE_PER_TOKEN = 0, 1
 MOE_DEV_DUPLICATE_EXPERT, MOE_DEV_TIMEOUT = 1, 2
+MOE_WEIGHTS_F32, MOE_WEIGHTS_BF16 = 0, 1
 
 EXPORTED = [
     "moe_status_string", "moe_abi_version", "moe_quantize_input", "moe_plan_capacity",
@@ -60,9 +63,9 @@ def _declare(lib):
         "moe_forward_workspace_layout": (c_int32, [c_int32, c_int32, ctypes.POINTER(WeightsT), c_int32,
                                                    ctypes.POINTER(c_size_t)]),
         "moe_grouped_fp4_forward": (c_int32, [P, P, P, c_int32, c_int32, P, P, P, ctypes.POINTER(WeightsT),
-                                              P, c_size_t, P, c_float, c_int32, P, P, P, c_size_t, P,
-                                              ctypes.POINTER(c_void_p), c_int32, P]),
-        "moe_finalize": (c_int32, [P, P, P, c_int32, c_int32, c_int32, P, P]),
+                                              P, c_size_t, P, c_int32, c_float, c_float, c_int32, P, P, P,
+                                              c_size_t, P, ctypes.POINTER(c_void_p), c_int32, P]),
+        "moe_finalize": (c_int32, [P, P, c_int32, c_float, P, c_int32, c_int32, c_int32, P, P]),
         "moe_debug_gemm1": (c_int32, [P, P, c_int32, c_int32, P, P, P, ctypes.POINTER(WeightsT), P,
                                       c_size_t, c_int32, P, P, c_size_t, P, P]),
     }
@@ -178,9 +181,18 @@ def moe_forward_workspace_layout(M, top_k, w: WeightsT, do_finalize) -> list[int
     return list(arr)
 
 
+def _weights_dtype(topk_weights) -> int:
+    import torch
+    if topk_weights.dtype == torch.bfloat16:
+        return MOE_WEIGHTS_BF16
+    if topk_weights.dtype == torch.float32:
+        return MOE_WEIGHTS_F32
+    raise MoEError("topk_weights must be float32 or bfloat16")
+
+
 def moe_grouped_fp4_forward(padded_offsets, row_to_slot, token_to_row, xq, xsf, xs, w: WeightsT, prepared,
                             topk_weights, fc2_input_scale, do_finalize, out, gemm2_out, workspace,
-                            dev_status, step_events=None, stream=None):
+                            dev_status, step_events=None, stream=None, routed_scaling_factor=1.0):
     M, k = token_to_row.shape
     ev = None
     nev = 0
@@ -193,15 +205,16 @@ def moe_grouped_fp4_forward(padded_offsets, row_to_slot, token_to_row, xq, xsf, 
     _check(lib().moe_grouped_fp4_forward(
         _ptr(padded_offsets), _ptr(row_to_slot), _ptr(token_to_row), M, k, _ptr(xq), _ptr(xsf), _ptr(xs),
         ctypes.byref(w), _ptr(prepared), prepared.numel() * prepared.element_size(), _ptr(topk_weights),
-        float(fc2_input_scale), int(do_finalize), _ptr(out), _ptr(gemm2_out), _ptr(workspace),
+        _weights_dtype(topk_weights), float(routed_scaling_factor), float(fc2_input_scale), int(do_finalize), _ptr(out), _ptr(gemm2_out), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(dev_status), ev, nev, _stream(stream)),
         "moe_grouped_fp4_forward")
 
 
-def moe_finalize(gemm2_out, topk_weights, token_to_row, out, stream=None):
+def moe_finalize(gemm2_out, topk_weights, token_to_row, out, stream=None, routed_scaling_factor=1.0):
     M, k = token_to_row.shape
     H = out.shape[1]
-    _check(lib().moe_finalize(_ptr(gemm2_out), _ptr(topk_weights), _ptr(token_to_row), M, k, H, _ptr(out),
+    _check(lib().moe_finalize(_ptr(gemm2_out), _ptr(topk_weights), _weights_dtype(topk_weights),
+                              float(routed_scaling_factor), _ptr(token_to_row), M, k, H, _ptr(out),
                               _stream(stream)), "moe_finalize")
 
 

@@ -17,7 +17,7 @@ namespace {
 
 moe_status_t check_weights(const moe_nvfp4_weights_t* w) {
   MOE_CHECK(w != nullptr, MOE_ERR_INVALID_ARGUMENT);
-  MOE_CHECK(w->activation == MOE_ACT_SWIGLU || w->activation == MOE_ACT_RELU2, MOE_ERR_INVALID_ARGUMENT);
+  MOE_CHECK(w->activation >= MOE_ACT_SWIGLU && w->activation <= MOE_ACT_IDENTITY, MOE_ERR_INVALID_ARGUMENT);
   MOE_CHECK(w->num_local_experts >= 1 && w->hidden > 0 && w->inter > 0, MOE_ERR_INVALID_ARGUMENT);
   MOE_CHECK(w->num_local_experts <= kMaxLocalExperts, MOE_ERR_UNSUPPORTED_SHAPE);
   MOE_CHECK(w->hidden % 128 == 0 && w->inter % 128 == 0, MOE_ERR_UNSUPPORTED_SHAPE);
@@ -96,6 +96,7 @@ GemmLaunch gemm1_launch(const Dims& d, const WorkspaceLayout& L, const Bufs& b, 
   g.top_k = top_k;
   g.inter = static_cast<int>(d.I);
   g.gated = d.gated;
+  g.act = d.act;
   g.g2 = 1.0f;
   g.out = b.iq;
   g.out_sf = b.isf;
@@ -181,7 +182,8 @@ extern "C" moe_status_t moe_grouped_fp4_forward(const int32_t* padded_offsets, c
                                                 const int32_t* token_to_row, int32_t M, int32_t top_k,
                                                 const uint8_t* xq, const uint8_t* xsf, const float* xs,
                                                 const moe_nvfp4_weights_t* w, const void* prepared,
-                                                size_t prepared_bytes, const float* topk_weights,
+                                                size_t prepared_bytes, const void* topk_weights,
+                                                int32_t topk_weights_dtype, float routed_scaling_factor,
                                                 float fc2_input_scale, int32_t do_finalize, uint16_t* out,
                                                 uint16_t* gemm2_out, void* workspace, size_t workspace_bytes,
                                                 int32_t* dev_status, void* const* step_events,
@@ -196,6 +198,10 @@ extern "C" moe_status_t moe_grouped_fp4_forward(const int32_t* padded_offsets, c
                             workspace, workspace_bytes, dev_status, L.total);
   if (st != MOE_OK) return st;
   MOE_CHECK(isfinite(fc2_input_scale) && fc2_input_scale > 0.0f, MOE_ERR_INVALID_ARGUMENT);
+  MOE_CHECK(isfinite(routed_scaling_factor), MOE_ERR_INVALID_ARGUMENT);
+  MOE_CHECK(topk_weights_dtype == MOE_WEIGHTS_F32 || topk_weights_dtype == MOE_WEIGHTS_BF16,
+            MOE_ERR_INVALID_ARGUMENT);
+  const size_t wbytes = static_cast<size_t>(M) * top_k * (topk_weights_dtype == MOE_WEIGHTS_BF16 ? 2 : 4);
   MOE_CHECK(num_step_events == 0 || (num_step_events == 5 && step_events != nullptr), MOE_ERR_INVALID_ARGUMENT);
   if (M == 0) return MOE_OK;
   MOE_CHECK(token_to_row && topk_weights, MOE_ERR_INVALID_ARGUMENT);
@@ -208,7 +214,7 @@ extern "C" moe_status_t moe_grouped_fp4_forward(const int32_t* padded_offsets, c
     MOE_CHECK(!overlaps(out, ob, xq, static_cast<size_t>(M) * d.H / 2) &&
                   !overlaps(out, ob, xsf, static_cast<size_t>(M) * d.H / 16) &&
                   !overlaps(out, ob, xs, static_cast<size_t>(M) * 4) &&
-                  !overlaps(out, ob, topk_weights, static_cast<size_t>(M) * top_k * 4) &&
+                  !overlaps(out, ob, topk_weights, wbytes) &&
                   !overlaps(out, ob, token_to_row, static_cast<size_t>(M) * top_k * 4) &&
                   !overlaps(out, ob, workspace, L.total) && !overlaps(out, ob, prepared, prepared_bytes),
               MOE_ERR_OVERLAP);
@@ -268,6 +274,7 @@ extern "C" moe_status_t moe_grouped_fp4_forward(const int32_t* padded_offsets, c
   g2.top_k = top_k;
   g2.inter = static_cast<int>(d.I);
   g2.gated = false;  // GEMM2 columns are plain output columns
+  g2.act = MOE_ACT_IDENTITY;
   g2.g2 = fc2_input_scale;
   g2.out = rows_out;
   g2.out_sf = nullptr;
@@ -277,7 +284,8 @@ extern "C" moe_status_t moe_grouped_fp4_forward(const int32_t* padded_offsets, c
   if (st != MOE_OK) return st;
   if ((st = mark(3)) != MOE_OK) return st;
   if (fin) {
-    st = launch_finalize(rows_out, topk_weights, token_to_row, M, top_k, static_cast<int>(d.H), out, s);
+    st = launch_finalize(rows_out, topk_weights, topk_weights_dtype == MOE_WEIGHTS_BF16, routed_scaling_factor,
+                         token_to_row, M, top_k, static_cast<int>(d.H), out, s);
     if (st != MOE_OK) return st;
   }
   return mark(4);

@@ -16,6 +16,7 @@ namespace moe {
 struct Dims {
   int64_t El, H, I, N1;
   bool gated;
+  int act;
   int64_t N1p;  // W1 rows per expert in the prepared layout
   int64_t Hp;   // H padded to 256: GEMM1 K, and W2 rows per expert
   int64_t Ip;   // I padded to 256: GEMM2 K
@@ -26,7 +27,8 @@ inline Dims make_dims(const moe_nvfp4_weights_t* w) {
   d.El = w->num_local_experts;
   d.H = w->hidden;
   d.I = w->inter;
-  d.gated = w->activation == MOE_ACT_SWIGLU;
+  d.act = w->activation;
+  d.gated = w->activation == MOE_ACT_SWIGLU || w->activation == MOE_ACT_GEGLU;
   d.N1 = d.gated ? 2 * d.I : d.I;
   d.N1p = roundup64(d.N1, kTileN);
   d.Hp = roundup64(d.H, kTileK);
@@ -108,6 +110,7 @@ struct GemmLaunch {
   int64_t cap, El, K, Kp, N, Np;
   int top_k, inter;
   bool gated;
+  int act;
   float g2;
   void* out;
   uint8_t* out_sf;
@@ -119,8 +122,8 @@ moe_status_t launch_gemm(const GemmLaunch& g, cudaStream_t s);
 moe_status_t launch_permute(const int32_t* padded_offsets, int El, const int32_t* row_to_slot, int top_k,
                             int64_t cap, const uint8_t* xq, const uint8_t* xsf, int H, uint8_t* aq, uint8_t* asf,
                             int32_t* tile_counters, cudaStream_t s);
-moe_status_t launch_finalize(const uint16_t* rows, const float* topk_weights, const int32_t* token_to_row, int M,
-                             int top_k, int H, uint16_t* out, cudaStream_t s);
+moe_status_t launch_finalize(const uint16_t* rows, const void* topk_weights, int weights_bf16, float rsf,
+                             const int32_t* token_to_row, int M, int top_k, int H, uint16_t* out, cudaStream_t s);
 moe_status_t launch_prepare_matrix(const uint8_t* src, const uint8_t* src_sf, int E, int rows, int rows_p, int K,
                                    int gated_inter, uint8_t* dst, uint8_t* dst_sf, cudaStream_t s);
 

@@ -7,6 +7,8 @@
 // multiplications and additions; unrouted slots and their scores ignored); Megatron-Core
 // core.inference.moe.flashinfer_nvfp4 (_pad_fc1: gate and up halves interleaved in row
 // blocks so a GEMM tile sees both; prepare_routed_nvfp4_weights(out=...) refreshes in place).
+#include <math.h>
+
 #include "common.cuh"
 #include "host_util.h"
 #include "layout.h"
@@ -98,11 +100,18 @@ __global__ void __launch_bounds__(256) prepare_matrix_kernel(const uint8_t* __re
 constexpr int kMaxSlots = 8;
 constexpr int kBatchedFinalizeMaxTokens = 256;
 
+// route weight of slot i: FP32 or BF16 storage, times the routed scaling factor
+__device__ __forceinline__ float route_weight(const void* w, int bf16, int64_t i, float rsf) {
+  const float v = bf16 ? __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t*>(w)[i]) << 16)
+                       : static_cast<const float*>(w)[i];
+  return __fmul_rn(v, rsf);
+}
+
 template <bool BATCHED>
 __global__ void __launch_bounds__(256) finalize_kernel(const uint16_t* __restrict__ rows,
-                                                       const float* __restrict__ topk_weights,
-                                                       const int32_t* __restrict__ token_to_row, int M, int top_k,
-                                                       int H, uint16_t* __restrict__ out) {
+                                                       const void* __restrict__ topk_weights, int weights_bf16,
+                                                       float rsf, const int32_t* __restrict__ token_to_row, int M,
+                                                       int top_k, int H, uint16_t* __restrict__ out) {
   pdl_trigger();
   pdl_wait();
   const int t = blockIdx.y;
@@ -115,7 +124,7 @@ __global__ void __launch_bounds__(256) finalize_kernel(const uint16_t* __restric
     for (int j = 0; j < top_k; ++j) {
       const int r = token_to_row[static_cast<int64_t>(t) * top_k + j];
       if (r < 0) continue;
-      const float w = topk_weights[static_cast<int64_t>(t) * top_k + j];
+      const float w = route_weight(topk_weights, weights_bf16, static_cast<int64_t>(t) * top_k + j, rsf);
       const uint4 v = *reinterpret_cast<const uint4*>(rows + static_cast<int64_t>(r) * H + c8 * 8);
       const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -137,7 +146,7 @@ __global__ void __launch_bounds__(256) finalize_kernel(const uint16_t* __restric
       w[j] = 0.0f;
       v[j] = make_uint4(0, 0, 0, 0);
       if (r[j] >= 0) {
-        w[j] = topk_weights[static_cast<int64_t>(t) * top_k + j0 + j];
+        w[j] = route_weight(topk_weights, weights_bf16, static_cast<int64_t>(t) * top_k + j0 + j, rsf);
         v[j] = *reinterpret_cast<const uint4*>(rows + static_cast<int64_t>(r[j]) * H + c8 * 8);
       }
     }
@@ -178,16 +187,16 @@ moe_status_t launch_permute(const int32_t* padded_offsets, int El, const int32_t
                     xq, xsf, H, aq, asf, tile_counters);
 }
 
-moe_status_t launch_finalize(const uint16_t* rows, const float* topk_weights, const int32_t* token_to_row, int M,
-                             int top_k, int H, uint16_t* out, cudaStream_t s) {
+moe_status_t launch_finalize(const uint16_t* rows, const void* topk_weights, int weights_bf16, float rsf,
+                             const int32_t* token_to_row, int M, int top_k, int H, uint16_t* out, cudaStream_t s) {
   if (M == 0) return MOE_OK;
   const int threads = 256;
   const int bx = (H / 8 + threads - 1) / threads;
   if (M <= kBatchedFinalizeMaxTokens)
-    return launch_pdl(finalize_kernel<true>, dim3(bx, M), dim3(threads), 0, s, rows, topk_weights, token_to_row, M,
-                      top_k, H, out);
-  return launch_pdl(finalize_kernel<false>, dim3(bx, M), dim3(threads), 0, s, rows, topk_weights, token_to_row, M,
-                    top_k, H, out);
+    return launch_pdl(finalize_kernel<true>, dim3(bx, M), dim3(threads), 0, s, rows, topk_weights, weights_bf16, rsf,
+                      token_to_row, M, top_k, H, out);
+  return launch_pdl(finalize_kernel<false>, dim3(bx, M), dim3(threads), 0, s, rows, topk_weights, weights_bf16, rsf,
+                    token_to_row, M, top_k, H, out);
 }
 
 moe_status_t launch_prepare_matrix(const uint8_t* src, const uint8_t* src_sf, int E, int rows, int rows_p, int K,
@@ -201,10 +210,13 @@ moe_status_t launch_prepare_matrix(const uint8_t* src, const uint8_t* src_sf, in
 
 using namespace moe;
 
-extern "C" moe_status_t moe_finalize(const uint16_t* gemm2_out, const float* topk_weights,
-                                     const int32_t* token_to_row, int32_t M, int32_t top_k, int32_t H, uint16_t* out,
-                                     moe_stream_t stream) {
+extern "C" moe_status_t moe_finalize(const uint16_t* gemm2_out, const void* topk_weights, int32_t topk_weights_dtype,
+                                     float routed_scaling_factor, const int32_t* token_to_row, int32_t M,
+                                     int32_t top_k, int32_t H, uint16_t* out, moe_stream_t stream) {
   MOE_CHECK(M >= 0 && top_k >= 1 && H > 0, MOE_ERR_INVALID_ARGUMENT);
+  MOE_CHECK(topk_weights_dtype == MOE_WEIGHTS_F32 || topk_weights_dtype == MOE_WEIGHTS_BF16,
+            MOE_ERR_INVALID_ARGUMENT);
+  MOE_CHECK(isfinite(routed_scaling_factor), MOE_ERR_INVALID_ARGUMENT);
   MOE_CHECK(H % 128 == 0, MOE_ERR_UNSUPPORTED_SHAPE);
   MOE_CHECK(M < 65536, MOE_ERR_UNSUPPORTED_SHAPE);
   if (M == 0) return MOE_OK;
@@ -212,9 +224,11 @@ extern "C" moe_status_t moe_finalize(const uint16_t* gemm2_out, const float* top
   MOE_CHECK(aligned16(gemm2_out) && aligned16(topk_weights) && aligned16(token_to_row) && aligned16(out),
             MOE_ERR_MISALIGNED);
   const size_t ob = static_cast<size_t>(M) * H * 2;
-  MOE_CHECK(!overlaps(out, ob, topk_weights, static_cast<size_t>(M) * top_k * 4) &&
+  const size_t wb = static_cast<size_t>(M) * top_k * (topk_weights_dtype == MOE_WEIGHTS_BF16 ? 2 : 4);
+  MOE_CHECK(!overlaps(out, ob, topk_weights, wb) &&
                 !overlaps(out, ob, token_to_row, static_cast<size_t>(M) * top_k * 4) &&
                 !overlaps(out, ob, gemm2_out, 1),
             MOE_ERR_OVERLAP);
-  return launch_finalize(gemm2_out, topk_weights, token_to_row, M, top_k, H, out, as_stream(stream));
+  return launch_finalize(gemm2_out, topk_weights, topk_weights_dtype == MOE_WEIGHTS_BF16, routed_scaling_factor,
+                         token_to_row, M, top_k, H, out, as_stream(stream));
 }

@@ -8,9 +8,11 @@
 // matrix; NVFP4_BLOCK_SIZE, FLOAT4_E2M1_MAX, FLOAT8_E4M3_MAX); vLLM flashinfer_utils
 // (quantize_nvfp4_per_token_input: linear scale-factor layout).
 //
-// One warp per row: the row is read once for its amax (per-token mode) and once more, from
-// L1/L2, for the blocks. Lane i handles 16-value blocks i, i+32, ...; each block is two
-// 16-byte loads and one 8-byte store of codes, so a warp's loads and stores are contiguous.
+// Few activation rows (up to 512) of up to 8192 values: one CTA per row with the row in
+// registers (one global read, short latency chain). Otherwise one warp per row; the row is read once for its
+// amax and once more, from L1/L2, for the blocks. Lane i handles 16-value blocks i, i+32,
+// ...; each block is two 16-byte loads and one 8-byte store of codes, so a warp's loads and
+// stores are contiguous.
 #include "common.cuh"
 #include "host_util.h"
 
@@ -95,6 +97,65 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const uint16_t* __re
   }
 }
 
+// Rows of at most kRowCtaMaxCols values: one 128-thread CTA per row, each thread keeping up
+// to four 16-value blocks in registers, so the row is read from global memory once; the
+// per-token amax is a block reduction.
+constexpr int kRowCtaThreads = 128;
+constexpr int kRowCtaBlocks = 4;
+constexpr int kRowCtaMaxCols = kRowCtaThreads * kRowCtaBlocks * kBlock;  // 8192
+// with many rows the warp-per-row kernel keeps more loads in flight per SM and wins
+constexpr int kRowCtaMaxRows = 512;
+
+__global__ void __launch_bounds__(kRowCtaThreads) quantize_rows_cta_kernel(
+    const uint16_t* __restrict__ x, int64_t rows, int cols, int64_t ld, int per_row, uint8_t* __restrict__ data,
+    uint8_t* __restrict__ sf, float* __restrict__ dec_out) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ float red[kRowCtaThreads / 32];
+  const int nblk = cols / kBlock;
+  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+    const uint16_t* row = x + r * ld;
+    float v[kRowCtaBlocks][16];
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kRowCtaBlocks; ++j) {
+      const int b = threadIdx.x + j * kRowCtaThreads;
+      if (b < nblk) {
+        load_block16(row + b * kBlock, v[j]);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[j][i]));
+      }
+    }
+    float g = 1.0f, dec = 1.0f;
+    if (per_row) {
+      amax = warp_max(amax);
+      if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+      __syncthreads();
+      amax = red[0];
+#pragma unroll
+      for (int w = 1; w < kRowCtaThreads / 32; ++w) amax = fmaxf(amax, red[w]);
+      if (amax > 0.0f) {
+        g = __fdiv_rn(kGlobalNumerator, amax);
+        dec = __fdiv_rn(amax, kGlobalNumerator);
+      }
+    }
+    uint8_t* drow = data + r * (cols / 2);
+    uint8_t* srow = sf + r * nblk;
+#pragma unroll
+    for (int j = 0; j < kRowCtaBlocks; ++j) {
+      const int b = threadIdx.x + j * kRowCtaThreads;
+      if (b < nblk) {
+        uint32_t codes[2];
+        const uint32_t q = quantize_block16(v[j], g, codes);
+        *reinterpret_cast<uint2*>(drow + b * 8) = make_uint2(codes[0], codes[1]);
+        srow[b] = static_cast<uint8_t>(q);
+      }
+    }
+    if (threadIdx.x == 0) dec_out[r] = dec;
+    __syncthreads();  // red[] is reused by the next row
+  }
+}
+
 // amax over each matrix (non-negative floats order like their bit patterns)
 __global__ void __launch_bounds__(256) matrix_amax_kernel(const uint16_t* __restrict__ w, int64_t mat_elems,
                                                           float* __restrict__ amax) {
@@ -148,6 +209,13 @@ extern "C" moe_status_t moe_quantize_input(const uint16_t* x, int32_t M, int32_t
                 !overlaps(x, xbytes, xsf, static_cast<size_t>(M) * H / 16) &&
                 !overlaps(x, xbytes, xs, static_cast<size_t>(M) * 4),
             MOE_ERR_OVERLAP);
+  if (H <= kRowCtaMaxCols && M <= kRowCtaMaxRows) {
+    const int64_t cap = static_cast<int64_t>(num_sms()) * 16;
+    const unsigned grid = static_cast<unsigned>(M < cap ? M : cap);
+    return launch_pdl(quantize_rows_cta_kernel, dim3(grid), dim3(kRowCtaThreads), 0, as_stream(stream), x,
+                      static_cast<int64_t>(M), static_cast<int>(H), ld_x,
+                      static_cast<int>(mode == MOE_SCALE_PER_TOKEN ? 1 : 0), xq, xsf, xs);
+  }
   return launch_pdl(quantize_rows_kernel, dim3(rows_grid(M)), dim3(256), 0, as_stream(stream), x,
                     static_cast<int64_t>(M), static_cast<int>(H), ld_x,
                     static_cast<int>(mode == MOE_SCALE_PER_TOKEN ? kGPerRow : kGOne),

@@ -30,15 +30,19 @@ class NVFP4RoutedMoE:
 
     def __init__(self, w1, w1_sf, w1_alpha, w2, w2_sf, w2_alpha, activation: str = "swiglu",
                  num_experts: int | None = None, local_expert_offset: int = 0,
-                 fc2_input_scale: float = 1.0, scale_mode: str = "per_token"):
+                 fc2_input_scale: float = 1.0, scale_mode: str = "per_token",
+                 routed_scaling_factor: float = 1.0):
         El, N1, Hh = w1.shape
         self.El = El
         self.H = Hh * 2
         self.I = w2.shape[2] * 2
-        self.act = L.MOE_ACT_SWIGLU if activation == "swiglu" else L.MOE_ACT_RELU2
+        if activation not in L.ACTIVATIONS:
+            raise ValueError(f"activation must be one of {sorted(L.ACTIVATIONS)}")
+        self.act = L.ACTIVATIONS[activation]
         self.num_experts = num_experts if num_experts is not None else El + local_expert_offset
         self.local_expert_offset = local_expert_offset
         self.fc2_input_scale = float(fc2_input_scale)
+        self.routed_scaling_factor = float(routed_scaling_factor)
         self.scale_mode = L.MOE_SCALE_PER_TOKEN if scale_mode == "per_token" else L.MOE_SCALE_GLOBAL_ONE
         self.device = w1.device
         self.linear = (w1, w1_sf, w1_alpha, w2, w2_sf, w2_alpha)
@@ -90,11 +94,11 @@ class NVFP4RoutedMoE:
         L.moe_grouped_fp4_forward(b["padded_offsets"], b["row_to_slot"], b["token_to_row"], b["xq"], b["xsf"],
                                   b["xs"], self.w, self.prepared, topk_weights, self.fc2_input_scale,
                                   do_finalize, b["out"], b["gemm2_out"], b["ws"], b["dev_status"],
-                                  step_events=step_events)
+                                  step_events=step_events, routed_scaling_factor=self.routed_scaling_factor)
 
     def forward(self, x: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor,
                 do_finalize: bool = True, step_events=None):
-        """x [M, H] bf16, topk_ids [M, k] int32, topk_weights [M, k] f32 (all on the GPU).
+        """x [M, H] bf16, topk_ids [M, k] int32, topk_weights [M, k] f32 or bf16 (all on the GPU).
 
         Returns out [M, H] bf16, or (gemm2_out [capacity, H], topk_weights, token_to_row)
         when do_finalize is False. The returned tensors are the layer's reusable buffers.

@@ -21,8 +21,10 @@ Readings:
   products (each product ``e2m1 * e4m3`` pair is exact in float64).
 * GEMM1 output ``y = acc * xs[t] * alpha1[e]``; SwiGLU ``h = silu(g) * u``
   with ``silu(g) = g / (1 + exp(-g))``, gate = rows ``[0, I)`` and up = rows
-  ``[I, 2I)`` of W1; squared-ReLU ``h = max(y, 0)**2``; both in float64, then
-  rounded to BF16 (the BF16 intermediate).
+  ``[I, 2I)`` of W1; squared-ReLU ``h = max(y, 0)**2``; the other typed
+  activations of the cuDNN backend page (GeGLU, GELU, ReLU, SiLU, Identity) with
+  GELU in its erf form; all in float64, then rounded to BF16 (the BF16
+  intermediate).
 * The intermediate is requantised by the block quantiser with the static
   encode scale ``fc2_input_scale`` (1.0 = "a global scale of one"); GEMM2 output
   ``y2 = acc2 / fc2_input_scale * alpha2[e]``, rounded to BF16 (the expert
@@ -95,15 +97,37 @@ def silu(g: np.ndarray) -> np.ndarray:
         return g / (1.0 + np.exp(-g))
 
 
+GATED_ACTIVATIONS = ("swiglu", "geglu")
+ACTIVATIONS = ("swiglu", "relu2", "geglu", "gelu", "relu", "silu", "identity")
+
+
+def gelu(x: np.ndarray) -> np.ndarray:
+    """GELU in its defining form x * Phi(x) = x/2 * (1 + erf(x / sqrt(2)))."""
+    from scipy.special import erf
+    return 0.5 * x * (1.0 + erf(x / np.sqrt(2.0)))
+
+
 def activation(y: np.ndarray, act: str, inter: int) -> np.ndarray:
-    """float64 pre-activations [rows, N1] -> float64 activations [rows, I]."""
-    if act == "swiglu":
+    """float64 pre-activations [rows, N1] -> float64 activations [rows, I].
+
+    Gated (FC1 rows [gate; up], N1 = 2I): swiglu = silu(g) * u, geglu = gelu(g) * u.
+    Non-gated (N1 = I): relu2 = max(y, 0)^2, gelu, relu = max(y, 0), silu, identity.
+    """
+    if act in GATED_ACTIVATIONS:
         g = y[:, :inter]
         u = y[:, inter:2 * inter]
-        return silu(g) * u
+        return (silu(g) if act == "swiglu" else gelu(g)) * u
     if act == "relu2":
         r = np.maximum(y, 0.0)
         return r * r
+    if act == "gelu":
+        return gelu(y)
+    if act == "relu":
+        return np.maximum(y, 0.0)
+    if act == "silu":
+        return silu(y)
+    if act == "identity":
+        return y.copy()
     raise ValueError(act)
 
 
@@ -130,14 +154,20 @@ def expert_chain(A_deq: np.ndarray, xs: np.ndarray, pack1: ExpertPack, pack2: Ex
             "rows": bf16_round(y2)}
 
 
-def finalize(rows: np.ndarray, topk_weights: np.ndarray, token_to_row: np.ndarray) -> np.ndarray:
+def finalize(rows: np.ndarray, topk_weights: np.ndarray, token_to_row: np.ndarray,
+             routed_scaling_factor: float = 1.0) -> np.ndarray:
     """Ordered FP32 combine of BF16 expert rows -> BF16 [M, H] (as float64 values).
 
     ``acc = 0``; for j = 0..k-1 in order, skipping masked slots:
-    ``acc = acc + w[t, j] * row`` with a separate FP32 multiply and add;
+    ``acc = acc + w'[t, j] * row`` with a separate FP32 multiply and add;
     ``out = bf16(acc)``. A token whose slots are all masked gets a zero row.
+    ``w' = fp32(w * routed_scaling_factor)`` (the AlphaMoE page's scalar applied to each
+    routed contribution, read as scaling the route weight); BF16 weights enter as their
+    exact FP32 values.
     """
     w = np.asarray(topk_weights, dtype=F32)
+    if routed_scaling_factor != 1.0:
+        w = (w * F32(routed_scaling_factor)).astype(F32)
     t2r = np.asarray(token_to_row)
     M, k = t2r.shape
     H = rows.shape[1]
@@ -155,7 +185,8 @@ def finalize(rows: np.ndarray, topk_weights: np.ndarray, token_to_row: np.ndarra
 def forward(xq: np.ndarray, xsf: np.ndarray, xs: np.ndarray, topk_ids: np.ndarray,
             topk_weights: np.ndarray, weights: ExpertWeights, act: str,
             local_expert_offset: int = 0, fc2_input_scale: float = 1.0,
-            plan: Optional[dict] = None, allow_duplicates: bool = False) -> dict:
+            plan: Optional[dict] = None, allow_duplicates: bool = False,
+            routed_scaling_factor: float = 1.0) -> dict:
     """The whole path on quantised activations, in plan row order.
 
     Returns the plan and, per row of the padded plan (NaN in padding rows):
@@ -188,7 +219,8 @@ def forward(xq: np.ndarray, xsf: np.ndarray, xs: np.ndarray, topk_ids: np.ndarra
                          fc2_input_scale)
         for key in ("preact", "act_bf16", "icodes", "isf", "rows"):
             res[key][prow] = r[key]
-    res["out"] = finalize(np.nan_to_num(res["rows"]), topk_weights, plan["token_to_row"])
+    res["out"] = finalize(np.nan_to_num(res["rows"]), topk_weights, plan["token_to_row"],
+                          routed_scaling_factor)
     res["plan"] = plan
     return res
 
@@ -196,7 +228,7 @@ def forward(xq: np.ndarray, xsf: np.ndarray, xs: np.ndarray, topk_ids: np.ndarra
 def forward_tokens(tokens: Sequence[int], xq: np.ndarray, xsf: np.ndarray, xs: np.ndarray,
                    topk_ids: np.ndarray, topk_weights: np.ndarray, weights: ExpertWeights,
                    act: str, local_expert_offset: int = 0,
-                   fc2_input_scale: float = 1.0) -> dict:
+                   fc2_input_scale: float = 1.0, routed_scaling_factor: float = 1.0) -> dict:
     """Output rows of selected tokens only, each computed on its own.
 
     Every step of the path is row-local (per-token scales, static FC2 input
@@ -225,5 +257,5 @@ def forward_tokens(tokens: Sequence[int], xq: np.ndarray, xsf: np.ndarray, xs: n
                 sub_rows.append(rows[(t, j)])
     R = np.array(sub_rows) if sub_rows else np.zeros((0, weights.hidden))
     w = np.asarray(topk_weights)[list(tokens)]
-    out = finalize(R if len(R) else np.zeros((1, weights.hidden)), w, t2r)
+    out = finalize(R if len(R) else np.zeros((1, weights.hidden)), w, t2r, routed_scaling_factor)
     return {"out": out, "rows": rows}

@@ -45,7 +45,7 @@ def oracle_expert(cfg_key: tuple, l: int):
 def cfg_key(cfg: mi.MoEConfig) -> tuple:
     # only what the weights depend on (name and routing fields do not matter)
     return ("w", 0, cfg.H, cfg.I, cfg.E, 1, cfg.act, "per_token", 0, cfg.weight_seed, 0.0,
-            cfg.local_offset, cfg.num_local, 1.0)
+            cfg.local_offset, cfg.num_local, 1.0, 1.0)
 
 
 def oracle_weights(cfg: mi.MoEConfig) -> O.ExpertWeights:
@@ -71,7 +71,8 @@ class Problem:
         self.q2 = pkg.quantize_weights(self.w2_bf16)
         self.layer = pkg.NVFP4RoutedMoE(*self.q1, *self.q2, activation=cfg.act, num_experts=cfg.E,
                                         local_expert_offset=cfg.local_offset,
-                                        fc2_input_scale=cfg.fc2_input_scale, scale_mode=cfg.scale_mode)
+                                        fc2_input_scale=cfg.fc2_input_scale, scale_mode=cfg.scale_mode,
+                                        routed_scaling_factor=cfg.routed_scaling_factor)
 
     def run(self, do_finalize=True):
         res = self.layer.forward(self.x, self.ids_t, self.tw_t, do_finalize=do_finalize)
@@ -89,7 +90,8 @@ class Problem:
         xq, xsf, xs = self.oracle_inputs()
         return O.forward(xq, xsf, xs, self.ids, self.tw, oracle_weights(self.cfg), self.cfg.act,
                          local_expert_offset=self.cfg.local_offset,
-                         fc2_input_scale=self.cfg.fc2_input_scale, **kw)
+                         fc2_input_scale=self.cfg.fc2_input_scale,
+                         routed_scaling_factor=self.cfg.routed_scaling_factor, **kw)
 
 
 def assert_close_output(got: np.ndarray, ref: np.ndarray, what: str = ""):

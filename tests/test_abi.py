@@ -101,25 +101,25 @@ def test_forward_validation(lib):
     f = lib.moe_grouped_fp4_forward
     null = None
     # missing prepared buffer
-    st = f(16, 32, 48, 4, 2, 64, 80, 96, ctypes.byref(w), null, 0, 112, 1.0, 1, 128, null, 144, 1 << 30,
+    st = f(16, 32, 48, 4, 2, 64, 80, 96, ctypes.byref(w), null, 0, 112, 0, 1.0, 1.0, 1, 128, null, 144, 1 << 30,
            160, null, 0, null)
     assert st == 1
     # workspace too small
     pb = pkg.moe_prepared_weights_bytes(w)
-    st = f(16, 32, 48, 4, 2, 64, 80, 96, ctypes.byref(w), 4096, pb, 112, 1.0, 1, 128, null, 144, 16,
+    st = f(16, 32, 48, 4, 2, 64, 80, 96, ctypes.byref(w), 4096, pb, 112, 0, 1.0, 1.0, 1, 128, null, 144, 16,
            160, null, 0, null)
     assert st == 4
     # bad fc2_input_scale
     ws = pkg.moe_forward_workspace_bytes(4, 2, w, 1)
-    st = f(16, 32, 48, 4, 2, 64, 80, 96, ctypes.byref(w), 4096, pb, 112, 0.0, 1, 1 << 40, null, 1 << 36, ws,
+    st = f(16, 32, 48, 4, 2, 64, 80, 96, ctypes.byref(w), 4096, pb, 112, 0, 1.0, 0.0, 1, 1 << 40, null, 1 << 36, ws,
            160, null, 0, null)
     assert st == 1
     # out overlapping the workspace
-    st = f(16, 32, 48, 4, 2, 64, 80, 96, ctypes.byref(w), 4096, pb, 112, 1.0, 1, 1 << 36, null, 1 << 36, ws,
+    st = f(16, 32, 48, 4, 2, 64, 80, 96, ctypes.byref(w), 4096, pb, 112, 0, 1.0, 1.0, 1, 1 << 36, null, 1 << 36, ws,
            160, null, 0, null)
     assert st == 6
     # step events: count must be 0 or 5
-    st = f(16, 32, 48, 4, 2, 64, 80, 96, ctypes.byref(w), 4096, pb, 112, 1.0, 1, 1 << 40, null, 1 << 36, ws,
+    st = f(16, 32, 48, 4, 2, 64, 80, 96, ctypes.byref(w), 4096, pb, 112, 0, 1.0, 1.0, 1, 1 << 40, null, 1 << 36, ws,
            160, null, 3, null)
     assert st == 1
 
@@ -127,10 +127,12 @@ def test_forward_validation(lib):
 @host_only
 def test_finalize_validation(lib):
     f = lib.moe_finalize
-    assert f(16, 32, 48, 4, 2, 100, 64, None) == 2                 # H % 128
-    assert f(16, 32, 48, 4, 0, 128, 64, None) == 1                 # top_k == 0
-    assert f(16, 32, 48, 4, 2, 128, 24, None) == 3                 # misaligned out
-    assert f(16, 32, 48, 0, 2, 128, 64, None) == 0                 # M == 0 no-op
+    assert f(16, 32, 0, 1.0, 48, 4, 2, 100, 64, None) == 2         # H % 128
+    assert f(16, 32, 0, 1.0, 48, 4, 0, 128, 64, None) == 1         # top_k == 0
+    assert f(16, 32, 0, 1.0, 48, 4, 2, 128, 24, None) == 3         # misaligned out
+    assert f(16, 32, 0, 1.0, 48, 0, 2, 128, 64, None) == 0         # M == 0 no-op
+    assert f(16, 32, 5, 1.0, 48, 4, 2, 128, 64, None) == 1         # bad weights dtype
+    assert f(16, 32, 0, float("inf"), 48, 4, 2, 128, 64, None) == 1  # non-finite scaling factor
 
 
 def test_missing_library_fails_loudly(tmp_path, monkeypatch):

@@ -207,3 +207,37 @@ def test_cuda_graph_replay_with_new_routing():
     assert np.array_equal(got, ref)
     p2 = Problem(cfg2)
     assert_close_output(got, p2.oracle_forward()["out"], "graph")
+
+
+@pytest.mark.parametrize("act", ["geglu", "gelu", "relu", "silu", "identity"])
+def test_forward_other_activations(act):
+    # the typed activations of the cuDNN backend page beyond SwiGLU / squared-ReLU
+    gated = act == "geglu"
+    cfg = mi.MoEConfig(f"act_{act}", M=300, H=384, I=384 if not gated else 256, E=8, top_k=2, act=act,
+                       seed=21, weight_seed=21)
+    p = Problem(cfg)
+    ref = p.oracle_forward()
+    assert_close_output(bf16_np(p.run(True)), ref["out"], act)
+    # the fused requantiser stays bit-exact on the kernel's own intermediate
+    h = _gpu_debug(p, 1)
+    p.run(True)
+    b = p.bufs(True)
+    offs = pkg.moe_forward_workspace_layout(cfg.M, cfg.top_k, p.layer.w, 1)
+    ws = to_np(b["ws"])
+    cap = b["capacity"]
+    real = to_np(b["row_to_slot"])[:cap] >= 0
+    iq = ws[offs[2]:offs[2] + cap * cfg.I // 2].reshape(cap, cfg.I // 2)[real]
+    codes, _ = Q.quantize_blocks(bf16_np(h)[real].astype(np.float32), np.float32(1.0))
+    assert np.array_equal(iq, pack_e2m1(codes))
+
+
+def test_forward_routed_scaling_factor_and_bf16_weights():
+    cfg = SMALL["swiglu_ragged"].with_(routed_scaling_factor=2.5)
+    p = Problem(cfg)
+    assert_close_output(bf16_np(p.run(True)), p.oracle_forward()["out"], "rsf")
+    # BF16 route weights: the same result as FP32 weights holding the same (BF16) values
+    tw16 = p.tw_t.to(torch.bfloat16)
+    out16 = bf16_np(p.layer.forward(p.x, p.ids_t, tw16)).copy()
+    out32 = bf16_np(p.layer.forward(p.x, p.ids_t, tw16.float())).copy()
+    torch.cuda.synchronize()
+    assert np.array_equal(out16, out32)

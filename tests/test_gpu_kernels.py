@@ -189,3 +189,17 @@ def test_permute_bitexact(name, overrides):
     if kp != cfg.H:
         pad = sf_tiles_to_linear(ws[offs[1]:offs[2]], cap, kp // 16)[real][:, cfg.H // 16:]
         assert not pad.any()
+
+
+@pytest.mark.parametrize("rsf", [1.0, 0.75, 3.0])
+def test_finalize_bf16_weights_and_scaling_bitexact(rsf):
+    M, k, H, R = 50, 6, 512, 200
+    rng = np.random.default_rng(11)
+    rows = torch.from_numpy(rng.standard_normal((R, H)).astype(np.float32)).to(torch.bfloat16).to(DEV)
+    t2r = rng.integers(-1, R, size=(M, k)).astype(np.int32)
+    w16 = torch.from_numpy(rng.random((M, k)).astype(np.float32)).to(torch.bfloat16)
+    out = torch.empty(M, H, dtype=torch.bfloat16, device=DEV)
+    pkg.moe_finalize(rows, w16.to(DEV), torch.from_numpy(t2r).to(DEV), out, routed_scaling_factor=rsf)
+    torch.cuda.synchronize()
+    ref = O.finalize(bf16_np(rows), w16.float().numpy(), t2r, routed_scaling_factor=rsf)
+    assert np.array_equal(bf16_np(out), ref)

@@ -245,3 +245,55 @@ def test_forward_tokens_matches_forward():
 
 def test_plan_capacity_matches_plan_module():
     assert P.plan_capacity(4096, 8, 256) == 32768 + 127 * 256  # already a multiple of 128
+
+
+def test_gelu_closed_forms():
+    x = np.linspace(-8, 8, 401)
+    g = O.gelu(x)
+    # x*Phi(x) - (-x)*Phi(-x) = x, Phi(0) = 1/2, GELU(x) -> x and -> 0 in the tails
+    assert np.allclose(g - O.gelu(-x), x, rtol=0, atol=1e-14)
+    assert O.gelu(np.array([0.0]))[0] == 0.0
+    assert abs(O.gelu(np.array([1e-9]))[0] / 1e-9 - 0.5) < 1e-8
+    assert abs(O.gelu(np.array([10.0]))[0] - 10.0) < 1e-20 + 10.0 * 1e-15
+    # Phi(1) = 0.841344746068543 (standard normal table)
+    assert abs(O.gelu(np.array([1.0]))[0] - 0.841344746068543) < 1e-12
+
+
+@pytest.mark.parametrize("act", ["relu", "silu", "identity", "gelu"])
+def test_nongated_activations_elementwise(act):
+    y = np.array([[-2.0, -0.5, 0.0, 0.5, 3.0]])
+    h = O.activation(y, act, 5)
+    if act == "relu":
+        assert h.tolist() == [[0.0, 0.0, 0.0, 0.5, 3.0]]
+    elif act == "identity":
+        assert h.tolist() == y.tolist()
+    elif act == "silu":
+        assert np.array_equal(h, O.silu(y))
+    else:
+        assert np.array_equal(h, O.gelu(y))
+
+
+def test_geglu_uses_gate_half():
+    # gate rows give g, up rows give u: geglu = gelu(g) * u, swapping halves differs
+    y = np.array([[2.0, -1.0, 0.5, 4.0]])      # I = 2: g = [2, -1], u = [0.5, 4]
+    h = O.activation(y, "geglu", 2)
+    assert np.allclose(h, O.gelu(np.array([[2.0, -1.0]])) * np.array([[0.5, 4.0]]), rtol=0, atol=0)
+    assert not np.allclose(h, O.gelu(np.array([[0.5, 4.0]])) * np.array([[2.0, -1.0]]))
+
+
+def test_activation_names_cover_cudnn_page():
+    assert set(O.ACTIVATIONS) == {"swiglu", "relu2", "geglu", "gelu", "relu", "silu", "identity"}
+    with pytest.raises(ValueError):
+        O.activation(np.zeros((1, 2)), "tanh", 1)
+
+
+def test_routed_scaling_factor_scales_route_weights():
+    rows = np.array([[1.0, -2.0], [0.5, 4.0]])
+    t2r = np.array([[0, 1]], np.int32)
+    w = np.array([[0.25, 0.5]], np.float32)
+    a = O.finalize(rows, w, t2r, routed_scaling_factor=2.0)
+    b = O.finalize(rows, (w * 2).astype(np.float32), t2r)
+    assert np.array_equal(a, b)
+    # 0.5*1 + 1.0*0.5 = 1.0 ; 0.5*-2 + 1.0*4 = 3.0 (exact)
+    assert a.tolist() == [[1.0, 3.0]]
+    assert np.array_equal(O.finalize(rows, w, t2r, 1.0), O.finalize(rows, w, t2r))
