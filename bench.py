@@ -35,6 +35,9 @@ NV = 0.5 + 1.0 / 16.0      # NVFP4 bytes per element: packed E2M1 + one E4M3 sca
 FP4_OVER_BF16 = 13.5 / 2.25  # nominal dense ratio (GB300): FP4 tensor rate / BF16 tensor rate
 
 
+OUTPUT_MODES = {"finalized": 1, "accumulate": 2}
+
+
 def workload_name(cfg) -> str:
     s = f"{cfg.name}: T={cfg.M} H={cfg.H} I={cfg.I} E={cfg.E} top_k={cfg.top_k} {cfg.act}"
     if cfg.num_local is not None:
@@ -166,12 +169,12 @@ def setup_gpu(cfg, dev):
 def traffic_from_profiles(kernel: str, workload: str):
     """DRAM bytes per launch of `kernel` from the committed ncu summary
     (profiles/dram_traffic.txt), or None when the kernel's source has changed since the
-    counters were taken (sha256 of gemm.cu followed by common.cuh)."""
+    counters were taken (sha256 of gemm_kernel.cuh followed by common.cuh)."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(p):
         return None
     csrc = os.path.join(ROOT, "nvfp4_routed_moe_sort_gb300", "csrc")
-    h = hashlib.sha256(open(os.path.join(csrc, "gemm.cu"), "rb").read()
+    h = hashlib.sha256(open(os.path.join(csrc, "gemm_kernel.cuh"), "rb").read()
                        + open(os.path.join(csrc, "common.cuh"), "rb").read()).hexdigest()[:16]
     with open(p) as f:
         for ln in f:
@@ -192,13 +195,16 @@ def run_gpu(args, cfg, rank, world):
     ids_t = torch.from_numpy(ids).to(dev)
     tw_t = torch.from_numpy(tw).to(dev)
     M, k = ids.shape
-    b = layer.buffers(M, k, True)
+    mode = OUTPUT_MODES[args.output]
+    b = layer.buffers(M, k, mode)
+    # accumulated output: every step adds into this caller-owned tensor
+    acc_out = torch.zeros(M, cfg.H, dtype=torch.bfloat16, device=dev) if mode == 2 else None
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     n_ev = 8
     K, W = args.steps, args.warmup
 
     # the timed step: one CUDA-graph replay of the whole path
-    graph = layer.capture(x, ids_t, tw_t, True)
+    graph = layer.capture(x, ids_t, tw_t, mode, out=acc_out)
     for i in range(W):
         flush.zero_()
         graph.replay()
@@ -231,7 +237,7 @@ def run_gpu(args, cfg, rank, world):
             e.record()
     for _ in range(W):
         flush.zero_()
-        layer.forward(x, ids_t, tw_t)
+        layer.forward(x, ids_t, tw_t, mode, out=acc_out)
     torch.cuda.synchronize()
     torch.cuda._sleep(int(60e6))   # ~30 ms at 2 GHz
     for e in evs:
@@ -240,12 +246,12 @@ def run_gpu(args, cfg, rank, world):
         layer.quantize(x, b)
         e[1].record()
         layer.plan(ids_t, b)
-        layer.experts(tw_t, b, True, step_events=e[2:7])
+        layer.experts(tw_t, b, mode, step_events=e[2:7], out=acc_out)
         e[7].record()
     torch.cuda.synchronize()
     kern_times = [[e[j].elapsed_time(e[j + 1]) for j in range(n_ev - 1)] for e in evs]
     eager_ms = float(np.mean([e[0].elapsed_time(e[7]) for e in evs]))
-    assert layer.device_status(M, k, True) == 0, "device status word set"
+    assert layer.device_status(M, k, mode) == 0, "device status word set"
     names = ["quantize", "plan", "permute", "gemm1", "gemm2", "finalize"]
     per = {n: [t[c] for t in kern_times] for c, n in enumerate(names)}
     steps_ms = step_times
@@ -284,6 +290,7 @@ def run_gpu(args, cfg, rank, world):
         "config": {"workload": workload_name(cfg), "tokens": M, "hidden": cfg.H, "inter": cfg.I,
                    "experts": cfg.E, "top_k": k, "routed_rows": R, "active_experts": active,
                    "l2": "flushed between steps (256 MB write outside the timed events)",
+                   "output": args.output,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roof,
         "step_roofline": {"frac": step_roof_s / (ms * 1e-3), "bytes": stepw["bytes"], "flops": stepw["flops"],
@@ -454,6 +461,8 @@ def main():
     ap.add_argument("--workload", default="decode_t8", choices=sorted(mi.CONFIGS))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--output", default="finalized", choices=sorted(OUTPUT_MODES),
+                    help="finalized: ordered combine into a fresh out; accumulate: FP32 reduction into out")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer run (profiling)")
     ap.add_argument("--set", action="append", default=[], metavar="FIELD=VALUE",
                     help="override a workload field (e.g. E=64 M=1024) for smaller profiling cases")

@@ -44,7 +44,7 @@
 extern "C" {
 #endif
 
-#define MOE_NVFP4_ABI_VERSION 1
+#define MOE_NVFP4_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define MOE_API __attribute__((visibility("default")))
@@ -83,8 +83,29 @@ typedef enum {
   MOE_ACT_IDENTITY = 6
 } moe_activation_t;
 
-/* Storage of the route weights ([CUDNN] "Routing weights: ... unpacked FP32 / BF16"). */
-typedef enum { MOE_WEIGHTS_F32 = 0, MOE_WEIGHTS_BF16 = 1 } moe_weights_dtype_t;
+/* Storage of the route weights ([CUDNN] "Routing weights: packed, or unpacked FP32 / BF16").
+ * MOE_WEIGHTS_PACKED: one int32 per slot holding the BF16 score in bits 31..16 and the
+ * expert id, unsigned, in bits 15..0 (the pages name the packed form but not its bits; this
+ * is the reading taken). [FROST]: "packed routing scores retain BF16 rounding". */
+typedef enum { MOE_WEIGHTS_F32 = 0, MOE_WEIGHTS_BF16 = 1, MOE_WEIGHTS_PACKED = 2 } moe_weights_dtype_t;
+
+/* Storage of the routing ids given to moe_plan: plain int32 ids, or the packed int32 slots
+ * of MOE_WEIGHTS_PACKED (id = bits 15..0, so 0..65535; ids past the local range are masked). */
+typedef enum { MOE_IDS_INT32 = 0, MOE_IDS_PACKED = 1 } moe_ids_format_t;
+
+/* What moe_grouped_fp4_forward writes (its `do_finalize` argument).
+ *  MOE_OUTPUT_UNFINALIZED  [CUDNN] MoEFinalizeConfig(do_finalize=False): BF16 expert rows
+ *  MOE_OUTPUT_FINALIZED    ordered, deterministic FP32 combine into a fresh `out` ([FROST])
+ *  MOE_OUTPUT_ACCUMULATE   [ALPHA]: contributions added in FP32 to the values already in
+ *                          `out` (an FP32 copy of out is made first, out is rewritten once at
+ *                          the end); the FP32 additions run in GEMM2's epilogue in whatever
+ *                          order the tiles finish, so results may differ in the last bits
+ *                          from run to run */
+typedef enum {
+  MOE_OUTPUT_UNFINALIZED = 0,
+  MOE_OUTPUT_FINALIZED = 1,
+  MOE_OUTPUT_ACCUMULATE = 2
+} moe_output_mode_t;
 
 /* Activation global scale: [CUDNN] "a global scale of one" (prepare_activations) or
  * [MCORE]/[VLLM] one FP32 decode scale per token computed online. */
@@ -98,6 +119,11 @@ typedef enum { MOE_SCALE_GLOBAL_ONE = 0, MOE_SCALE_PER_TOKEN = 1 } moe_act_scale
  *   w2       [El, H, I/2]   packed E2M1
  *   w2_sf    [El, H, I/16]  E4M3 block scales
  *   w2_alpha [El]           FP32 per-expert dequant of W2
+ *   w1_gate_alpha [El]      optional FP32 per-expert dequant of the gate rows of a gated W1
+ *                           ([ALPHA] output1_scale_gate_scalar, applied to each gate
+ *                           accumulator before the activation, while w1_alpha plays
+ *                           output1_scale_scalar for the up rows); NULL = w1_alpha for both.
+ *                           Ignored by non-gated activations.
  * H and I must be multiples of 128 ([CUDNN] "hidden_size and intermediate_size must be
  * multiples of 128"); 1 <= El <= 512. moe_prepare_weights reads the pointers; the forward
  * reads only the sizes and `activation` (the prepared buffer is self-contained). */
@@ -112,6 +138,7 @@ typedef struct {
   int32_t hidden;
   int32_t inter;
   int32_t activation; /* moe_activation_t */
+  const float* w1_gate_alpha;
 } moe_nvfp4_weights_t;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -138,8 +165,10 @@ MOE_API moe_status_t moe_quantize_input(const uint16_t* x, int32_t M, int32_t H,
  * segment padded to a multiple of 128 rows" (moe_sort); "assignments to non-local experts
  * are masked out"; [MCORE] "rows whose routing entries are -1 contribute zero";
  * [FROST] "expert IDs outside [0, num_experts) mark unrouted slots".
- *   topk_ids       [M, top_k] int32 global expert ids; ids outside
- *                  [local_expert_offset, local_expert_offset + El) are masked (not errors)
+ *   topk_ids       [M, top_k] int32 global expert ids (topk_ids_format MOE_IDS_INT32), or the
+ *                  packed slots of MOE_WEIGHTS_PACKED (MOE_IDS_PACKED: id = bits 15..0);
+ *                  ids outside [local_expert_offset, local_expert_offset + El) are masked
+ *                  (not errors)
  *   counts         [El]       routed rows per local expert (out)
  *   padded_offsets [El + 1]   segment starts, padded_offsets[l+1] - padded_offsets[l] =
  *                             roundup(counts[l], 128) (out)
@@ -152,7 +181,7 @@ MOE_API moe_status_t moe_quantize_input(const uint16_t* x, int32_t M, int32_t H,
  * ---------------------------------------------------------------------------------------- */
 MOE_API size_t moe_plan_capacity(int32_t M, int32_t top_k, int32_t num_local_experts);
 MOE_API size_t moe_plan_workspace_bytes(int32_t M, int32_t top_k, int32_t num_local_experts);
-MOE_API moe_status_t moe_plan(const int32_t* topk_ids, int32_t M, int32_t top_k, int32_t num_experts,
+MOE_API moe_status_t moe_plan(const int32_t* topk_ids, int32_t topk_ids_format, int32_t M, int32_t top_k, int32_t num_experts,
                       int32_t local_expert_offset, int32_t num_local_experts, int32_t* counts,
                       int32_t* padded_offsets, int32_t* row_to_slot, int32_t* token_to_row,
                       void* workspace, size_t workspace_bytes, int32_t* dev_status,
@@ -177,7 +206,7 @@ MOE_API moe_status_t moe_plan(const int32_t* topk_ids, int32_t M, int32_t top_k,
  *    threads) race on it and must be serialised by the caller.
  * ---------------------------------------------------------------------------------------- */
 #define MOE_PLAN_NOALLOC_SCRATCH_BYTES (1 << 20)
-MOE_API moe_status_t moe_plan_noalloc(const int32_t* topk_ids, int32_t M, int32_t top_k, int32_t num_experts,
+MOE_API moe_status_t moe_plan_noalloc(const int32_t* topk_ids, int32_t topk_ids_format, int32_t M, int32_t top_k, int32_t num_experts,
                               int32_t local_expert_offset, int32_t num_local_experts, int32_t* counts,
                               int32_t* padded_offsets, int32_t* row_to_slot, int32_t* token_to_row,
                               int32_t* dev_status, moe_stream_t stream);
@@ -191,7 +220,8 @@ MOE_API moe_status_t moe_plan_noalloc(const int32_t* topk_ids, int32_t M, int32_
  * [num_mats] = amax/2688 (1 for an all-zero matrix), with g_enc = 2688/amax in the block
  * rule of moe_quantize_input. `amax_scratch` holds num_mats floats of device scratch.
  *
- * moe_prepare_weights - lays the linear weights out for the kernels: SwiGLU gate and up rows
+ * moe_prepare_weights - lays the linear weights out for the kernels (w1_gate_alpha, or w1_alpha
+ * when it is NULL, is copied into the buffer as the gate scalars): SwiGLU gate and up rows
  * interleaved in 128-row blocks (so one 256-row GEMM1 tile holds matching gate and up
  * columns), rows padded to 256 per expert, block scales in 128-row x 4-scale tiles.
  * The buffer (moe_prepared_weights_bytes) is self-contained; refreshing it in place keeps
@@ -212,17 +242,23 @@ MOE_API moe_status_t moe_prepare_weights(const moe_nvfp4_weights_t* w, void* pre
  *   padded_offsets, row_to_slot, token_to_row  from moe_plan
  *   xq, xsf, xs        activation pack from moe_quantize_input ([M, H/2], [M, H/16], [M])
  *   w, prepared        sizes/activation and the moe_prepare_weights buffer
- *   topk_weights       [M, top_k] route weights, FP32 or BF16 per topk_weights_dtype (entries of
- *                      masked slots are never read)
+ *   topk_weights       [M, top_k] route weights, FP32, BF16 or packed per topk_weights_dtype
+ *                      (entries of masked slots are never read)
  *   routed_scaling_factor  finite FP32 scalar applied to each routed contribution ([ALPHA]
  *                      routed_scaling_factor): the combine uses w' = fp32(w * factor); 1.0 = none
  *   fc2_input_scale    static FP32 encode scale of the intermediate (1.0 = global scale one);
  *                      GEMM2 rows are multiplied by alpha2[e] / fc2_input_scale
- *   do_finalize = 1    out [M, H] BF16 = bf16(sum_j w'[t,j] * gemm2 row), ordered FP32
+ *   do_finalize (moe_output_mode_t):
+ *     MOE_OUTPUT_FINALIZED    out [M, H] BF16 = bf16(sum_j w'[t,j] * gemm2 row), ordered FP32
  *                      multiply + add over ascending j ([FROST] ordered combine); gemm2_out
  *                      may be NULL (rows go to the workspace)
- *   do_finalize = 0    gemm2_out [capacity, H] BF16 expert outputs, bf16(y2) in real rows,
- *                      padding rows untouched; out may be NULL
+ *     MOE_OUTPUT_UNFINALIZED  gemm2_out [capacity, H] BF16 expert outputs, bf16(y2) in real
+ *                      rows, padding rows untouched; out may be NULL
+ *     MOE_OUTPUT_ACCUMULATE   out [M, H] BF16 (read and written) = bf16(out + sum_j y2 * w'[t,j])
+ *                      with y2 the FP32 GEMM2 row (not rounded to BF16), FP32 additions in
+ *                      any order ([ALPHA]: accumulation in an FP32 [M, H] buffer initialised
+ *                      from out, converted back once); rows of tokens with no local slot keep
+ *                      their value; gemm2_out may be NULL
  *   workspace          moe_forward_workspace_bytes(...) bytes of device scratch
  *   step_events        optional array of `num_step_events` (0 or 5) cudaEvent_t recorded on
  *                      `stream` before permute, gemm1, gemm2, finalize and at the end
@@ -231,7 +267,8 @@ MOE_API size_t moe_forward_workspace_bytes(int32_t M, int32_t top_k, const moe_n
                                    int32_t do_finalize);
 /* Byte offsets inside the forward workspace of: [0] permuted activations [cap, H/2],
  * [1] their scales (128x4 tiles), [2] intermediate [cap, I/2], [3] its scales,
- * [4] gemm2 rows [cap, H] (do_finalize only), [5] total. For tests and tools. */
+ * [4] gemm2 rows [cap, H] BF16 (MOE_OUTPUT_FINALIZED) or the FP32 accumulator [M, H]
+ * (MOE_OUTPUT_ACCUMULATE), 0 otherwise, [5] total. For tests and tools. */
 MOE_API moe_status_t moe_forward_workspace_layout(int32_t M, int32_t top_k, const moe_nvfp4_weights_t* w,
                                           int32_t do_finalize, size_t offsets[6]);
 MOE_API moe_status_t moe_grouped_fp4_forward(const int32_t* padded_offsets, const int32_t* row_to_slot,
@@ -249,7 +286,7 @@ MOE_API moe_status_t moe_grouped_fp4_forward(const int32_t* padded_offsets, cons
  * S7  moe_finalize - [CUDNN] moe_unpermute; [FROST] "ordered, separate FP32 multiplication
  * and addition"; unrouted slots and their scores are ignored.
  *   gemm2_out    [rows, H] BF16 expert rows
- *   topk_weights [M, top_k] route weights, FP32 or BF16 (topk_weights_dtype)
+ *   topk_weights [M, top_k] route weights, FP32, BF16 or packed (topk_weights_dtype)
  *   routed_scaling_factor  finite FP32 scalar, w' = fp32(w * factor) ([ALPHA])
  *   token_to_row [M, top_k] row per slot or -1;  out [M, H] BF16
  * out[t,:] = bf16(acc) with acc = 0; acc = acc + w'[t,j]*row for j = 0..top_k-1, row != -1.

@@ -9,7 +9,9 @@ from . import _lib
 from ._lib import (  # noqa: F401
     ACTIVATIONS, EXPORTED, MOE_ACT_GEGLU, MOE_ACT_GELU, MOE_ACT_IDENTITY, MOE_ACT_RELU, MOE_ACT_RELU2,
     MOE_ACT_SILU, MOE_ACT_SWIGLU, MOE_DEV_DUPLICATE_EXPERT, MOE_DEV_TIMEOUT,
-    MOE_SCALE_GLOBAL_ONE, MOE_SCALE_PER_TOKEN, MOE_WEIGHTS_BF16, MOE_WEIGHTS_F32, MoEError, WeightsT, lib, make_weights,
+    MOE_IDS_INT32, MOE_IDS_PACKED, MOE_OUTPUT_ACCUMULATE, MOE_OUTPUT_FINALIZED, MOE_OUTPUT_UNFINALIZED,
+    MOE_SCALE_GLOBAL_ONE, MOE_SCALE_PER_TOKEN, MOE_WEIGHTS_BF16, MOE_WEIGHTS_F32, MOE_WEIGHTS_PACKED, MoEError,
+    WeightsT, lib, make_weights,
     moe_abi_version, moe_debug_gemm1, moe_finalize, moe_forward_workspace_bytes,
     moe_forward_workspace_layout, moe_grouped_fp4_forward, moe_plan, moe_plan_capacity,
     moe_plan_workspace_bytes, moe_plan_noalloc, moe_prepare_weights, moe_prepared_weights_bytes, moe_quantize_input,

@@ -20,7 +20,9 @@ ACTIVATIONS = {"swiglu": MOE_ACT_SWIGLU, "relu2": MOE_ACT_RELU2, "geglu": MOE_AC
                "relu": MOE_ACT_RELU, "silu": MOE_ACT_SILU, "identity": MOE_ACT_IDENTITY}
 MOE_SCALE_GLOBAL_ONE, MOE_SCALE_PER_TOKEN = 0, 1
 MOE_DEV_DUPLICATE_EXPERT, MOE_DEV_TIMEOUT = 1, 2
-MOE_WEIGHTS_F32, MOE_WEIGHTS_BF16 = 0, 1
+MOE_WEIGHTS_F32, MOE_WEIGHTS_BF16, MOE_WEIGHTS_PACKED = 0, 1, 2
+MOE_IDS_INT32, MOE_IDS_PACKED = 0, 1
+MOE_OUTPUT_UNFINALIZED, MOE_OUTPUT_FINALIZED, MOE_OUTPUT_ACCUMULATE = 0, 1, 2
 
 EXPORTED = [
     "moe_status_string", "moe_abi_version", "moe_quantize_input", "moe_plan_capacity",
@@ -41,7 +43,7 @@ class WeightsT(ctypes.Structure):
         ("w1", c_void_p), ("w1_sf", c_void_p), ("w1_alpha", c_void_p),
         ("w2", c_void_p), ("w2_sf", c_void_p), ("w2_alpha", c_void_p),
         ("num_local_experts", c_int32), ("hidden", c_int32), ("inter", c_int32),
-        ("activation", c_int32),
+        ("activation", c_int32), ("w1_gate_alpha", c_void_p),
     ]
 
 
@@ -53,9 +55,10 @@ def _declare(lib):
         "moe_quantize_input": (c_int32, [P, c_int32, c_int32, c_int64, c_int32, P, P, P, P]),
         "moe_plan_capacity": (c_size_t, [c_int32, c_int32, c_int32]),
         "moe_plan_workspace_bytes": (c_size_t, [c_int32, c_int32, c_int32]),
-        "moe_plan": (c_int32, [P, c_int32, c_int32, c_int32, c_int32, c_int32, P, P, P, P, P, c_size_t,
-                               P, P]),
-        "moe_plan_noalloc": (c_int32, [P, c_int32, c_int32, c_int32, c_int32, c_int32, P, P, P, P, P, P]),
+        "moe_plan": (c_int32, [P, c_int32, c_int32, c_int32, c_int32, c_int32, c_int32, P, P, P, P, P,
+                               c_size_t, P, P]),
+        "moe_plan_noalloc": (c_int32, [P, c_int32, c_int32, c_int32, c_int32, c_int32, c_int32, P, P, P, P,
+                                       P, P]),
         "moe_quantize_weights": (c_int32, [P, c_int32, c_int32, c_int32, P, P, P, P, P]),
         "moe_prepared_weights_bytes": (c_size_t, [ctypes.POINTER(WeightsT)]),
         "moe_prepare_weights": (c_int32, [ctypes.POINTER(WeightsT), P, c_size_t, P]),
@@ -112,9 +115,10 @@ def _stream(stream):
 
 
 def make_weights(num_local_experts: int, hidden: int, inter: int, activation: int,
-                 w1=None, w1_sf=None, w1_alpha=None, w2=None, w2_sf=None, w2_alpha=None) -> WeightsT:
+                 w1=None, w1_sf=None, w1_alpha=None, w2=None, w2_sf=None, w2_alpha=None,
+                 w1_gate_alpha=None) -> WeightsT:
     return WeightsT(_ptr(w1), _ptr(w1_sf), _ptr(w1_alpha), _ptr(w2), _ptr(w2_sf), _ptr(w2_alpha),
-                    num_local_experts, hidden, inter, activation)
+                    num_local_experts, hidden, inter, activation, _ptr(w1_gate_alpha))
 
 
 # ---------------------------------------------------------------- entry points
@@ -137,20 +141,23 @@ def moe_plan_workspace_bytes(M, top_k, num_local_experts) -> int:
 
 
 def moe_plan(topk_ids, num_experts, local_expert_offset, num_local_experts, counts, padded_offsets,
-             row_to_slot, token_to_row, workspace, dev_status, stream=None):
+             row_to_slot, token_to_row, workspace, dev_status, stream=None, packed=False):
+    """packed=True: topk_ids holds packed slots (BF16 score << 16 | expert id)."""
     M, k = topk_ids.shape
     wsb = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    _check(lib().moe_plan(_ptr(topk_ids), M, k, num_experts, local_expert_offset, num_local_experts,
+    fmt = MOE_IDS_PACKED if packed else MOE_IDS_INT32
+    _check(lib().moe_plan(_ptr(topk_ids), fmt, M, k, num_experts, local_expert_offset, num_local_experts,
                           _ptr(counts), _ptr(padded_offsets), _ptr(row_to_slot), _ptr(token_to_row),
                           _ptr(workspace), wsb, _ptr(dev_status), _stream(stream)), "moe_plan")
 
 
 def moe_plan_noalloc(topk_ids, num_experts, local_expert_offset, num_local_experts, counts, padded_offsets,
-                     row_to_slot, token_to_row, dev_status, stream=None):
+                     row_to_slot, token_to_row, dev_status, stream=None, packed=False):
     """moe_plan without a workspace, for callers that cannot allocate device memory (its
     histogram scratch is a fixed 1 MiB array inside the library; see the C header)."""
     M, k = topk_ids.shape
-    _check(lib().moe_plan_noalloc(_ptr(topk_ids), M, k, num_experts, local_expert_offset, num_local_experts,
+    fmt = MOE_IDS_PACKED if packed else MOE_IDS_INT32
+    _check(lib().moe_plan_noalloc(_ptr(topk_ids), fmt, M, k, num_experts, local_expert_offset, num_local_experts,
                                   _ptr(counts), _ptr(padded_offsets), _ptr(row_to_slot), _ptr(token_to_row),
                                   _ptr(dev_status), _stream(stream)), "moe_plan_noalloc")
 
@@ -182,17 +189,21 @@ def moe_forward_workspace_layout(M, top_k, w: WeightsT, do_finalize) -> list[int
 
 
 def _weights_dtype(topk_weights) -> int:
+    """float32 / bfloat16 route weights, or int32 packed slots (BF16 score in bits 31..16)."""
     import torch
     if topk_weights.dtype == torch.bfloat16:
         return MOE_WEIGHTS_BF16
     if topk_weights.dtype == torch.float32:
         return MOE_WEIGHTS_F32
-    raise MoEError("topk_weights must be float32 or bfloat16")
+    if topk_weights.dtype == torch.int32:
+        return MOE_WEIGHTS_PACKED
+    raise MoEError("topk_weights must be float32, bfloat16 or int32 (packed)")
 
 
 def moe_grouped_fp4_forward(padded_offsets, row_to_slot, token_to_row, xq, xsf, xs, w: WeightsT, prepared,
                             topk_weights, fc2_input_scale, do_finalize, out, gemm2_out, workspace,
                             dev_status, step_events=None, stream=None, routed_scaling_factor=1.0):
+    """do_finalize: 0/False unfinalized rows, 1/True ordered finalize, 2 accumulate into out."""
     M, k = token_to_row.shape
     ev = None
     nev = 0
@@ -205,7 +216,8 @@ def moe_grouped_fp4_forward(padded_offsets, row_to_slot, token_to_row, xq, xsf, 
     _check(lib().moe_grouped_fp4_forward(
         _ptr(padded_offsets), _ptr(row_to_slot), _ptr(token_to_row), M, k, _ptr(xq), _ptr(xsf), _ptr(xs),
         ctypes.byref(w), _ptr(prepared), prepared.numel() * prepared.element_size(), _ptr(topk_weights),
-        _weights_dtype(topk_weights), float(routed_scaling_factor), float(fc2_input_scale), int(do_finalize), _ptr(out), _ptr(gemm2_out), _ptr(workspace),
+        _weights_dtype(topk_weights), float(routed_scaling_factor), float(fc2_input_scale), int(do_finalize),
+        _ptr(out), _ptr(gemm2_out), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(dev_status), ev, nev, _stream(stream)),
         "moe_grouped_fp4_forward")
 

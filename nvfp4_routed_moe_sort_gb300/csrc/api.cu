@@ -15,6 +15,8 @@ using namespace moe;
 
 namespace {
 
+bool valid_output_mode(int32_t m) { return m >= MOE_OUTPUT_UNFINALIZED && m <= MOE_OUTPUT_ACCUMULATE; }
+
 moe_status_t check_weights(const moe_nvfp4_weights_t* w) {
   MOE_CHECK(w != nullptr, MOE_ERR_INVALID_ARGUMENT);
   MOE_CHECK(w->activation >= MOE_ACT_SWIGLU && w->activation <= MOE_ACT_IDENTITY, MOE_ERR_INVALID_ARGUMENT);
@@ -45,13 +47,13 @@ Bufs carve(void* ws, const WorkspaceLayout& L) {
 
 struct Prepared {
   const uint8_t *w1, *w1sf, *w2, *w2sf;
-  const float *a1, *a2;
+  const float *a1, *a2, *a1g;
 };
 
 Prepared prepared_ptrs(const void* prepared, const PreparedLayout& L) {
   const uint8_t* b = static_cast<const uint8_t*>(prepared);
   return {b + L.w1, b + L.w1sf, b + L.w2, b + L.w2sf, reinterpret_cast<const float*>(b + L.a1),
-          reinterpret_cast<const float*>(b + L.a2)};
+          reinterpret_cast<const float*>(b + L.a2), reinterpret_cast<const float*>(b + L.a1g)};
 }
 
 // checks shared by the forward and the GEMM1 test hook
@@ -84,6 +86,7 @@ GemmLaunch gemm1_launch(const Dims& d, const WorkspaceLayout& L, const Bufs& b, 
   g.b = pw.w1;
   g.b_sf = pw.w1sf;
   g.alpha = pw.a1;
+  g.alpha_gate = pw.a1g;
   g.xs = xs;
   g.padded_offsets = padded_offsets;
   g.row_to_slot = row_to_slot;
@@ -135,7 +138,8 @@ extern "C" moe_status_t moe_prepare_weights(const moe_nvfp4_weights_t* w, void* 
   MOE_CHECK(w->w1 && w->w1_sf && w->w1_alpha && w->w2 && w->w2_sf && w->w2_alpha && prepared,
             MOE_ERR_INVALID_ARGUMENT);
   MOE_CHECK(aligned16(w->w1) && aligned16(w->w1_sf) && aligned16(w->w1_alpha) && aligned16(w->w2) &&
-                aligned16(w->w2_sf) && aligned16(w->w2_alpha) && aligned16(prepared),
+                aligned16(w->w2_sf) && aligned16(w->w2_alpha) && aligned16(prepared) &&
+                (w->w1_gate_alpha == nullptr || aligned16(w->w1_gate_alpha)),
             MOE_ERR_MISALIGNED);
   const Dims d = make_dims(w);
   const PreparedLayout L = prepared_layout(d);
@@ -154,21 +158,23 @@ extern "C" moe_status_t moe_prepare_weights(const moe_nvfp4_weights_t* w, void* 
   if (st != MOE_OK) return st;
   MOE_CUDA(cudaMemcpyAsync(b + L.a1, w->w1_alpha, d.El * 4, cudaMemcpyDeviceToDevice, s));
   MOE_CUDA(cudaMemcpyAsync(b + L.a2, w->w2_alpha, d.El * 4, cudaMemcpyDeviceToDevice, s));
+  MOE_CUDA(cudaMemcpyAsync(b + L.a1g, w->w1_gate_alpha ? w->w1_gate_alpha : w->w1_alpha, d.El * 4,
+                           cudaMemcpyDeviceToDevice, s));
   return MOE_OK;
 }
 
 extern "C" size_t moe_forward_workspace_bytes(int32_t M, int32_t top_k, const moe_nvfp4_weights_t* w,
                                               int32_t do_finalize) {
-  if (check_weights(w) != MOE_OK || M < 0 || top_k < 1) return 0;
-  return workspace_layout(make_dims(w), M, top_k, do_finalize != 0).total;
+  if (check_weights(w) != MOE_OK || M < 0 || top_k < 1 || !valid_output_mode(do_finalize)) return 0;
+  return workspace_layout(make_dims(w), M, top_k, do_finalize).total;
 }
 
 extern "C" moe_status_t moe_forward_workspace_layout(int32_t M, int32_t top_k, const moe_nvfp4_weights_t* w,
                                                      int32_t do_finalize, size_t offsets[6]) {
   moe_status_t st = check_weights(w);
   if (st != MOE_OK) return st;
-  MOE_CHECK(M >= 0 && top_k >= 1 && offsets, MOE_ERR_INVALID_ARGUMENT);
-  const WorkspaceLayout L = workspace_layout(make_dims(w), M, top_k, do_finalize != 0);
+  MOE_CHECK(M >= 0 && top_k >= 1 && offsets && valid_output_mode(do_finalize), MOE_ERR_INVALID_ARGUMENT);
+  const WorkspaceLayout L = workspace_layout(make_dims(w), M, top_k, do_finalize);
   offsets[0] = L.aq;
   offsets[1] = L.asf;
   offsets[2] = L.iq;
@@ -190,16 +196,17 @@ extern "C" moe_status_t moe_grouped_fp4_forward(const int32_t* padded_offsets, c
                                                 int32_t num_step_events, moe_stream_t stream) {
   moe_status_t st = check_weights(w);
   if (st != MOE_OK) return st;
-  MOE_CHECK(M >= 0 && top_k >= 1, MOE_ERR_INVALID_ARGUMENT);
+  MOE_CHECK(M >= 0 && top_k >= 1 && valid_output_mode(do_finalize), MOE_ERR_INVALID_ARGUMENT);
   const Dims d = make_dims(w);
-  const bool fin = do_finalize != 0;
-  const WorkspaceLayout L = workspace_layout(d, M, top_k, fin);
+  const bool fin = do_finalize == MOE_OUTPUT_FINALIZED;
+  const bool accum = do_finalize == MOE_OUTPUT_ACCUMULATE;
+  const WorkspaceLayout L = workspace_layout(d, M, top_k, do_finalize);
   st = check_forward_common(padded_offsets, row_to_slot, M, top_k, xq, xsf, xs, w, prepared, prepared_bytes,
                             workspace, workspace_bytes, dev_status, L.total);
   if (st != MOE_OK) return st;
   MOE_CHECK(isfinite(fc2_input_scale) && fc2_input_scale > 0.0f, MOE_ERR_INVALID_ARGUMENT);
   MOE_CHECK(isfinite(routed_scaling_factor), MOE_ERR_INVALID_ARGUMENT);
-  MOE_CHECK(topk_weights_dtype == MOE_WEIGHTS_F32 || topk_weights_dtype == MOE_WEIGHTS_BF16,
+  MOE_CHECK(topk_weights_dtype >= MOE_WEIGHTS_F32 && topk_weights_dtype <= MOE_WEIGHTS_PACKED,
             MOE_ERR_INVALID_ARGUMENT);
   const size_t wbytes = static_cast<size_t>(M) * top_k * (topk_weights_dtype == MOE_WEIGHTS_BF16 ? 2 : 4);
   MOE_CHECK(num_step_events == 0 || (num_step_events == 5 && step_events != nullptr), MOE_ERR_INVALID_ARGUMENT);
@@ -207,7 +214,7 @@ extern "C" moe_status_t moe_grouped_fp4_forward(const int32_t* padded_offsets, c
   MOE_CHECK(token_to_row && topk_weights, MOE_ERR_INVALID_ARGUMENT);
   MOE_CHECK(aligned16(token_to_row) && aligned16(topk_weights), MOE_ERR_MISALIGNED);
   uint16_t* rows_out;
-  if (fin) {
+  if (fin || accum) {
     MOE_CHECK(out != nullptr, MOE_ERR_INVALID_ARGUMENT);
     MOE_CHECK(aligned16(out), MOE_ERR_MISALIGNED);
     const size_t ob = static_cast<size_t>(M) * d.H * 2;
@@ -231,6 +238,7 @@ extern "C" moe_status_t moe_grouped_fp4_forward(const int32_t* padded_offsets, c
   cudaStream_t s = as_stream(stream);
   const Bufs b = carve(workspace, L);
   if (fin) rows_out = b.g;
+  float* acc = accum ? reinterpret_cast<float*>(b.g) : nullptr;
   const Prepared pw = prepared_ptrs(prepared, prepared_layout(d));
   // while the stream is being captured, the marks become external event-record nodes so the
   // caller can read their timestamps after each graph launch
@@ -247,7 +255,8 @@ extern "C" moe_status_t moe_grouped_fp4_forward(const int32_t* padded_offsets, c
   };
   if ((st = mark(0)) != MOE_OK) return st;
   st = launch_permute(padded_offsets, static_cast<int>(d.El), row_to_slot, top_k, L.cap, xq, xsf,
-                      static_cast<int>(d.H), b.aq, b.asf, b.sched, s);
+                      static_cast<int>(d.H), b.aq, b.asf, b.sched, accum ? out : nullptr, acc,
+                      accum ? static_cast<int64_t>(M) * d.H : 0, s);
   if (st != MOE_OK) return st;
   if ((st = mark(1)) != MOE_OK) return st;
   GemmLaunch g1 = gemm1_launch(d, L, b, pw, padded_offsets, row_to_slot, xs, top_k, dev_status);
@@ -256,12 +265,13 @@ extern "C" moe_status_t moe_grouped_fp4_forward(const int32_t* padded_offsets, c
   if (st != MOE_OK) return st;
   if ((st = mark(2)) != MOE_OK) return st;
   GemmLaunch g2;
-  g2.mode = kG2Rows;
+  g2.mode = accum ? kG2Reduce : kG2Rows;
   g2.a = b.iq;
   g2.a_sf = b.isf;
   g2.b = pw.w2;
   g2.b_sf = pw.w2sf;
   g2.alpha = pw.a2;
+  g2.alpha_gate = nullptr;
   g2.xs = nullptr;
   g2.padded_offsets = padded_offsets;
   g2.row_to_slot = row_to_slot;
@@ -276,16 +286,22 @@ extern "C" moe_status_t moe_grouped_fp4_forward(const int32_t* padded_offsets, c
   g2.gated = false;  // GEMM2 columns are plain output columns
   g2.act = MOE_ACT_IDENTITY;
   g2.g2 = fc2_input_scale;
-  g2.out = rows_out;
+  g2.out = accum ? static_cast<void*>(acc) : static_cast<void*>(rows_out);
   g2.out_sf = nullptr;
+  g2.route_w = topk_weights;
+  g2.route_w_dtype = topk_weights_dtype;
+  g2.rsf = routed_scaling_factor;
   g2.dev_status = dev_status;
   g2.tile_counter = b.sched + 1;
   st = launch_gemm(g2, s);
   if (st != MOE_OK) return st;
   if ((st = mark(3)) != MOE_OK) return st;
   if (fin) {
-    st = launch_finalize(rows_out, topk_weights, topk_weights_dtype == MOE_WEIGHTS_BF16, routed_scaling_factor,
-                         token_to_row, M, top_k, static_cast<int>(d.H), out, s);
+    st = launch_finalize(rows_out, topk_weights, topk_weights_dtype, routed_scaling_factor, token_to_row, M, top_k,
+                         static_cast<int>(d.H), out, s);
+    if (st != MOE_OK) return st;
+  } else if (accum) {
+    st = launch_store_acc(acc, static_cast<int64_t>(M) * d.H, out, s);
     if (st != MOE_OK) return st;
   }
   return mark(4);
@@ -300,7 +316,7 @@ extern "C" moe_status_t moe_debug_gemm1(const int32_t* padded_offsets, const int
   if (st != MOE_OK) return st;
   MOE_CHECK(M >= 0 && top_k >= 1 && (mode == 0 || mode == 1), MOE_ERR_INVALID_ARGUMENT);
   const Dims d = make_dims(w);
-  const WorkspaceLayout L = workspace_layout(d, M, top_k, false);
+  const WorkspaceLayout L = workspace_layout(d, M, top_k, MOE_OUTPUT_UNFINALIZED);
   st = check_forward_common(padded_offsets, row_to_slot, M, top_k, xq, xsf, xs, w, prepared, prepared_bytes,
                             workspace, workspace_bytes, dev_status, L.total);
   if (st != MOE_OK) return st;
@@ -311,7 +327,7 @@ extern "C" moe_status_t moe_debug_gemm1(const int32_t* padded_offsets, const int
   const Bufs b = carve(workspace, L);
   const Prepared pw = prepared_ptrs(prepared, prepared_layout(d));
   st = launch_permute(padded_offsets, static_cast<int>(d.El), row_to_slot, top_k, L.cap, xq, xsf,
-                      static_cast<int>(d.H), b.aq, b.asf, b.sched, s);
+                      static_cast<int>(d.H), b.aq, b.asf, b.sched, nullptr, nullptr, 0, s);
   if (st != MOE_OK) return st;
   GemmLaunch g1 = gemm1_launch(d, L, b, pw, padded_offsets, row_to_slot, xs, top_k, dev_status);
   g1.mode = mode == 0 ? kG1Preact : kG1Act;

@@ -94,6 +94,19 @@ __device__ __forceinline__ uint32_t quantize_block16(const float* x, float g, ui
   return q;
 }
 
+// Route weight of slot i stored as FP32, BF16 or packed (BF16 score in bits 31..16),
+// times the routed scaling factor: fp32(w * rsf).
+__device__ __forceinline__ float route_weight(const void* w, int dtype, int64_t i, float rsf) {
+  float v;
+  if (dtype == MOE_WEIGHTS_F32)
+    v = static_cast<const float*>(w)[i];
+  else if (dtype == MOE_WEIGHTS_BF16)
+    v = __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t*>(w)[i]) << 16);
+  else
+    v = __uint_as_float(static_cast<const uint32_t*>(w)[i] & 0xFFFF0000u);
+  return __fmul_rn(v, rsf);
+}
+
 __device__ __forceinline__ float bf16_round_f32(float x) {
   return __bfloat162float(__float2bfloat16_rn(x));
 }

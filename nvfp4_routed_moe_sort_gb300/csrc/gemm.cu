@@ -82,6 +82,10 @@ moe_status_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
   prm.row_to_slot = g.row_to_slot;
   prm.xs = g.xs;
   prm.alpha = g.alpha;
+  prm.alpha_gate = g.alpha_gate;
+  prm.route_w = g.route_w;
+  prm.route_w_dtype = g.route_w_dtype;
+  prm.rsf = g.rsf;
   prm.out = g.out;
   prm.out_sf = g.out_sf;
   prm.dev_status = g.dev_status;
@@ -99,7 +103,7 @@ moe_status_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
   prm.g2 = g.g2;
   const int64_t units_max = (g.cap / kTileM) * prm.n_tiles;
   const size_t smem = static_cast<size_t>(kStages) * kStageBytes + kSmemExtra + (g.El + 1) * 4;
-  if (g.mode == kG2Rows) return gemm::launch_rows(prm, units_max, smem, s);
+  if (g.mode == kG2Rows || g.mode == kG2Reduce) return gemm::launch_rows(g.mode, prm, units_max, smem, s);
   switch (g.act) {
     case MOE_ACT_SWIGLU:
     case MOE_ACT_GEGLU: return gemm::launch_gated(g.mode, g.act, prm, units_max, smem, s);

@@ -45,13 +45,25 @@ struct GemmParams {
   const int32_t* row_to_slot;
   const float* xs;
   const float* alpha;
+  const float* alpha_gate;  // gate rows of a gated GEMM1
   void* out;
   uint8_t* out_sf;
   int32_t* dev_status;
   int32_t* tile_counter;  // zeroed before the launch (by the permute kernel)
   int32_t El, Kp, nkb, N, Np, n_tiles, top_k, inter, gated, act;
   float g2;
+  const void* route_w;  // kG2Reduce: route weights, their storage and the routed scaling factor
+  int32_t route_w_dtype;
+  float rsf;
 };
+
+__host__ __device__ constexpr bool is_g2(int mode) { return mode == kG2Rows || mode == kG2Reduce; }
+
+// out[0..3] += v (FP32 additions performed at L2, in arrival order)
+__device__ __forceinline__ void red_add_f32x4(float* out, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(out), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
 
 __host__ __device__ constexpr bool is_gated(int act) { return act == MOE_ACT_SWIGLU || act == MOE_ACT_GEGLU; }
 
@@ -108,7 +120,7 @@ __device__ __forceinline__ uint32_t requant32_store(const float* h, float g2, ui
 // [128h, 128h+128).
 template <int MODE, int ACT>
 __device__ __forceinline__ void load_acc(uint32_t tmem_row, int half, uint32_t* r, uint64_t* acc_empty) {
-  if (MODE != kG2Rows && is_gated(ACT)) {
+  if (!is_g2(MODE) && is_gated(ACT)) {
     tmem_ld32_issue(tmem_row + half * 64, r);
     tmem_ld32_issue(tmem_row + half * 64 + 32, r + 32);
     tmem_ld32_issue(tmem_row + 128 + half * 64, r + 64);
@@ -148,9 +160,24 @@ __device__ __forceinline__ void epilogue_compute(const GemmParams& p, uint32_t* 
       for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(__uint_as_float(r[32 * c + i]), d2);
       store_bf16x32(orow + 32 * c, v);
     }
+  } else if constexpr (MODE == kG2Reduce) {
+    // acc[t, :] += (y2 * w') for this row's token t, w' = fp32(w * rsf)
+    const float d2 = __fmul_rn(p.alpha[e], __fdiv_rn(1.0f, p.g2));
+    const int col0 = nt * kTileN + half * 128;
+    if (!real || col0 >= p.N) return;
+    const float w = route_weight(p.route_w, p.route_w_dtype, slot, p.rsf);
+    float* orow = static_cast<float*>(p.out) + static_cast<int64_t>(slot / p.top_k) * p.N + col0;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      float v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v[i] = __fmul_rn(__fmul_rn(__uint_as_float(r[4 * c + i]), d2), w);
+      red_add_f32x4(orow + 4 * c, v[0], v[1], v[2], v[3]);
+    }
   } else {
     if (!real) return;
     const float a1 = p.alpha[e];
+    const float a1g = kGated ? p.alpha_gate[e] : a1;  // gate rows' scalar
     const int I = p.inter;
     const int ip16 = static_cast<int>(roundup64(I, kTileK) / 16);  // scale columns of the intermediate
     // intermediate columns [i0, i0 + nout) come from this thread's registers
@@ -162,7 +189,7 @@ __device__ __forceinline__ void epilogue_compute(const GemmParams& p, uint32_t* 
       float* o = static_cast<float*>(p.out) + prow * ld;
 #pragma unroll
       for (int i = 0; i < 128; ++i) {
-        const float y = __fmul_rn(__fmul_rn(__uint_as_float(r[i]), xs_t), a1);
+        const float y = __fmul_rn(__fmul_rn(__uint_as_float(r[i]), xs_t), i < nout ? a1g : a1);
         if (i < nout) o[i0 + i] = y;                    // gate (or all) columns
         else if (kGated) o[I + i0 + i - 64] = y;        // up columns
       }
@@ -176,12 +203,13 @@ __device__ __forceinline__ void epilogue_compute(const GemmParams& p, uint32_t* 
       float h[32];
       // the activation is a compile-time constant: each kernel carries only its own code
 #define MOE_Y(idx) __fmul_rn(__fmul_rn(__uint_as_float(r[idx]), xs_t), a1)
+#define MOE_YG(idx) __fmul_rn(__fmul_rn(__uint_as_float(r[idx]), xs_t), a1g)
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         if constexpr (ACT == MOE_ACT_SWIGLU) {
-          h[i] = bf16_round_f32(__fmul_rn(silu_f32(MOE_Y(32 * c + i)), MOE_Y(64 + 32 * c + i)));
+          h[i] = bf16_round_f32(__fmul_rn(silu_f32(MOE_YG(32 * c + i)), MOE_Y(64 + 32 * c + i)));
         } else if constexpr (ACT == MOE_ACT_GEGLU) {
-          h[i] = bf16_round_f32(__fmul_rn(gelu_f32(MOE_Y(32 * c + i)), MOE_Y(64 + 32 * c + i)));
+          h[i] = bf16_round_f32(__fmul_rn(gelu_f32(MOE_YG(32 * c + i)), MOE_Y(64 + 32 * c + i)));
         } else if constexpr (ACT == MOE_ACT_RELU2) {
           const float t = fmaxf(MOE_Y(32 * c + i), 0.0f);
           h[i] = bf16_round_f32(__fmul_rn(t, t));
@@ -196,6 +224,7 @@ __device__ __forceinline__ void epilogue_compute(const GemmParams& p, uint32_t* 
         }
       }
 #undef MOE_Y
+#undef MOE_YG
       const int ic = i0 + 32 * c;
       if constexpr (MODE == kG1Act) {
         store_bf16x32(static_cast<uint16_t*>(p.out) + prow * I + ic, h);
@@ -387,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       decode_unit(u, s_off, p.El, p.n_tiles, e, nt, mi);
       const int64_t prow = s_off[e] + mi * kTileM + r;
       const int slot = p.row_to_slot[prow];
-      const float xs_t = (MODE != kG2Rows && slot >= 0) ? p.xs[slot / p.top_k] : 0.0f;
+      const float xs_t = (!is_g2(MODE) && slot >= 0) ? p.xs[slot / p.top_k] : 0.0f;
       bool ok = mbar_wait(acc_full, acc_phase, abort_flag, p.dev_status);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -421,7 +450,7 @@ moe_status_t launch_plain_a(int mode, int act, const GemmParams& prm, int64_t un
                             cudaStream_t s);
 moe_status_t launch_plain_b(int mode, int act, const GemmParams& prm, int64_t units_max, size_t smem,
                             cudaStream_t s);
-moe_status_t launch_rows(const GemmParams& prm, int64_t units_max, size_t smem, cudaStream_t s);
+moe_status_t launch_rows(int mode, const GemmParams& prm, int64_t units_max, size_t smem, cudaStream_t s);
 
 }  // namespace gemm
 }  // namespace moe

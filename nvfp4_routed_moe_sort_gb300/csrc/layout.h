@@ -43,9 +43,10 @@ inline size_t take(size_t& cursor, size_t bytes) {
 }
 
 // Prepared weights: W1 data [El, N1p, H/2], W1 scale tiles [El][N1p/128][Hp/64][512],
-// W2 data [El, Hp, I/2], W2 scale tiles [El][Hp/128][Ip/64][512], alpha1 [El], alpha2 [El].
+// W2 data [El, Hp, I/2], W2 scale tiles [El][Hp/128][Ip/64][512], alpha1 [El], alpha2 [El],
+// gate alpha1 [El] (the W1 gate rows' scalars; a copy of alpha1 unless given separately).
 struct PreparedLayout {
-  size_t w1, w1sf, w2, w2sf, a1, a2, total;
+  size_t w1, w1sf, w2, w2sf, a1, a2, a1g, total;
 };
 
 inline PreparedLayout prepared_layout(const Dims& d) {
@@ -57,13 +58,14 @@ inline PreparedLayout prepared_layout(const Dims& d) {
   L.w2sf = take(c, d.El * d.Hp * d.Ip / 16);
   L.a1 = take(c, d.El * 4);
   L.a2 = take(c, d.El * 4);
+  L.a1g = take(c, d.El * 4);
   L.total = c;
   return L;
 }
 
 // Forward workspace: GEMM tile counters (256 B), permuted activations [cap, H/2] + scale tiles [cap/128][Hp/64][512],
-// intermediate [cap, I/2] + scale tiles [cap/128][Ip/64][512], and (finalize only) the
-// BF16 expert rows [cap, H].
+// intermediate [cap, I/2] + scale tiles [cap/128][Ip/64][512], and the BF16 expert rows
+// [cap, H] (finalized output) or the FP32 accumulator [M, H] (accumulated output).
 struct WorkspaceLayout {
   size_t sched, aq, asf, iq, isf, g, total;
   int64_t cap;
@@ -75,7 +77,7 @@ inline int64_t plan_capacity_rows(int64_t M, int64_t top_k, int64_t El) {
   return roundup64(slots + (kSegAlign - 1) * segs, kSegAlign);
 }
 
-inline WorkspaceLayout workspace_layout(const Dims& d, int64_t M, int64_t top_k, bool finalize) {
+inline WorkspaceLayout workspace_layout(const Dims& d, int64_t M, int64_t top_k, int out_mode) {
   WorkspaceLayout L;
   L.cap = plan_capacity_rows(M, top_k, d.El);
   size_t c = 0;
@@ -84,7 +86,9 @@ inline WorkspaceLayout workspace_layout(const Dims& d, int64_t M, int64_t top_k,
   L.asf = take(c, L.cap * d.Hp / 16);
   L.iq = take(c, L.cap * d.I / 2);
   L.isf = take(c, L.cap * d.Ip / 16);
-  L.g = finalize ? take(c, L.cap * d.H * 2) : 0;
+  L.g = out_mode == MOE_OUTPUT_FINALIZED     ? take(c, L.cap * d.H * 2)
+        : out_mode == MOE_OUTPUT_ACCUMULATE ? take(c, M * d.H * 4)
+                                            : 0;
   L.total = c;
   return L;
 }
@@ -95,6 +99,7 @@ enum GemmMode : int {
   kG1Preact = 1,  // FP32 pre-activations (test hook)
   kG1Act = 2,     // BF16 intermediate (test hook)
   kG2Rows = 3,    // BF16 expert rows
+  kG2Reduce = 4,  // route-weighted rows added in FP32 into the [M, H] accumulator
 };
 
 struct GemmLaunch {
@@ -104,6 +109,7 @@ struct GemmLaunch {
   const uint8_t* b;      // [El * Np, K/2]
   const uint8_t* b_sf;   // [El][Np/128][Kp/64][512]
   const float* alpha;    // [El]
+  const float* alpha_gate;  // [El] gate scalars of a gated GEMM1 (else unused)
   const float* xs;       // per-token scale (GEMM1)
   const int32_t* padded_offsets;
   const int32_t* row_to_slot;
@@ -116,14 +122,20 @@ struct GemmLaunch {
   uint8_t* out_sf;
   int32_t* dev_status;
   int32_t* tile_counter;
+  // kG2Reduce: route weights (moe_weights_dtype_t storage) and routed scaling factor
+  const void* route_w = nullptr;
+  int route_w_dtype = 0;
+  float rsf = 1.0f;
 };
 
 moe_status_t launch_gemm(const GemmLaunch& g, cudaStream_t s);
 moe_status_t launch_permute(const int32_t* padded_offsets, int El, const int32_t* row_to_slot, int top_k,
                             int64_t cap, const uint8_t* xq, const uint8_t* xsf, int H, uint8_t* aq, uint8_t* asf,
-                            int32_t* tile_counters, cudaStream_t s);
-moe_status_t launch_finalize(const uint16_t* rows, const void* topk_weights, int weights_bf16, float rsf,
+                            int32_t* tile_counters, const uint16_t* acc_init, float* acc, int64_t acc_elems,
+                            cudaStream_t s);
+moe_status_t launch_finalize(const uint16_t* rows, const void* topk_weights, int weights_dtype, float rsf,
                              const int32_t* token_to_row, int M, int top_k, int H, uint16_t* out, cudaStream_t s);
+moe_status_t launch_store_acc(const float* acc, int64_t elems, uint16_t* out, cudaStream_t s);
 moe_status_t launch_prepare_matrix(const uint8_t* src, const uint8_t* src_sf, int E, int rows, int rows_p, int K,
                                    int gated_inter, uint8_t* dst, uint8_t* dst_sf, cudaStream_t s);
 

@@ -19,12 +19,15 @@ namespace {
 // One warp per plan row p < padded_offsets[El]: copy the token's packed row (16-byte
 // vectors) and scatter its scale row into 128x4 tiles; scale columns past H/16 (K padding
 // up to a multiple of 256) are written as zero. Padding rows are skipped: the GEMM rows
-// they feed are never read.
+// they feed are never read. For an accumulated output, the same launch also copies the
+// caller's BF16 out [M, H] into the FP32 accumulator that GEMM2 adds to.
 __global__ void __launch_bounds__(256) permute_kernel(const int32_t* __restrict__ padded_offsets, int El,
                                                       const int32_t* __restrict__ row_to_slot, int top_k,
                                                       const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xsf,
                                                       int H, uint8_t* __restrict__ aq, uint8_t* __restrict__ asf,
-                                                      int32_t* __restrict__ tile_counters) {
+                                                      int32_t* __restrict__ tile_counters,
+                                                      const uint16_t* __restrict__ acc_init, float* __restrict__ acc,
+                                                      int64_t acc_elems) {
   pdl_trigger();
   pdl_wait();
   const int lane = threadIdx.x & 31;
@@ -48,6 +51,36 @@ __global__ void __launch_bounds__(256) permute_kernel(const int32_t* __restrict_
       const uint32_t val = (c4 < kcols / 4) ? ssrc[c4] : 0u;
       *reinterpret_cast<uint32_t*>(asf + sf_tile_offset(p, 4 * c4, kcols_p)) = val;
     }
+  }
+  // accumulator = fp32(out), 8 values per thread and step
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = tid; i < acc_elems / 8; i += nthreads) {
+    const uint4 v = reinterpret_cast<const uint4*>(acc_init)[i];
+    float4* d = reinterpret_cast<float4*>(acc) + 2 * i;
+    d[0] = make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u), __uint_as_float(v.y << 16),
+                       __uint_as_float(v.y & 0xFFFF0000u));
+    d[1] = make_float4(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xFFFF0000u), __uint_as_float(v.w << 16),
+                       __uint_as_float(v.w & 0xFFFF0000u));
+  }
+}
+
+// out = bf16(acc), 8 values per thread
+__global__ void __launch_bounds__(256) store_acc_kernel(const float* __restrict__ acc, int64_t elems,
+                                                        uint16_t* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < elems / 8; i += stride) {
+    const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
+    const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
+    uint32_t o[4];
+    const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      o[k] = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v[2 * k]))) |
+             (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v[2 * k + 1]))) << 16);
+    reinterpret_cast<uint4*>(out)[i] = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
@@ -100,16 +133,9 @@ __global__ void __launch_bounds__(256) prepare_matrix_kernel(const uint8_t* __re
 constexpr int kMaxSlots = 8;
 constexpr int kBatchedFinalizeMaxTokens = 256;
 
-// route weight of slot i: FP32 or BF16 storage, times the routed scaling factor
-__device__ __forceinline__ float route_weight(const void* w, int bf16, int64_t i, float rsf) {
-  const float v = bf16 ? __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t*>(w)[i]) << 16)
-                       : static_cast<const float*>(w)[i];
-  return __fmul_rn(v, rsf);
-}
-
 template <bool BATCHED>
 __global__ void __launch_bounds__(256) finalize_kernel(const uint16_t* __restrict__ rows,
-                                                       const void* __restrict__ topk_weights, int weights_bf16,
+                                                       const void* __restrict__ topk_weights, int weights_dtype,
                                                        float rsf, const int32_t* __restrict__ token_to_row, int M,
                                                        int top_k, int H, uint16_t* __restrict__ out) {
   pdl_trigger();
@@ -124,7 +150,7 @@ __global__ void __launch_bounds__(256) finalize_kernel(const uint16_t* __restric
     for (int j = 0; j < top_k; ++j) {
       const int r = token_to_row[static_cast<int64_t>(t) * top_k + j];
       if (r < 0) continue;
-      const float w = route_weight(topk_weights, weights_bf16, static_cast<int64_t>(t) * top_k + j, rsf);
+      const float w = route_weight(topk_weights, weights_dtype, static_cast<int64_t>(t) * top_k + j, rsf);
       const uint4 v = *reinterpret_cast<const uint4*>(rows + static_cast<int64_t>(r) * H + c8 * 8);
       const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -146,7 +172,7 @@ __global__ void __launch_bounds__(256) finalize_kernel(const uint16_t* __restric
       w[j] = 0.0f;
       v[j] = make_uint4(0, 0, 0, 0);
       if (r[j] >= 0) {
-        w[j] = route_weight(topk_weights, weights_bf16, static_cast<int64_t>(t) * top_k + j0 + j, rsf);
+        w[j] = route_weight(topk_weights, weights_dtype, static_cast<int64_t>(t) * top_k + j0 + j, rsf);
         v[j] = *reinterpret_cast<const uint4*>(rows + static_cast<int64_t>(r[j]) * H + c8 * 8);
       }
     }
@@ -181,21 +207,34 @@ int warp_grid(int64_t rows) {
 
 moe_status_t launch_permute(const int32_t* padded_offsets, int El, const int32_t* row_to_slot, int top_k,
                             int64_t cap, const uint8_t* xq, const uint8_t* xsf, int H, uint8_t* aq, uint8_t* asf,
-                            int32_t* tile_counters, cudaStream_t s) {
+                            int32_t* tile_counters, const uint16_t* acc_init, float* acc, int64_t acc_elems,
+                            cudaStream_t s) {
   if (cap == 0) return MOE_OK;
-  return launch_pdl(permute_kernel, dim3(warp_grid(cap)), dim3(256), 0, s, padded_offsets, El, row_to_slot, top_k,
-                    xq, xsf, H, aq, asf, tile_counters);
+  int grid = warp_grid(cap);
+  const int64_t acc_blocks = (acc_elems / 8 + 255) / 256;
+  const int64_t acc_cap = static_cast<int64_t>(num_sms()) * 8;
+  if (acc_blocks > grid) grid = static_cast<int>(acc_blocks < acc_cap ? acc_blocks : acc_cap);
+  return launch_pdl(permute_kernel, dim3(grid), dim3(256), 0, s, padded_offsets, El, row_to_slot, top_k, xq, xsf, H,
+                    aq, asf, tile_counters, acc_init, acc, acc_elems);
 }
 
-moe_status_t launch_finalize(const uint16_t* rows, const void* topk_weights, int weights_bf16, float rsf,
+moe_status_t launch_store_acc(const float* acc, int64_t elems, uint16_t* out, cudaStream_t s) {
+  if (elems == 0) return MOE_OK;
+  const int64_t blocks = (elems / 8 + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(num_sms()) * 8;
+  return launch_pdl(store_acc_kernel, dim3(static_cast<unsigned>(blocks < cap ? blocks : cap)), dim3(256), 0, s, acc,
+                    elems, out);
+}
+
+moe_status_t launch_finalize(const uint16_t* rows, const void* topk_weights, int weights_dtype, float rsf,
                              const int32_t* token_to_row, int M, int top_k, int H, uint16_t* out, cudaStream_t s) {
   if (M == 0) return MOE_OK;
   const int threads = 256;
   const int bx = (H / 8 + threads - 1) / threads;
   if (M <= kBatchedFinalizeMaxTokens)
-    return launch_pdl(finalize_kernel<true>, dim3(bx, M), dim3(threads), 0, s, rows, topk_weights, weights_bf16, rsf,
+    return launch_pdl(finalize_kernel<true>, dim3(bx, M), dim3(threads), 0, s, rows, topk_weights, weights_dtype, rsf,
                       token_to_row, M, top_k, H, out);
-  return launch_pdl(finalize_kernel<false>, dim3(bx, M), dim3(threads), 0, s, rows, topk_weights, weights_bf16, rsf,
+  return launch_pdl(finalize_kernel<false>, dim3(bx, M), dim3(threads), 0, s, rows, topk_weights, weights_dtype, rsf,
                     token_to_row, M, top_k, H, out);
 }
 
@@ -214,7 +253,7 @@ extern "C" moe_status_t moe_finalize(const uint16_t* gemm2_out, const void* topk
                                      float routed_scaling_factor, const int32_t* token_to_row, int32_t M,
                                      int32_t top_k, int32_t H, uint16_t* out, moe_stream_t stream) {
   MOE_CHECK(M >= 0 && top_k >= 1 && H > 0, MOE_ERR_INVALID_ARGUMENT);
-  MOE_CHECK(topk_weights_dtype == MOE_WEIGHTS_F32 || topk_weights_dtype == MOE_WEIGHTS_BF16,
+  MOE_CHECK(topk_weights_dtype >= MOE_WEIGHTS_F32 && topk_weights_dtype <= MOE_WEIGHTS_PACKED,
             MOE_ERR_INVALID_ARGUMENT);
   MOE_CHECK(isfinite(routed_scaling_factor), MOE_ERR_INVALID_ARGUMENT);
   MOE_CHECK(H % 128 == 0, MOE_ERR_UNSUPPORTED_SHAPE);
@@ -229,6 +268,6 @@ extern "C" moe_status_t moe_finalize(const uint16_t* gemm2_out, const void* topk
                 !overlaps(out, ob, token_to_row, static_cast<size_t>(M) * top_k * 4) &&
                 !overlaps(out, ob, gemm2_out, 1),
             MOE_ERR_OVERLAP);
-  return launch_finalize(gemm2_out, topk_weights, topk_weights_dtype == MOE_WEIGHTS_BF16, routed_scaling_factor,
+  return launch_finalize(gemm2_out, topk_weights, topk_weights_dtype, routed_scaling_factor,
                          token_to_row, M, top_k, H, out, as_stream(stream));
 }

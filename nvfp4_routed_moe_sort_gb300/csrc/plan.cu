@@ -28,6 +28,9 @@ struct PlanSmem {
   alignas(16) uint8_t warp_cnt[32][kMaxLocalExperts];
 };
 
+// the id of a routing entry: all 32 bits (plain ids) or bits 15..0 (packed slots, id_mask 0xFFFF)
+__device__ __forceinline__ int entry_id(const int32_t* ids, int64_t s, int id_mask) { return ids[s] & id_mask; }
+
 __device__ __forceinline__ int local_of(int id, int off, int El) {
   const int l = id - off;
   return (l >= 0 && l < El) ? l : -1;
@@ -74,20 +77,20 @@ __device__ void fill_padding(const int* start, const int* cnt, int El, int total
 }
 
 // place slots [begin, end) in order; sm.cursor[l] holds the first free row of expert l
-__device__ void place_range(const int32_t* __restrict__ ids, int64_t begin, int64_t end, int top_k, int off, int El,
-                            PlanSmem& sm, int32_t* __restrict__ row_to_slot, int32_t* __restrict__ token_to_row,
+__device__ void place_range(const int32_t* __restrict__ ids, int id_mask, int64_t begin, int64_t end, int top_k,
+                            int off, int El, PlanSmem& sm, int32_t* __restrict__ row_to_slot, int32_t* __restrict__ token_to_row,
                             int32_t* dev_status) {
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   for (int64_t base = begin; base < end; base += kPlanThreads) {
     const int64_t s = base + tid;
     int l = -1;
     if (s < end) {
-      const int id = ids[s];
+      const int id = entry_id(ids, s, id_mask);
       l = local_of(id, off, El);
       if (l >= 0) {
         const int64_t t0 = s - s % top_k;
         for (int64_t q = t0; q < s; ++q)
-          if (ids[q] == id) atomicOr(dev_status, MOE_DEV_DUPLICATE_EXPERT);
+          if (entry_id(ids, q, id_mask) == id) atomicOr(dev_status, MOE_DEV_DUPLICATE_EXPERT);
       } else {
         token_to_row[s] = -1;
       }
@@ -124,7 +127,8 @@ __device__ void zero_tables(PlanSmem& sm, int El) {
 }
 
 __global__ void __launch_bounds__(kPlanThreads) plan_single_kernel(
-    const int32_t* __restrict__ ids, int64_t n, int top_k, int off, int El, int64_t cap, int32_t* __restrict__ counts,
+    const int32_t* __restrict__ ids, int id_mask, int64_t n, int top_k, int off, int El, int64_t cap,
+    int32_t* __restrict__ counts,
     int32_t* __restrict__ padded_offsets, int32_t* __restrict__ row_to_slot, int32_t* __restrict__ token_to_row,
     int32_t* dev_status) {
   __shared__ PlanSmem sm;
@@ -133,7 +137,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_single_kernel(
   pdl_wait();
   __syncthreads();
   for (int64_t s = threadIdx.x; s < n; s += blockDim.x) {
-    const int l = local_of(ids[s], off, El);
+    const int l = local_of(entry_id(ids, s, id_mask), off, El);
     if (l >= 0) atomicAdd(&sm.cnt[l], 1);
   }
   __syncthreads();
@@ -145,12 +149,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_single_kernel(
   }
   fill_padding(sm.cursor, sm.cnt, El, sm.cursor[El], cap, row_to_slot);
   __syncthreads();
-  place_range(ids, 0, n, top_k, off, El, sm, row_to_slot, token_to_row, dev_status);
+  place_range(ids, id_mask, 0, n, top_k, off, El, sm, row_to_slot, token_to_row, dev_status);
 }
 
 // per-block histograms: hist[b * El + l]
-__global__ void __launch_bounds__(kPlanThreads) plan_hist_kernel(const int32_t* __restrict__ ids, int64_t n, int off,
-                                                                 int El, int32_t* __restrict__ hist) {
+__global__ void __launch_bounds__(kPlanThreads) plan_hist_kernel(const int32_t* __restrict__ ids, int id_mask,
+                                                                 int64_t n, int off, int El,
+                                                                 int32_t* __restrict__ hist) {
   __shared__ int cnt[kMaxLocalExperts];
   pdl_trigger();
   for (int i = threadIdx.x; i < El; i += blockDim.x) cnt[i] = 0;
@@ -159,7 +164,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_hist_kernel(const int32_t* 
   const int64_t b0 = static_cast<int64_t>(blockIdx.x) * kSlotsPerBlock;
   const int64_t b1 = min(n, b0 + kSlotsPerBlock);
   for (int64_t s = b0 + threadIdx.x; s < b1; s += blockDim.x) {
-    const int l = local_of(ids[s], off, El);
+    const int l = local_of(entry_id(ids, s, id_mask), off, El);
     if (l >= 0) atomicAdd(&cnt[l], 1);
   }
   __syncthreads();
@@ -196,7 +201,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_scan_kernel(int32_t* __rest
   fill_padding(sm.cursor, sm.cnt, El, sm.cursor[El], cap, row_to_slot);
 }
 
-__global__ void __launch_bounds__(kPlanThreads) plan_place_kernel(const int32_t* __restrict__ ids, int64_t n,
+__global__ void __launch_bounds__(kPlanThreads) plan_place_kernel(const int32_t* __restrict__ ids, int id_mask,
+                                                                  int64_t n,
                                                                   int top_k, int off, int El,
                                                                   const int32_t* __restrict__ base,
                                                                   int32_t* __restrict__ row_to_slot,
@@ -210,10 +216,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_place_kernel(const int32_t*
   __syncthreads();
   const int64_t b0 = static_cast<int64_t>(blockIdx.x) * kSlotsPerBlock;
   const int64_t b1 = min(n, b0 + kSlotsPerBlock);
-  place_range(ids, b0, b1, top_k, off, El, sm, row_to_slot, token_to_row, dev_status);
+  place_range(ids, id_mask, b0, b1, top_k, off, El, sm, row_to_slot, token_to_row, dev_status);
 }
 
 int64_t plan_blocks(int64_t n) { return (n + kSlotsPerBlock - 1) / kSlotsPerBlock; }
+
+int id_mask_of(int32_t fmt) { return fmt == MOE_IDS_PACKED ? 0xFFFF : -1; }
 
 }  // namespace
 }  // namespace moe
@@ -235,11 +243,14 @@ extern "C" size_t moe_plan_workspace_bytes(int32_t M, int32_t top_k, int32_t num
   return static_cast<size_t>(roundup64(nb * num_local_experts * 4, 256));
 }
 
-extern "C" moe_status_t moe_plan(const int32_t* topk_ids, int32_t M, int32_t top_k, int32_t num_experts,
+extern "C" moe_status_t moe_plan(const int32_t* topk_ids, int32_t topk_ids_format, int32_t M, int32_t top_k,
+                                 int32_t num_experts,
                                  int32_t local_expert_offset, int32_t num_local_experts, int32_t* counts,
                                  int32_t* padded_offsets, int32_t* row_to_slot, int32_t* token_to_row,
                                  void* workspace, size_t workspace_bytes, int32_t* dev_status, moe_stream_t stream) {
   MOE_CHECK(M >= 0 && top_k >= 1 && num_local_experts >= 1 && num_experts >= 1, MOE_ERR_INVALID_ARGUMENT);
+  MOE_CHECK(topk_ids_format == MOE_IDS_INT32 || topk_ids_format == MOE_IDS_PACKED, MOE_ERR_INVALID_ARGUMENT);
+  const int id_mask = id_mask_of(topk_ids_format);
   MOE_CHECK(local_expert_offset >= 0 && local_expert_offset + num_local_experts <= num_experts,
             MOE_ERR_INVALID_ARGUMENT);
   MOE_CHECK(num_local_experts <= kMaxLocalExperts, MOE_ERR_UNSUPPORTED_SHAPE);
@@ -263,16 +274,16 @@ extern "C" moe_status_t moe_plan(const int32_t* topk_ids, int32_t M, int32_t top
   const int off = local_expert_offset, El = num_local_experts;
   const dim3 block(kPlanThreads);
   if (nb <= 1)
-    return launch_pdl(plan_single_kernel, dim3(1), block, 0, s, topk_ids, n, top_k, off, El, cap, counts,
+    return launch_pdl(plan_single_kernel, dim3(1), block, 0, s, topk_ids, id_mask, n, top_k, off, El, cap, counts,
                       padded_offsets, row_to_slot, token_to_row, dev_status);
   int32_t* hist = static_cast<int32_t*>(workspace);
   const dim3 grid(static_cast<unsigned>(nb));
-  moe_status_t st = launch_pdl(plan_hist_kernel, grid, block, 0, s, topk_ids, n, off, El, hist);
+  moe_status_t st = launch_pdl(plan_hist_kernel, grid, block, 0, s, topk_ids, id_mask, n, off, El, hist);
   if (st != MOE_OK) return st;
   st = launch_pdl(plan_scan_kernel, dim3(1), block, 0, s, hist, static_cast<int>(nb), El, cap, counts,
                   padded_offsets, row_to_slot);
   if (st != MOE_OK) return st;
-  return launch_pdl(plan_place_kernel, grid, block, 0, s, topk_ids, n, top_k, off, El,
+  return launch_pdl(plan_place_kernel, grid, block, 0, s, topk_ids, id_mask, n, top_k, off, El,
                     static_cast<const int32_t*>(hist), row_to_slot, token_to_row, dev_status);
 }
 
@@ -323,11 +334,14 @@ moe_status_t noalloc_scratch(int32_t** out) {
 }  // namespace
 }  // namespace moe
 
-extern "C" moe_status_t moe_plan_noalloc(const int32_t* topk_ids, int32_t M, int32_t top_k, int32_t num_experts,
+extern "C" moe_status_t moe_plan_noalloc(const int32_t* topk_ids, int32_t topk_ids_format, int32_t M,
+                                         int32_t top_k, int32_t num_experts,
                                          int32_t local_expert_offset, int32_t num_local_experts, int32_t* counts,
                                          int32_t* padded_offsets, int32_t* row_to_slot, int32_t* token_to_row,
                                          int32_t* dev_status, moe_stream_t stream) {
   MOE_CHECK(M >= 0 && top_k >= 1 && num_local_experts >= 1 && num_experts >= 1, MOE_ERR_INVALID_ARGUMENT);
+  MOE_CHECK(topk_ids_format == MOE_IDS_INT32 || topk_ids_format == MOE_IDS_PACKED, MOE_ERR_INVALID_ARGUMENT);
+  const int id_mask = id_mask_of(topk_ids_format);
   MOE_CHECK(local_expert_offset >= 0 && local_expert_offset + num_local_experts <= num_experts,
             MOE_ERR_INVALID_ARGUMENT);
   MOE_CHECK(num_local_experts <= kMaxLocalExperts, MOE_ERR_UNSUPPORTED_SHAPE);
@@ -349,16 +363,17 @@ extern "C" moe_status_t moe_plan_noalloc(const int32_t* topk_ids, int32_t M, int
   cudaStream_t s = as_stream(stream);
   const int off = local_expert_offset, El = num_local_experts;
   if (nb <= 1) {
-    plan_single_kernel<<<1, kPlanThreads, 0, s>>>(topk_ids, n, top_k, off, El, cap, counts, padded_offsets,
-                                                  row_to_slot, token_to_row, dev_status);
+    plan_single_kernel<<<1, kPlanThreads, 0, s>>>(topk_ids, id_mask, n, top_k, off, El, cap, counts,
+                                                  padded_offsets, row_to_slot, token_to_row, dev_status);
     return launch_status();
   }
-  plan_hist_kernel<<<static_cast<unsigned>(nb), kPlanThreads, 0, s>>>(topk_ids, n, off, El, hist);
+  plan_hist_kernel<<<static_cast<unsigned>(nb), kPlanThreads, 0, s>>>(topk_ids, id_mask, n, off, El, hist);
   MOE_CHECK(launch_status() == MOE_OK, MOE_ERR_CUDA);
   plan_scan_kernel<<<1, kPlanThreads, 0, s>>>(hist, static_cast<int>(nb), El, cap, counts, padded_offsets,
                                               row_to_slot);
   MOE_CHECK(launch_status() == MOE_OK, MOE_ERR_CUDA);
-  plan_place_kernel<<<static_cast<unsigned>(nb), kPlanThreads, 0, s>>>(topk_ids, n, top_k, off, El, hist,
-                                                                       row_to_slot, token_to_row, dev_status);
+  plan_place_kernel<<<static_cast<unsigned>(nb), kPlanThreads, 0, s>>>(topk_ids, id_mask, n, top_k, off, El,
+                                                                       hist, row_to_slot, token_to_row,
+                                                                       dev_status);
   return launch_status();
 }

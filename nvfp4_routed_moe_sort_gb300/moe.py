@@ -31,7 +31,9 @@ class NVFP4RoutedMoE:
     def __init__(self, w1, w1_sf, w1_alpha, w2, w2_sf, w2_alpha, activation: str = "swiglu",
                  num_experts: int | None = None, local_expert_offset: int = 0,
                  fc2_input_scale: float = 1.0, scale_mode: str = "per_token",
-                 routed_scaling_factor: float = 1.0):
+                 routed_scaling_factor: float = 1.0, w1_gate_alpha=None):
+        """w1_gate_alpha [E_local] f32 (optional): separate dequant scalars of the gate rows of a
+        gated W1; w1_alpha then scales the up rows only."""
         El, N1, Hh = w1.shape
         self.El = El
         self.H = Hh * 2
@@ -45,8 +47,9 @@ class NVFP4RoutedMoE:
         self.routed_scaling_factor = float(routed_scaling_factor)
         self.scale_mode = L.MOE_SCALE_PER_TOKEN if scale_mode == "per_token" else L.MOE_SCALE_GLOBAL_ONE
         self.device = w1.device
-        self.linear = (w1, w1_sf, w1_alpha, w2, w2_sf, w2_alpha)
-        self.w = L.make_weights(El, self.H, self.I, self.act, w1, w1_sf, w1_alpha, w2, w2_sf, w2_alpha)
+        self.linear = (w1, w1_sf, w1_alpha, w2, w2_sf, w2_alpha, w1_gate_alpha)
+        self.w = L.make_weights(El, self.H, self.I, self.act, w1, w1_sf, w1_alpha, w2, w2_sf, w2_alpha,
+                                w1_gate_alpha)
         nbytes = L.moe_prepared_weights_bytes(self.w)
         self.prepared = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
         L.moe_prepare_weights(self.w, self.prepared)
@@ -56,8 +59,11 @@ class NVFP4RoutedMoE:
         """Re-prepare from the (updated) linear weights into the same buffer."""
         L.moe_prepare_weights(self.w, self.prepared)
 
-    def buffers(self, M: int, top_k: int, do_finalize: bool) -> dict:
-        key = (M, top_k, bool(do_finalize))
+    def buffers(self, M: int, top_k: int, do_finalize) -> dict:
+        """Buffers of one batch shape. do_finalize: False/0 unfinalized rows, True/1 finalized
+        output, 2 accumulated output (the caller's out)."""
+        mode = int(do_finalize)
+        key = (M, top_k, mode)
         if key in self._bufs:
             return self._bufs[key]
         dev = self.device
@@ -72,12 +78,13 @@ class NVFP4RoutedMoE:
             "token_to_row": torch.empty(M, top_k, dtype=torch.int32, device=dev),
             "plan_ws": torch.empty(max(L.moe_plan_workspace_bytes(M, top_k, self.El), 16),
                                    dtype=torch.uint8, device=dev),
-            "ws": torch.empty(max(L.moe_forward_workspace_bytes(M, top_k, self.w, do_finalize), 16),
+            "ws": torch.empty(max(L.moe_forward_workspace_bytes(M, top_k, self.w, mode), 16),
                               dtype=torch.uint8, device=dev),
             "dev_status": torch.zeros(4, dtype=torch.int32, device=dev),
-            "out": torch.empty(M, self.H, dtype=torch.bfloat16, device=dev) if do_finalize else None,
-            "gemm2_out": None if do_finalize else torch.empty(max(cap, 1), self.H, dtype=torch.bfloat16,
-                                                              device=dev),
+            "out": torch.empty(M, self.H, dtype=torch.bfloat16, device=dev)
+            if mode == L.MOE_OUTPUT_FINALIZED else None,
+            "gemm2_out": torch.empty(max(cap, 1), self.H, dtype=torch.bfloat16, device=dev)
+            if mode == L.MOE_OUTPUT_UNFINALIZED else None,
             "capacity": cap,
         }
         self._bufs[key] = b
@@ -86,34 +93,57 @@ class NVFP4RoutedMoE:
     def quantize(self, x: torch.Tensor, b: dict):
         L.moe_quantize_input(x.view(torch.int16), self.scale_mode, b["xq"], b["xsf"], b["xs"])
 
-    def plan(self, topk_ids: torch.Tensor, b: dict):
+    def plan(self, topk_ids: torch.Tensor, b: dict, packed: bool = False):
         L.moe_plan(topk_ids, self.num_experts, self.local_expert_offset, self.El, b["counts"],
-                   b["padded_offsets"], b["row_to_slot"], b["token_to_row"], b["plan_ws"], b["dev_status"])
+                   b["padded_offsets"], b["row_to_slot"], b["token_to_row"], b["plan_ws"], b["dev_status"],
+                   packed=packed)
 
-    def experts(self, topk_weights: torch.Tensor, b: dict, do_finalize: bool, step_events=None):
+    def experts(self, topk_weights: torch.Tensor, b: dict, do_finalize, step_events=None, out=None):
         L.moe_grouped_fp4_forward(b["padded_offsets"], b["row_to_slot"], b["token_to_row"], b["xq"], b["xsf"],
                                   b["xs"], self.w, self.prepared, topk_weights, self.fc2_input_scale,
-                                  do_finalize, b["out"], b["gemm2_out"], b["ws"], b["dev_status"],
-                                  step_events=step_events, routed_scaling_factor=self.routed_scaling_factor)
+                                  int(do_finalize), out if out is not None else b["out"], b["gemm2_out"],
+                                  b["ws"], b["dev_status"], step_events=step_events,
+                                  routed_scaling_factor=self.routed_scaling_factor)
 
-    def forward(self, x: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor,
-                do_finalize: bool = True, step_events=None):
+    def forward(self, x: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor | None,
+                do_finalize=True, step_events=None, out: torch.Tensor | None = None,
+                token_capacity: int | None = None):
         """x [M, H] bf16, topk_ids [M, k] int32, topk_weights [M, k] f32 or bf16 (all on the GPU).
 
-        Returns out [M, H] bf16, or (gemm2_out [capacity, H], topk_weights, token_to_row)
-        when do_finalize is False. The returned tensors are the layer's reusable buffers.
+        topk_weights None: topk_ids holds packed routing slots (int32: BF16 score in bits
+        31..16, expert id in bits 15..0) and supplies both the ids and the scores.
+        do_finalize: True/1 returns out [M, H] bf16 (ordered combine); False/0 returns
+        (gemm2_out [capacity, H], topk_weights, token_to_row); 2 adds the routed
+        contributions in FP32 to the caller's ``out`` [M, H] bf16 (required) and returns it.
+        out (finalized mode, optional): write into this [M, H] tensor instead of the layer's.
+        token_capacity: process only the first token_capacity rows of x and the routing
+        (a fixed prefix of a graph-stable dispatcher buffer); rows of ``out`` past it are left
+        untouched. Returned tensors other than a caller's out are the layer's reusable buffers.
         """
+        packed = topk_weights is None
+        if packed:
+            topk_weights = topk_ids
+        mode = int(do_finalize)
+        if mode == L.MOE_OUTPUT_ACCUMULATE and out is None:
+            raise ValueError("do_finalize=2 (accumulate) needs the caller's out tensor")
+        if token_capacity is not None:
+            T = int(token_capacity)
+            if not 0 <= T <= x.shape[0]:
+                raise ValueError("token_capacity must lie in [0, M]")
+            x, topk_ids, topk_weights = x[:T], topk_ids[:T], topk_weights[:T]
+            if out is not None:
+                out = out[:T]
         M, k = topk_ids.shape
-        b = self.buffers(M, k, do_finalize)
+        b = self.buffers(M, k, mode)
         self.quantize(x, b)
-        self.plan(topk_ids, b)
-        self.experts(topk_weights, b, do_finalize, step_events)
-        if do_finalize:
-            return b["out"]
-        return b["gemm2_out"], topk_weights, b["token_to_row"]
+        self.plan(topk_ids, b, packed)
+        self.experts(topk_weights, b, mode, step_events, out)
+        if mode == L.MOE_OUTPUT_UNFINALIZED:
+            return b["gemm2_out"], topk_weights, b["token_to_row"]
+        return out if out is not None else b["out"]
 
-    def capture(self, x: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor,
-                do_finalize: bool = True, step_events=None) -> torch.cuda.CUDAGraph:
+    def capture(self, x: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor | None,
+                do_finalize=True, step_events=None, out: torch.Tensor | None = None) -> torch.cuda.CUDAGraph:
         """Capture one forward (quantize, plan, permute, GEMM1, GEMM2, finalize) in a CUDA graph.
 
         The graph reads x, topk_ids and topk_weights at their current addresses and writes the
@@ -123,11 +153,19 @@ class NVFP4RoutedMoE:
         inside the graph: before quantize, plan, permute, gemm1, gemm2, finalize, and the end.
         """
         M, k = topk_ids.shape
-        b = self.buffers(M, k, do_finalize)
+        mode = int(do_finalize)
+        packed = topk_weights is None
+        if packed:
+            topk_weights = topk_ids
+        b = self.buffers(M, k, mode)
+        if mode == L.MOE_OUTPUT_ACCUMULATE and out is None:
+            raise ValueError("do_finalize=2 (accumulate) needs the caller's out tensor")
+        # warm-up outside the capture (an accumulating warm-up writes a copy of out)
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(side):          # warm-up outside the capture
-            self.forward(x, topk_ids, topk_weights, do_finalize)
+        with torch.cuda.stream(side):
+            warm_out = out.clone() if mode == L.MOE_OUTPUT_ACCUMULATE else out
+            self.forward(x, topk_ids, None if packed else topk_weights, mode, out=warm_out)
         torch.cuda.current_stream().wait_stream(side)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
@@ -136,11 +174,11 @@ class NVFP4RoutedMoE:
             self.quantize(x, b)
             if step_events:
                 step_events[1].record()
-            self.plan(topk_ids, b)
-            self.experts(topk_weights, b, do_finalize, step_events[2:7] if step_events else None)
+            self.plan(topk_ids, b, packed)
+            self.experts(topk_weights, b, mode, step_events[2:7] if step_events else None, out)
             if step_events:
                 step_events[7].record()
         return g
 
-    def device_status(self, M: int, top_k: int, do_finalize: bool) -> int:
+    def device_status(self, M: int, top_k: int, do_finalize) -> int:
         return int(self.buffers(M, top_k, do_finalize)["dev_status"][0].item())

@@ -29,6 +29,14 @@ Readings:
   encode scale ``fc2_input_scale`` (1.0 = "a global scale of one"); GEMM2 output
   ``y2 = acc2 / fc2_input_scale * alpha2[e]``, rounded to BF16 (the expert
   output); the finalize combines these BF16 rows.
+* FlashInfer ``fused_moe.alphamoe_nvfp4_aligned_moe`` (the fused variant):
+  separate per-expert scalars for the gate accumulators
+  (``output1_scale_gate_scalar``, applied before the activation) and the up
+  accumulators (``output1_scale_scalar``); each down accumulator times its
+  expert's scalar, the route weight and ``routed_scaling_factor`` is added in FP32
+  to an FP32 copy of the caller's BF16 ``out``, converted back once. The FP32
+  reduction there is order-dependent; the oracle sums in float64 (the exact
+  value up to the final BF16 rounding) and the GPU is held to a tolerance.
 """
 from __future__ import annotations
 
@@ -132,17 +140,21 @@ def activation(y: np.ndarray, act: str, inter: int) -> np.ndarray:
 
 
 def expert_chain(A_deq: np.ndarray, xs: np.ndarray, pack1: ExpertPack, pack2: ExpertPack,
-                 act: str, inter: int, fc2_input_scale: float) -> dict:
+                 act: str, inter: int, fc2_input_scale: float, alpha_gate=None) -> dict:
     """All steps for the rows routed to one expert.
 
     A_deq float64 [r, H] block-dequantised activations of those rows' tokens,
-    xs float32 [r] their per-token scales.
+    xs float32 [r] their per-token scales. ``alpha_gate`` (gated activations only):
+    the expert's separate scalar of the gate rows ``[0, I)``; W1's own alpha then
+    scales the up rows ``[I, 2I)`` only.
     """
     d1, s1, a1 = pack1
     d2, s2, a2 = pack2
     W1 = dequantize_rows(d1, s1)                       # [N1, H]
     acc1 = A_deq @ W1.T                                # float64 sums
     y = acc1 * np.asarray(xs, np.float64)[:, None] * np.float64(a1)
+    if alpha_gate is not None and act in GATED_ACTIVATIONS:
+        y[:, :inter] = acc1[:, :inter] * np.asarray(xs, np.float64)[:, None] * np.float64(alpha_gate)
     h = bf16_round(activation(y, act, inter))          # BF16 intermediate
     codes, isf = quantize_blocks(h.astype(F32), F32(fc2_input_scale))
     I_deq = (e2m1_decode(codes).reshape(codes.shape[0], -1, 16)
@@ -151,7 +163,7 @@ def expert_chain(A_deq: np.ndarray, xs: np.ndarray, pack1: ExpertPack, pack2: Ex
     acc2 = I_deq @ W2.T
     y2 = acc2 / np.float64(F32(fc2_input_scale)) * np.float64(a2)
     return {"preact": y, "act_bf16": h, "icodes": codes, "isf": isf,
-            "rows": bf16_round(y2)}
+            "rows": bf16_round(y2), "y2": y2}
 
 
 def finalize(rows: np.ndarray, topk_weights: np.ndarray, token_to_row: np.ndarray,
@@ -182,17 +194,41 @@ def finalize(rows: np.ndarray, topk_weights: np.ndarray, token_to_row: np.ndarra
     return bf16_round(acc.astype(np.float64))
 
 
+def combine_accumulate(out_prev: np.ndarray, y2_rows: np.ndarray, topk_weights: np.ndarray,
+                       token_to_row: np.ndarray, routed_scaling_factor: float = 1.0) -> np.ndarray:
+    """Accumulated output of the fused variant: ``bf16(out_prev + sum_j y2[row(t,j)] * w')``.
+
+    ``y2_rows`` are the unrounded GEMM2 rows, ``w' = fp32(w * routed_scaling_factor)``,
+    masked slots skipped; the sum is taken in float64 (exact up to the final BF16
+    rounding); a token with no routed local slot keeps its ``out_prev`` row.
+    """
+    w = np.asarray(topk_weights, dtype=F32)
+    if routed_scaling_factor != 1.0:
+        w = (w * F32(routed_scaling_factor)).astype(F32)
+    t2r = np.asarray(token_to_row)
+    acc = np.asarray(out_prev, dtype=np.float64).copy()
+    for j in range(t2r.shape[1]):
+        r = t2r[:, j]
+        m = r >= 0
+        if m.any():
+            acc[m] += w[m, j][:, None].astype(np.float64) * y2_rows[r[m]]
+    return bf16_round(acc)
+
+
 def forward(xq: np.ndarray, xsf: np.ndarray, xs: np.ndarray, topk_ids: np.ndarray,
             topk_weights: np.ndarray, weights: ExpertWeights, act: str,
             local_expert_offset: int = 0, fc2_input_scale: float = 1.0,
             plan: Optional[dict] = None, allow_duplicates: bool = False,
-            routed_scaling_factor: float = 1.0) -> dict:
+            routed_scaling_factor: float = 1.0, gate_alpha: Optional[np.ndarray] = None,
+            out_prev: Optional[np.ndarray] = None) -> dict:
     """The whole path on quantised activations, in plan row order.
 
     Returns the plan and, per row of the padded plan (NaN in padding rows):
     ``preact`` float64 [P_cap, N1], ``act_bf16`` [P_cap, I], ``icodes`` uint8
-    [P_cap, I], ``isf`` uint8 [P_cap, I/16], ``rows`` (= gemm2_out) [P_cap, H];
-    and ``out`` = finalize(rows) [M, H].
+    [P_cap, I], ``isf`` uint8 [P_cap, I/16], ``rows`` (= gemm2_out) [P_cap, H],
+    ``y2`` (unrounded rows); ``out`` = finalize(rows) [M, H]; and, when ``out_prev``
+    [M, H] is given, ``out_acc`` = combine_accumulate(out_prev, y2). ``gate_alpha``
+    [E_local]: separate gate-row scalars of a gated W1.
     """
     if plan is None:
         plan = make_plan(topk_ids, local_expert_offset, weights.num_local, allow_duplicates)
@@ -206,6 +242,7 @@ def forward(xq: np.ndarray, xsf: np.ndarray, xs: np.ndarray, topk_ids: np.ndarra
         "icodes": np.zeros((cap, I), dtype=np.uint8),
         "isf": np.zeros((cap, I // 16), dtype=np.uint8),
         "rows": np.full((cap, H), np.nan),
+        "y2": np.full((cap, H), np.nan),
     }
     A_all = dequantize_rows(xq, xsf)
     padded, counts = plan["padded_offsets"], plan["counts"]
@@ -216,11 +253,14 @@ def forward(xq: np.ndarray, xsf: np.ndarray, xs: np.ndarray, topk_ids: np.ndarra
         prow = np.arange(padded[l], padded[l] + c)
         tok = plan["row_to_slot"][prow] // k
         r = expert_chain(A_all[tok], xs[tok], weights.w1(l), weights.w2(l), act, I,
-                         fc2_input_scale)
-        for key in ("preact", "act_bf16", "icodes", "isf", "rows"):
+                         fc2_input_scale, None if gate_alpha is None else gate_alpha[l])
+        for key in ("preact", "act_bf16", "icodes", "isf", "rows", "y2"):
             res[key][prow] = r[key]
     res["out"] = finalize(np.nan_to_num(res["rows"]), topk_weights, plan["token_to_row"],
                           routed_scaling_factor)
+    if out_prev is not None:
+        res["out_acc"] = combine_accumulate(out_prev, np.nan_to_num(res["y2"]), topk_weights,
+                                            plan["token_to_row"], routed_scaling_factor)
     res["plan"] = plan
     return res
 
@@ -228,34 +268,41 @@ def forward(xq: np.ndarray, xsf: np.ndarray, xs: np.ndarray, topk_ids: np.ndarra
 def forward_tokens(tokens: Sequence[int], xq: np.ndarray, xsf: np.ndarray, xs: np.ndarray,
                    topk_ids: np.ndarray, topk_weights: np.ndarray, weights: ExpertWeights,
                    act: str, local_expert_offset: int = 0,
-                   fc2_input_scale: float = 1.0, routed_scaling_factor: float = 1.0) -> dict:
+                   fc2_input_scale: float = 1.0, routed_scaling_factor: float = 1.0,
+                   gate_alpha: Optional[np.ndarray] = None, out_prev: Optional[np.ndarray] = None) -> dict:
     """Output rows of selected tokens only, each computed on its own.
 
     Every step of the path is row-local (per-token scales, static FC2 input
     scale), so a token's output depends only on its own activations and the
     weights of its routed local experts. Returns ``out`` [len(tokens), H] and
-    the expert rows ``rows[(t, j)]``.
+    the expert rows ``rows[(t, j)]``; with ``out_prev`` [len(tokens), H] also ``out_acc``,
+    the accumulated output of those tokens.
     """
     ids = np.asarray(topk_ids, dtype=np.int64)
     M, k = ids.shape
     I = weights.inter
-    rows = {}
+    rows, y2 = {}, {}
     for t in tokens:
         A = dequantize_rows(xq[t:t + 1], xsf[t:t + 1])
         for j in range(k):
             l = int(ids[t, j]) - local_expert_offset
             if 0 <= l < weights.num_local:
                 r = expert_chain(A, xs[t:t + 1], weights.w1(l), weights.w2(l), act, I,
-                                 fc2_input_scale)
+                                 fc2_input_scale, None if gate_alpha is None else gate_alpha[l])
                 rows[(t, j)] = r["rows"][0]
-    sub_rows = []
+                y2[(t, j)] = r["y2"][0]
+    sub_rows, sub_y2 = [], []
     t2r = np.full((len(tokens), k), -1, dtype=np.int64)
     for i, t in enumerate(tokens):
         for j in range(k):
             if (t, j) in rows:
                 t2r[i, j] = len(sub_rows)
                 sub_rows.append(rows[(t, j)])
-    R = np.array(sub_rows) if sub_rows else np.zeros((0, weights.hidden))
+                sub_y2.append(y2[(t, j)])
+    R = np.array(sub_rows) if sub_rows else np.zeros((1, weights.hidden))
     w = np.asarray(topk_weights)[list(tokens)]
-    out = finalize(R if len(R) else np.zeros((1, weights.hidden)), w, t2r, routed_scaling_factor)
-    return {"out": out, "rows": rows}
+    res = {"out": finalize(R, w, t2r, routed_scaling_factor), "rows": rows}
+    if out_prev is not None:
+        Y = np.array(sub_y2) if sub_y2 else np.zeros((1, weights.hidden))
+        res["out_acc"] = combine_accumulate(out_prev, Y, w, t2r, routed_scaling_factor)
+    return res

@@ -27,6 +27,8 @@ from __future__ import annotations
 
 import numpy as np
 
+from .formats import bits_to_bf16
+
 SEGMENT_ALIGN = 128
 
 
@@ -42,6 +44,21 @@ def plan_capacity(M: int, top_k: int, num_local_experts: int) -> int:
     """
     slots = M * top_k
     return roundup(slots + (SEGMENT_ALIGN - 1) * min(num_local_experts, slots), SEGMENT_ALIGN)
+
+
+def unpack_topk(packed: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
+    """Packed routing slots -> (expert ids int64, scores float64).
+
+    FlashInfer ``fused_moe.CudnnGroupedGemmNvfp4Config`` accepts routing weights
+    "packed, or unpacked"; ``FrostLowLatencyConfig`` says packed scores keep their
+    BF16 rounding. The bit layout is a reading (the pages do not print it): one
+    32-bit word per slot, the BF16 score in bits 31..16 and the expert id, unsigned,
+    in bits 15..0.
+    """
+    word = np.asarray(packed).astype(np.int64) & 0xFFFFFFFF
+    ids = word & 0xFFFF
+    scores = bits_to_bf16((word >> 16).astype(np.uint16))
+    return ids, scores
 
 
 def make_plan(topk_ids: np.ndarray, local_expert_offset: int, num_local_experts: int,

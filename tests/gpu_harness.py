@@ -56,7 +56,10 @@ def oracle_weights(cfg: mi.MoEConfig) -> O.ExpertWeights:
 class Problem:
     """One seeded problem on the GPU (inputs, quantised weights, prepared layer)."""
 
-    def __init__(self, cfg: mi.MoEConfig, ids: np.ndarray | None = None, tw: np.ndarray | None = None):
+    def __init__(self, cfg: mi.MoEConfig, ids: np.ndarray | None = None, tw: np.ndarray | None = None,
+                 gate_factor: np.ndarray | None = None):
+        """gate_factor [E_local] (optional): the layer gets separate gate-row scalars
+        fp32(alpha1 * factor), with alpha1 taken from the oracle's own quantisation."""
         self.cfg = cfg
         self.x = mi.hidden_bf16(cfg, DEV)
         if ids is None:
@@ -69,10 +72,17 @@ class Problem:
         self.w2_bf16 = torch.stack([mi.expert_w2_bf16(cfg, l, DEV) for l in range(El)])
         self.q1 = pkg.quantize_weights(self.w1_bf16)
         self.q2 = pkg.quantize_weights(self.w2_bf16)
+        self.gate_alpha = None
+        if gate_factor is not None:
+            W = oracle_weights(cfg)
+            self.gate_alpha = np.array([np.float32(W.w1(l)[2]) * np.float32(gate_factor[l]) for l in range(El)],
+                                       dtype=np.float32)
+            self.gate_alpha_t = torch.from_numpy(self.gate_alpha).to(DEV)
         self.layer = pkg.NVFP4RoutedMoE(*self.q1, *self.q2, activation=cfg.act, num_experts=cfg.E,
                                         local_expert_offset=cfg.local_offset,
                                         fc2_input_scale=cfg.fc2_input_scale, scale_mode=cfg.scale_mode,
-                                        routed_scaling_factor=cfg.routed_scaling_factor)
+                                        routed_scaling_factor=cfg.routed_scaling_factor,
+                                        w1_gate_alpha=None if gate_factor is None else self.gate_alpha_t)
 
     def run(self, do_finalize=True):
         res = self.layer.forward(self.x, self.ids_t, self.tw_t, do_finalize=do_finalize)
@@ -91,7 +101,8 @@ class Problem:
         return O.forward(xq, xsf, xs, self.ids, self.tw, oracle_weights(self.cfg), self.cfg.act,
                          local_expert_offset=self.cfg.local_offset,
                          fc2_input_scale=self.cfg.fc2_input_scale,
-                         routed_scaling_factor=self.cfg.routed_scaling_factor, **kw)
+                         routed_scaling_factor=self.cfg.routed_scaling_factor, gate_alpha=self.gate_alpha,
+                         **kw)
 
 
 def assert_close_output(got: np.ndarray, ref: np.ndarray, what: str = ""):

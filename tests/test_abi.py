@@ -33,7 +33,7 @@ def test_header_declares_binding_names():
 def test_exports_every_declared_symbol(lib):
     for name in _declared():
         assert hasattr(lib, name), name
-    assert pkg.moe_abi_version() == 1
+    assert pkg.moe_abi_version() == 2
 
 
 def test_status_strings(lib):
@@ -63,6 +63,10 @@ def test_size_queries(lib):
     assert pkg.moe_forward_workspace_bytes(4, 2, w, 1) > pkg.moe_forward_workspace_bytes(4, 2, w, 0)
     off = pkg.moe_forward_workspace_layout(4, 2, w, 1)
     assert off[0] >= 0 and all(o % 256 == 0 for o in off) and off[5] == pkg.moe_forward_workspace_bytes(4, 2, w, 1)
+    # accumulated output: an FP32 [M, H] accumulator instead of BF16 rows [capacity, H]
+    acc = pkg.moe_forward_workspace_layout(4, 2, w, 2)
+    assert acc[5] - acc[4] >= 4 * 4 * 128 and acc[5] < off[5]
+    assert pkg.moe_forward_workspace_bytes(4, 2, w, 3) == 0      # unknown output mode
     assert pkg.moe_plan_workspace_bytes(4, 2, 4) == 0            # one block: no scratch
     assert pkg.moe_plan_workspace_bytes(4096, 8, 256) > 0
 
@@ -86,13 +90,17 @@ def test_shape_validation(lib):
 def test_plan_validation(lib):
     f = lib.moe_plan
     # local range outside the global expert count
-    assert f(None, 4, 2, 8, 6, 4, None, None, None, None, None, 0, None, None) == 1
+    assert f(None, 0, 4, 2, 8, 6, 4, None, None, None, None, None, 0, None, None) == 1
     # too many local experts
-    assert f(None, 4, 2, 1024, 0, 600, None, None, None, None, None, 0, None, None) == 2
+    assert f(None, 0, 4, 2, 1024, 0, 600, None, None, None, None, None, 0, None, None) == 2
     # misaligned counts pointer
-    assert f(16, 4, 2, 8, 0, 4, 8, 32, 48, 64, None, 0, 96, None) == 3
-    # workspace too small for the multi-block path
-    assert f(16, 4096, 8, 256, 0, 256, 16, 32, 48, 64, None, 0, 96, None) == 4
+    assert f(16, 0, 4, 2, 8, 0, 4, 8, 32, 48, 64, None, 0, 96, None) == 3
+    # workspace too small for the multi-block path (plain and packed ids)
+    assert f(16, 0, 4096, 8, 256, 0, 256, 16, 32, 48, 64, None, 0, 96, None) == 4
+    assert f(16, 1, 4096, 8, 256, 0, 256, 16, 32, 48, 64, None, 0, 96, None) == 4
+    # unknown id format
+    assert f(16, 2, 4, 2, 8, 0, 4, 16, 32, 48, 64, None, 0, 96, None) == 1
+    assert lib.moe_plan_noalloc(16, 7, 4, 2, 8, 0, 4, 16, 32, 48, 64, 96, None) == 1
 
 
 @host_only
@@ -122,6 +130,21 @@ def test_forward_validation(lib):
     st = f(16, 32, 48, 4, 2, 64, 80, 96, ctypes.byref(w), 4096, pb, 112, 0, 1.0, 1.0, 1, 1 << 40, null, 1 << 36, ws,
            160, null, 3, null)
     assert st == 1
+    # unknown output mode; unknown route-weight storage
+    st = f(16, 32, 48, 4, 2, 64, 80, 96, ctypes.byref(w), 4096, pb, 112, 0, 1.0, 1.0, 3, 1 << 40, null, 1 << 36, ws,
+           160, null, 0, null)
+    assert st == 1
+    st = f(16, 32, 48, 4, 2, 64, 80, 96, ctypes.byref(w), 4096, pb, 112, 3, 1.0, 1.0, 1, 1 << 40, null, 1 << 36, ws,
+           160, null, 0, null)
+    assert st == 1
+    # accumulated output needs out, and out must not overlap the workspace
+    wsa = pkg.moe_forward_workspace_bytes(4, 2, w, 2)
+    st = f(16, 32, 48, 4, 2, 64, 80, 96, ctypes.byref(w), 4096, pb, 112, 2, 1.0, 1.0, 2, null, null, 1 << 36, wsa,
+           160, null, 0, null)
+    assert st == 1
+    st = f(16, 32, 48, 4, 2, 64, 80, 96, ctypes.byref(w), 4096, pb, 112, 2, 1.0, 1.0, 2, 1 << 36, null, 1 << 36, wsa,
+           160, null, 0, null)
+    assert st == 6
 
 
 @host_only
@@ -132,6 +155,7 @@ def test_finalize_validation(lib):
     assert f(16, 32, 0, 1.0, 48, 4, 2, 128, 24, None) == 3         # misaligned out
     assert f(16, 32, 0, 1.0, 48, 0, 2, 128, 64, None) == 0         # M == 0 no-op
     assert f(16, 32, 5, 1.0, 48, 4, 2, 128, 64, None) == 1         # bad weights dtype
+    assert f(16, 32, 2, 1.0, 48, 0, 2, 128, 64, None) == 0         # packed weights accepted
     assert f(16, 32, 0, float("inf"), 48, 4, 2, 128, 64, None) == 1  # non-finite scaling factor
 
 

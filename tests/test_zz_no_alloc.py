@@ -74,6 +74,6 @@ def test_plan_noalloc_small_input_and_size_limit():
     # more histogram entries than the fixed array holds: rejected on the host, nothing runs
     M, k, El = 1 << 20, 2, 512                           # 1024 blocks x 512 experts x 4 B > 1 MiB
     one = torch.zeros(16, dtype=torch.int32, device=DEV)
-    st = pkg.lib().moe_plan_noalloc(one.data_ptr(), M, k, El, 0, El, one.data_ptr(), one.data_ptr(),
+    st = pkg.lib().moe_plan_noalloc(one.data_ptr(), 0, M, k, El, 0, El, one.data_ptr(), one.data_ptr(),
                                     one.data_ptr(), one.data_ptr(), one.data_ptr(), None)
     assert st == 2                                       # MOE_ERR_UNSUPPORTED_SHAPE
