@@ -102,7 +102,9 @@ moe_status_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
   prm.act = g.act;
   prm.g2 = g.g2;
   const int64_t units_max = (g.cap / kTileM) * prm.n_tiles;
-  const size_t smem = static_cast<size_t>(kStages) * kStageBytes + kSmemExtra + (g.El + 1) * 4;
+  prm.sparse = (g.mode == kG1Fused || g.mode == kG2Rows || g.mode == kG2Reduce) && g.El <= kSparseMaxExperts;
+  const size_t smem = static_cast<size_t>(kStages) * kStageBytes + kSmemExtra + roundup64((g.El + 1) * 4, 16) +
+                      (prm.sparse ? kSparseStageBytes : 0);
   if (g.mode == kG2Rows || g.mode == kG2Reduce) return gemm::launch_rows(g.mode, prm, units_max, smem, s);
   switch (g.act) {
     case MOE_ACT_SWIGLU:

@@ -30,6 +30,12 @@ constexpr int kThreads = 320;  // producer, MMA, 8 epilogue warps
 constexpr int kEpiThreads = 256;
 constexpr int kSmemExtra = 1024 /*align*/ + 256 /*barriers*/;
 constexpr int kUnitRing = 4;      // work-unit ids handed from the producer to the other roles
+// Tiles whose real rows all lie in the first kSparseRows rows (decode: a few tokens per
+// expert) take the sparse epilogue: those rows' accumulators are staged in shared memory
+// and every epilogue thread takes a share of the outputs.
+constexpr int kSparseRows = 8;
+constexpr int kSparseStageBytes = kSparseRows * kTileN * 4 + kSparseRows * 8;  // FP32 rows, slot + scalar
+constexpr int kSparseMaxExperts = 384;  // above this the expert offsets leave no room for the stage
 constexpr int kRingConsumers = 1 + kEpiThreads / 32;  // MMA thread + one lane per epilogue warp
 
 static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
@@ -55,9 +61,14 @@ struct GemmParams {
   const void* route_w;  // kG2Reduce: route weights, their storage and the routed scaling factor
   int32_t route_w_dtype;
   float rsf;
+  int32_t sparse;       // the sparse epilogue is enabled (shared memory holds its stage)
 };
 
 __host__ __device__ constexpr bool is_g2(int mode) { return mode == kG2Rows || mode == kG2Reduce; }
+
+__device__ __forceinline__ void red_add_f32(float* out, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(out), "f"(v) : "memory");
+}
 
 // out[0..3] += v (FP32 additions performed at L2, in arrival order)
 __device__ __forceinline__ void red_add_f32x4(float* out, float a, float b, float c, float d) {
@@ -249,6 +260,135 @@ __device__ __forceinline__ void epilogue_compute(const GemmParams& p, uint32_t* 
   }
 }
 
+// The activation of GEMM1 on one output: gated kinds take the gate and up pre-activations.
+template <int ACT>
+__device__ __forceinline__ float activation_f32(float yg, float yu) {
+  if constexpr (ACT == MOE_ACT_SWIGLU) return __fmul_rn(silu_f32(yg), yu);
+  else if constexpr (ACT == MOE_ACT_GEGLU) return __fmul_rn(gelu_f32(yg), yu);
+  else if constexpr (ACT == MOE_ACT_RELU2) {
+    const float t = fmaxf(yg, 0.0f);
+    return __fmul_rn(t, t);
+  } else if constexpr (ACT == MOE_ACT_GELU) return gelu_f32(yg);
+  else if constexpr (ACT == MOE_ACT_SILU) return silu_f32(yg);
+  else if constexpr (ACT == MOE_ACT_RELU) return fmaxf(yg, 0.0f);
+  else return yg;
+}
+
+// Sparse epilogue of one work unit (all its real rows among the first kSparseRows rows).
+// The two warps that own TMEM lanes 0-31 copy the real rows' 256 accumulator columns into
+// the shared stage and release the accumulator; then all 256 epilogue threads share the
+// outputs: thread o of a pass handles output o (consecutive threads = consecutive columns
+// of a row), so a 16-value requant block is 16 lanes of one warp (block max by shuffles).
+// The arithmetic per value is the dense epilogue's. Returns false after an aborted wait.
+template <int MODE, int ACT>
+__device__ __noinline__ bool sparse_epilogue(const GemmParams& p, uint32_t tmem_row, int q, int half, int lane,
+                                                int etid, int e, int nt, int64_t row0, int slot, float scal,
+                                                float* s_stage, int32_t* s_slot, float* s_scal, uint64_t* acc_empty,
+                                                uint64_t* stage_full, uint64_t* stage_empty, uint32_t& sphase,
+                                                volatile int* abort_flag) {
+  constexpr bool kGated = is_gated(ACT);
+  // scalars of the expert, loaded while the stage fills
+  const float a1 = p.alpha[e];
+  const float a1g = (!is_g2(MODE) && kGated) ? p.alpha_gate[e] : a1;
+  if (q == 0) {
+    bool ok = mbar_wait(stage_empty, sphase ^ 1, abort_flag, p.dev_status);
+    if (!__all_sync(0xffffffffu, ok)) return false;
+    // 32 columns at a time (few registers: this path runs inside the dense epilogue's loop)
+    float4* dst = reinterpret_cast<float4*>(s_stage + (lane & (kSparseRows - 1)) * kTileN + half * 128);
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      uint32_t acc[32];
+      tmem_ld32_issue(tmem_row + half * 128 + c * 32, acc);
+      tmem_wait_ld<32>(acc);
+      if (lane < kSparseRows) {
+#pragma unroll
+        for (int v = 0; v < 8; ++v)
+          dst[c * 8 + v] = make_float4(__uint_as_float(acc[4 * v]), __uint_as_float(acc[4 * v + 1]),
+                                       __uint_as_float(acc[4 * v + 2]), __uint_as_float(acc[4 * v + 3]));
+      }
+    }
+    tc_fence_before();
+    mbar_arrive(acc_empty);
+    if (lane < kSparseRows) {
+      if (half == 0) {
+        s_slot[lane] = slot;
+        s_scal[lane] = scal;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(stage_full);
+  } else {
+    tc_fence_before();
+    mbar_arrive(acc_empty);
+  }
+  bool ok = mbar_wait(stage_full, sphase, abort_flag, p.dev_status);
+  if (!__all_sync(0xffffffffu, ok)) return false;
+  sphase ^= 1;
+  int nrows = 0;  // real rows lead the tile
+#pragma unroll
+  for (int i = 0; i < kSparseRows; ++i) nrows += s_slot[i] >= 0 ? 1 : 0;
+  if constexpr (is_g2(MODE)) {
+    const float d2 = __fmul_rn(a1, __fdiv_rn(1.0f, p.g2));
+    const int n_out = nrows * kTileN;
+    for (int o = etid; o < n_out; o += kEpiThreads) {
+      const int row = o >> 8, j = o & (kTileN - 1);
+      const int col = nt * kTileN + j;
+      if (col >= p.N) continue;
+      const float y = __fmul_rn(s_stage[row * kTileN + j], d2);
+      if constexpr (MODE == kG2Rows) {
+        static_cast<uint16_t*>(p.out)[(row0 + row) * p.N + col] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
+      } else {
+        const int t = s_slot[row] / p.top_k;
+        red_add_f32(static_cast<float*>(p.out) + static_cast<int64_t>(t) * p.N + col, __fmul_rn(y, s_scal[row]));
+      }
+    }
+  } else {
+    const int I = p.inter;
+    const int ip16 = static_cast<int>(roundup64(I, kTileK) / 16);
+    constexpr int kOut = kGated ? 128 : kTileN;  // intermediate columns per row of the tile
+    const int n_out = nrows * kOut;
+    uint8_t* out = static_cast<uint8_t*>(p.out);
+    // every lane runs every pass (the block max is a warp shuffle); 16-lane groups are
+    // wholly valid or wholly not
+    for (int o0 = 0; o0 < n_out; o0 += kEpiThreads) {
+      const int o = o0 + etid;
+      const int row = (o / kOut) & (kSparseRows - 1);
+      const int j = o % kOut;
+      const int ic = kGated ? nt * 128 + j : nt * kTileN + j;
+      const bool valid = o < n_out && ic < I;
+      float h = 0.0f;
+      if (valid) {
+        const float xs_t = s_scal[row];
+        const float* st = s_stage + row * kTileN;
+        const float yg = __fmul_rn(__fmul_rn(st[j], xs_t), kGated ? a1g : a1);
+        const float yu = kGated ? __fmul_rn(__fmul_rn(st[128 + j], xs_t), a1) : 0.0f;
+        h = bf16_round_f32(activation_f32<ACT>(yg, yu));
+      }
+      float amax = fmaxf(0.0f, fabsf(h));
+#pragma unroll
+      for (int m = 8; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+      const float sc = __fmul_rn(__fdiv_rn(amax, 6.0f), p.g2);
+      const uint32_t qs = f32_to_e4m3(sc);
+      const float qf = e4m3_to_f32(qs);
+      const float inv = (qf == 0.0f) ? 0.0f : __fdiv_rn(p.g2, qf);
+      const float hn = __shfl_down_sync(0xffffffffu, h, 1);
+      if (valid) {
+        const int64_t prow = row0 + row;
+        if ((j & 1) == 0) out[prow * (I / 2) + ic / 2] = static_cast<uint8_t>(f32x2_to_e2m1(__fmul_rn(h, inv), __fmul_rn(hn, inv)));
+        if ((j & 15) == 0) p.out_sf[sf_tile_offset(prow, ic >> 4, ip16)] = static_cast<uint8_t>(qs);
+      }
+    }
+    // zero the scale columns of the K padding once per real row (last column tile)
+    if (nt == p.n_tiles - 1 && etid < nrows) {
+      for (int c4 = I / 64; c4 < ip16 / 4; ++c4)
+        *reinterpret_cast<uint32_t*>(p.out_sf + sf_tile_offset(row0 + etid, 4 * c4, ip16)) = 0u;
+    }
+  }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(stage_empty);
+  return true;
+}
+
 template <int MODE, int ACT>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -260,10 +400,16 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
   uint64_t* final_bar = acc_empty + 1;
   uint64_t* unit_full = final_bar + 1;
   uint64_t* unit_empty = unit_full + kUnitRing;
-  volatile int32_t* unit_ring = reinterpret_cast<volatile int32_t*>(unit_empty + kUnitRing);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(unit_empty + kUnitRing) + kUnitRing;
+  uint64_t* stage_full = unit_empty + kUnitRing;
+  uint64_t* stage_empty = stage_full + 1;
+  volatile int32_t* unit_ring = reinterpret_cast<volatile int32_t*>(stage_empty + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stage_empty + 1) + kUnitRing;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int32_t* s_off = reinterpret_cast<int32_t*>(smem + kStages * kStageBytes + 256);
+  // sparse-epilogue stage: [kSparseRows][kTileN] FP32, then per-row slot and scalar
+  float* s_stage = reinterpret_cast<float*>(smem + kStages * kStageBytes + 256 + roundup64((p.El + 1) * 4, 16));
+  int32_t* s_slot = reinterpret_cast<int32_t*>(s_stage + kSparseRows * kTileN);
+  float* s_scal = reinterpret_cast<float*>(s_slot + kSparseRows);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_trigger();
@@ -279,6 +425,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       mbar_init(&unit_full[i], 1);
       mbar_init(&unit_empty[i], kRingConsumers);
     }
+    mbar_init(stage_full, 2);                  // the two warps holding TMEM lanes 0-31
+    mbar_init(stage_empty, kEpiThreads / 32);  // one arrival per epilogue warp
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -407,20 +555,32 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     const int half = (warp - 2) >> 2;       // column half of the tile
     const int r = q * 32 + lane;            // row inside the 128-row tile
     const uint32_t tmem_row = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    uint32_t acc_phase = 0;
+    uint32_t acc_phase = 0, sphase = 0;
     uint32_t rslot = 0, rphase = 0;
+    const int etid = threadIdx.x - 64;      // 0..255 over the epilogue warps
     while (true) {
       const int u = take_unit(rslot, rphase, false);
       if (u < 0) break;
       int e, nt, mi;
       decode_unit(u, s_off, p.El, p.n_tiles, e, nt, mi);
-      const int64_t prow = s_off[e] + mi * kTileM + r;
+      const int64_t row0 = s_off[e] + mi * kTileM;
+      const int64_t prow = row0 + r;
       const int slot = p.row_to_slot[prow];
       const float xs_t = (!is_g2(MODE) && slot >= 0) ? p.xs[slot / p.top_k] : 0.0f;
+      const bool sparse = (MODE == kG1Fused || is_g2(MODE)) && p.sparse && p.row_to_slot[row0 + kSparseRows] < 0;
+      float scal = xs_t;
+      if constexpr (MODE == kG2Reduce) scal = slot >= 0 ? route_weight(p.route_w, p.route_w_dtype, slot, p.rsf) : 0.0f;
       bool ok = mbar_wait(acc_full, acc_phase, abort_flag, p.dev_status);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
+      if (sparse) {
+        acc_phase ^= 1;
+        if (!sparse_epilogue<MODE, ACT>(p, tmem_row, q, half, lane, etid, e, nt, row0, slot, scal, s_stage, s_slot,
+                                        s_scal, acc_empty, stage_full, stage_empty, sphase, abort_flag))
+          break;
+        continue;
+      }
       uint32_t acc[128];
       load_acc<MODE, ACT>(tmem_row, half, acc, acc_empty);
       acc_phase ^= 1;
