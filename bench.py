@@ -196,11 +196,11 @@ def run_gpu(args, cfg, rank, world):
     tw_t = torch.from_numpy(tw).to(dev)
     M, k = ids.shape
     mode = OUTPUT_MODES[args.output]
-    b = layer.buffers(M, k, mode)
+    b = layer.routed_buffers(M, k, mode)
     # accumulated output: every step adds into this caller-owned tensor
     acc_out = torch.zeros(M, cfg.H, dtype=torch.bfloat16, device=dev) if mode == 2 else None
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    n_ev = 8
+    n_ev = 5
     K, W = args.steps, args.warmup
 
     # the timed step: one CUDA-graph replay of the whole path
@@ -242,17 +242,13 @@ def run_gpu(args, cfg, rank, world):
     torch.cuda._sleep(int(60e6))   # ~30 ms at 2 GHz
     for e in evs:
         flush.zero_()
-        e[0].record()
-        layer.quantize(x, b)
-        e[1].record()
-        layer.plan(ids_t, b)
-        layer.experts(tw_t, b, mode, step_events=e[2:7], out=acc_out)
-        e[7].record()
+        layer.routed(x, ids_t, tw_t, b, mode, step_events=e, out=acc_out)
     torch.cuda.synchronize()
     kern_times = [[e[j].elapsed_time(e[j + 1]) for j in range(n_ev - 1)] for e in evs]
-    eager_ms = float(np.mean([e[0].elapsed_time(e[7]) for e in evs]))
+    eager_ms = float(np.mean([e[0].elapsed_time(e[4]) for e in evs]))
     assert layer.device_status(M, k, mode) == 0, "device status word set"
-    names = ["quantize", "plan", "permute", "gemm1", "gemm2", "finalize"]
+    # prologue = quantise + plan + permute (one kernel for small batches)
+    names = ["prologue", "gemm1", "gemm2", "combine"]
     per = {n: [t[c] for t in kern_times] for c, n in enumerate(names)}
     steps_ms = step_times
     ms = float(np.mean(steps_ms))
@@ -282,7 +278,8 @@ def run_gpu(args, cfg, rank, world):
     step_roof_s = max(stepw["bytes"] / (peaks["hbm_gbs"] * 1e9), stepw["flops"] / (fp4_peak * 1e12))
     # end to end through the public API with host buffers
     e2e = None if args.no_e2e else run_e2e(layer, x, ids, tw, dev, max(3, min(K, 50)))
-    launches_per_step = 6 + (2 if M * k > 2048 else 0)
+    small = M * k <= 2048 and M * cfg.H <= (1 << 17)
+    launches_per_step = 4 if small else 6 + (2 if M * k > 2048 else 0)
     res = {
         "metric": METRIC, "value": world * M / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -325,7 +322,7 @@ def run_e2e(layer, x, ids, tw, dev, steps):
     did.copy_(hid)
     dtw.copy_(htw)
     graph = layer.capture(dx, did, dtw, True)
-    out = layer.buffers(M, k, True)["out"]
+    out = layer.routed_buffers(M, k, True)["out"]
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     times = []
     for i in range(steps + 3):

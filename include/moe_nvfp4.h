@@ -8,6 +8,7 @@
  *   moe_grouped_fp4_forward permute -> GEMM1 + activation + NVFP4 requant -> GEMM2
  *                           -> finalize (or the unfinalized rows)
  *   moe_finalize            ordered FP32 combine of unfinalized rows (standalone)
+ *   moe_routed_forward      all of the above in one call, from BF16 hidden states
  *
  * plus one-time weight preparation (moe_quantize_weights, moe_prepare_weights).
  *
@@ -296,6 +297,40 @@ MOE_API moe_status_t moe_finalize(const uint16_t* gemm2_out, const void* topk_we
                           int32_t topk_weights_dtype, float routed_scaling_factor,
                           const int32_t* token_to_row, int32_t M, int32_t top_k, int32_t H,
                           uint16_t* out, moe_stream_t stream);
+
+/* ----------------------------------------------------------------------------------------
+ * moe_routed_forward - the whole layer in one call ([MCORE] flashinfer_routed_nvfp4_moe:
+ * BF16 hidden states, routing map and probabilities in, the layer output out). It computes
+ * exactly what moe_quantize_input, moe_plan and moe_grouped_fp4_forward compute in sequence
+ * (bit for bit, except the order of the FP32 additions of MOE_OUTPUT_ACCUMULATE). For small
+ * batches (M * top_k <= 2048 and M * H <= 131072) the quantiser, the plan and the
+ * permutation run as one kernel of one CTA.
+ *   x             [M, ld_x] BF16 hidden states (first H columns used), ld_x >= H, ld_x % 8 == 0
+ *   act_scale_mode  moe_act_scale_t, as moe_quantize_input
+ *   topk_ids, topk_ids_format, num_experts, local_expert_offset  as moe_plan
+ *   topk_weights, topk_weights_dtype, routed_scaling_factor, w, prepared, fc2_input_scale,
+ *   do_finalize, out, gemm2_out  as moe_grouped_fp4_forward (packed slots may pass the same
+ *                 buffer as topk_ids and topk_weights)
+ *   token_to_row  [M, top_k] int32 (out): the plan row of each slot or -1 (the third element of
+ *                 the unfinalized result)
+ *   workspace     moe_routed_forward_workspace_bytes(M, top_k, w, do_finalize) bytes; it holds
+ *                 the activation pack, the plan and the forward workspace
+ *   step_events   0 or 5 cudaEvent_t recorded before the prologue (quantise, plan, permute),
+ *                 GEMM1, GEMM2, the combine, and at the end
+ * Outputs must not overlap any input, the workspace or each other (MOE_ERR_OVERLAP).
+ * ---------------------------------------------------------------------------------------- */
+MOE_API size_t moe_routed_forward_workspace_bytes(int32_t M, int32_t top_k, const moe_nvfp4_weights_t* w,
+                                                  int32_t do_finalize);
+MOE_API moe_status_t moe_routed_forward(const uint16_t* x, int32_t M, int64_t ld_x, int32_t act_scale_mode,
+                                        const int32_t* topk_ids, int32_t topk_ids_format, int32_t top_k,
+                                        int32_t num_experts, int32_t local_expert_offset,
+                                        const void* topk_weights, int32_t topk_weights_dtype,
+                                        float routed_scaling_factor, const moe_nvfp4_weights_t* w,
+                                        const void* prepared, size_t prepared_bytes, float fc2_input_scale,
+                                        int32_t do_finalize, uint16_t* out, uint16_t* gemm2_out,
+                                        int32_t* token_to_row, void* workspace, size_t workspace_bytes,
+                                        int32_t* dev_status, void* const* step_events, int32_t num_step_events,
+                                        moe_stream_t stream);
 
 /* ----------------------------------------------------------------------------------------
  * Test hook: runs the forward's permute and GEMM1 with a plain epilogue instead of the

@@ -15,7 +15,7 @@ from ._lib import (  # noqa: F401
     moe_abi_version, moe_debug_gemm1, moe_finalize, moe_forward_workspace_bytes,
     moe_forward_workspace_layout, moe_grouped_fp4_forward, moe_plan, moe_plan_capacity,
     moe_plan_workspace_bytes, moe_plan_noalloc, moe_prepare_weights, moe_prepared_weights_bytes, moe_quantize_input,
-    moe_quantize_weights, status_string,
+    moe_quantize_weights, moe_routed_forward, moe_routed_forward_workspace_bytes, status_string,
 )
 from .build import LIB as LIB_PATH  # noqa: F401
 from .moe import NVFP4RoutedMoE, quantize_weights  # noqa: F401

@@ -29,6 +29,7 @@ EXPORTED = [
     "moe_plan_workspace_bytes", "moe_plan", "moe_quantize_weights", "moe_prepared_weights_bytes",
     "moe_prepare_weights", "moe_forward_workspace_bytes", "moe_forward_workspace_layout",
     "moe_grouped_fp4_forward", "moe_finalize", "moe_debug_gemm1", "moe_plan_noalloc",
+    "moe_routed_forward_workspace_bytes", "moe_routed_forward",
 ]
 MOE_PLAN_NOALLOC_SCRATCH_BYTES = 1 << 20
 
@@ -69,6 +70,10 @@ def _declare(lib):
                                               P, c_size_t, P, c_int32, c_float, c_float, c_int32, P, P, P,
                                               c_size_t, P, ctypes.POINTER(c_void_p), c_int32, P]),
         "moe_finalize": (c_int32, [P, P, c_int32, c_float, P, c_int32, c_int32, c_int32, P, P]),
+        "moe_routed_forward_workspace_bytes": (c_size_t, [c_int32, c_int32, ctypes.POINTER(WeightsT), c_int32]),
+        "moe_routed_forward": (c_int32, [P, c_int32, c_int64, c_int32, P, c_int32, c_int32, c_int32, c_int32, P,
+                                         c_int32, c_float, ctypes.POINTER(WeightsT), P, c_size_t, c_float, c_int32,
+                                         P, P, P, P, c_size_t, P, ctypes.POINTER(c_void_p), c_int32, P]),
         "moe_debug_gemm1": (c_int32, [P, P, c_int32, c_int32, P, P, P, ctypes.POINTER(WeightsT), P,
                                       c_size_t, c_int32, P, P, c_size_t, P, P]),
     }
@@ -200,19 +205,41 @@ def _weights_dtype(topk_weights) -> int:
     raise MoEError("topk_weights must be float32, bfloat16 or int32 (packed)")
 
 
+def _events(step_events):
+    if not step_events:
+        return None, 0
+    handles = [e.cuda_event for e in step_events]
+    if not all(handles):
+        raise MoEError("step_events: torch creates an event on its first record(); record each once first")
+    return (c_void_p * len(step_events))(*handles), len(step_events)
+
+
+def moe_routed_forward_workspace_bytes(M, top_k, w: WeightsT, do_finalize) -> int:
+    return lib().moe_routed_forward_workspace_bytes(M, top_k, ctypes.byref(w), int(do_finalize))
+
+
+def moe_routed_forward(x, act_scale_mode, topk_ids, num_experts, local_expert_offset, topk_weights, w: WeightsT,
+                       prepared, fc2_input_scale, do_finalize, out, gemm2_out, token_to_row, workspace, dev_status,
+                       step_events=None, stream=None, routed_scaling_factor=1.0, packed=False):
+    """The whole layer from BF16 hidden states x [M, H] (one C call). packed=True: topk_ids holds
+    packed slots (and topk_weights may be the same tensor)."""
+    M, k = topk_ids.shape
+    ev, nev = _events(step_events)
+    _check(lib().moe_routed_forward(
+        _ptr(x), M, x.stride(0), act_scale_mode, _ptr(topk_ids), MOE_IDS_PACKED if packed else MOE_IDS_INT32, k,
+        num_experts, local_expert_offset, _ptr(topk_weights), _weights_dtype(topk_weights),
+        float(routed_scaling_factor), ctypes.byref(w), _ptr(prepared), prepared.numel() * prepared.element_size(),
+        float(fc2_input_scale), int(do_finalize), _ptr(out), _ptr(gemm2_out), _ptr(token_to_row), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(dev_status), ev, nev, _stream(stream)),
+        "moe_routed_forward")
+
+
 def moe_grouped_fp4_forward(padded_offsets, row_to_slot, token_to_row, xq, xsf, xs, w: WeightsT, prepared,
                             topk_weights, fc2_input_scale, do_finalize, out, gemm2_out, workspace,
                             dev_status, step_events=None, stream=None, routed_scaling_factor=1.0):
     """do_finalize: 0/False unfinalized rows, 1/True ordered finalize, 2 accumulate into out."""
     M, k = token_to_row.shape
-    ev = None
-    nev = 0
-    if step_events:
-        handles = [e.cuda_event for e in step_events]
-        if not all(handles):
-            raise MoEError("step_events: torch creates an event on its first record(); record each once first")
-        ev = (c_void_p * len(step_events))(*handles)
-        nev = len(step_events)
+    ev, nev = _events(step_events)
     _check(lib().moe_grouped_fp4_forward(
         _ptr(padded_offsets), _ptr(row_to_slot), _ptr(token_to_row), M, k, _ptr(xq), _ptr(xsf), _ptr(xs),
         ctypes.byref(w), _ptr(prepared), prepared.numel() * prepared.element_size(), _ptr(topk_weights),

@@ -17,7 +17,9 @@ namespace {
 
 bool valid_output_mode(int32_t m) { return m >= MOE_OUTPUT_UNFINALIZED && m <= MOE_OUTPUT_ACCUMULATE; }
 
-moe_status_t check_weights(const moe_nvfp4_weights_t* w) {
+}  // namespace
+
+moe_status_t moe::check_weights(const moe_nvfp4_weights_t* w) {
   MOE_CHECK(w != nullptr, MOE_ERR_INVALID_ARGUMENT);
   MOE_CHECK(w->activation >= MOE_ACT_SWIGLU && w->activation <= MOE_ACT_IDENTITY, MOE_ERR_INVALID_ARGUMENT);
   MOE_CHECK(w->num_local_experts >= 1 && w->hidden > 0 && w->inter > 0, MOE_ERR_INVALID_ARGUMENT);
@@ -26,6 +28,8 @@ moe_status_t check_weights(const moe_nvfp4_weights_t* w) {
   MOE_CHECK(w->hidden <= 65536 && w->inter <= 65536, MOE_ERR_UNSUPPORTED_SHAPE);
   return MOE_OK;
 }
+
+namespace {
 
 struct Bufs {
   int32_t* sched;
@@ -184,60 +188,23 @@ extern "C" moe_status_t moe_forward_workspace_layout(int32_t M, int32_t top_k, c
   return MOE_OK;
 }
 
-extern "C" moe_status_t moe_grouped_fp4_forward(const int32_t* padded_offsets, const int32_t* row_to_slot,
-                                                const int32_t* token_to_row, int32_t M, int32_t top_k,
-                                                const uint8_t* xq, const uint8_t* xsf, const float* xs,
-                                                const moe_nvfp4_weights_t* w, const void* prepared,
-                                                size_t prepared_bytes, const void* topk_weights,
-                                                int32_t topk_weights_dtype, float routed_scaling_factor,
-                                                float fc2_input_scale, int32_t do_finalize, uint16_t* out,
-                                                uint16_t* gemm2_out, void* workspace, size_t workspace_bytes,
-                                                int32_t* dev_status, void* const* step_events,
-                                                int32_t num_step_events, moe_stream_t stream) {
-  moe_status_t st = check_weights(w);
-  if (st != MOE_OK) return st;
-  MOE_CHECK(M >= 0 && top_k >= 1 && valid_output_mode(do_finalize), MOE_ERR_INVALID_ARGUMENT);
+namespace moe {
+
+// The launches of one forward after validation: permute (unless a fused prologue already
+// laid the rows out), GEMM1 with the fused activation and requant, GEMM2, and the combine.
+moe_status_t forward_chain(const int32_t* padded_offsets, const int32_t* row_to_slot, const int32_t* token_to_row,
+                           int32_t M, int32_t top_k, const uint8_t* xq, const uint8_t* xsf, const float* xs,
+                           const moe_nvfp4_weights_t* w, const void* prepared, const void* topk_weights,
+                           int32_t topk_weights_dtype, float routed_scaling_factor, float fc2_input_scale,
+                           int32_t do_finalize, uint16_t* out, uint16_t* gemm2_out, void* workspace,
+                           int32_t* dev_status, void* const* step_events, int32_t num_step_events, bool run_permute,
+                           cudaStream_t s) {
   const Dims d = make_dims(w);
   const bool fin = do_finalize == MOE_OUTPUT_FINALIZED;
   const bool accum = do_finalize == MOE_OUTPUT_ACCUMULATE;
   const WorkspaceLayout L = workspace_layout(d, M, top_k, do_finalize);
-  st = check_forward_common(padded_offsets, row_to_slot, M, top_k, xq, xsf, xs, w, prepared, prepared_bytes,
-                            workspace, workspace_bytes, dev_status, L.total);
-  if (st != MOE_OK) return st;
-  MOE_CHECK(isfinite(fc2_input_scale) && fc2_input_scale > 0.0f, MOE_ERR_INVALID_ARGUMENT);
-  MOE_CHECK(isfinite(routed_scaling_factor), MOE_ERR_INVALID_ARGUMENT);
-  MOE_CHECK(topk_weights_dtype >= MOE_WEIGHTS_F32 && topk_weights_dtype <= MOE_WEIGHTS_PACKED,
-            MOE_ERR_INVALID_ARGUMENT);
-  const size_t wbytes = static_cast<size_t>(M) * top_k * (topk_weights_dtype == MOE_WEIGHTS_BF16 ? 2 : 4);
-  MOE_CHECK(num_step_events == 0 || (num_step_events == 5 && step_events != nullptr), MOE_ERR_INVALID_ARGUMENT);
-  if (M == 0) return MOE_OK;
-  MOE_CHECK(token_to_row && topk_weights, MOE_ERR_INVALID_ARGUMENT);
-  MOE_CHECK(aligned16(token_to_row) && aligned16(topk_weights), MOE_ERR_MISALIGNED);
-  uint16_t* rows_out;
-  if (fin || accum) {
-    MOE_CHECK(out != nullptr, MOE_ERR_INVALID_ARGUMENT);
-    MOE_CHECK(aligned16(out), MOE_ERR_MISALIGNED);
-    const size_t ob = static_cast<size_t>(M) * d.H * 2;
-    MOE_CHECK(!overlaps(out, ob, xq, static_cast<size_t>(M) * d.H / 2) &&
-                  !overlaps(out, ob, xsf, static_cast<size_t>(M) * d.H / 16) &&
-                  !overlaps(out, ob, xs, static_cast<size_t>(M) * 4) &&
-                  !overlaps(out, ob, topk_weights, wbytes) &&
-                  !overlaps(out, ob, token_to_row, static_cast<size_t>(M) * top_k * 4) &&
-                  !overlaps(out, ob, workspace, L.total) && !overlaps(out, ob, prepared, prepared_bytes),
-              MOE_ERR_OVERLAP);
-    rows_out = nullptr;  // set after carving
-  } else {
-    MOE_CHECK(gemm2_out != nullptr, MOE_ERR_INVALID_ARGUMENT);
-    MOE_CHECK(aligned16(gemm2_out), MOE_ERR_MISALIGNED);
-    const size_t gb = static_cast<size_t>(L.cap) * d.H * 2;
-    MOE_CHECK(!overlaps(gemm2_out, gb, workspace, L.total) && !overlaps(gemm2_out, gb, prepared, prepared_bytes) &&
-                  !overlaps(gemm2_out, gb, xq, static_cast<size_t>(M) * d.H / 2),
-              MOE_ERR_OVERLAP);
-    rows_out = gemm2_out;
-  }
-  cudaStream_t s = as_stream(stream);
   const Bufs b = carve(workspace, L);
-  if (fin) rows_out = b.g;
+  uint16_t* rows_out = fin ? b.g : gemm2_out;
   float* acc = accum ? reinterpret_cast<float*>(b.g) : nullptr;
   const Prepared pw = prepared_ptrs(prepared, prepared_layout(d));
   // while the stream is being captured, the marks become external event-record nodes so the
@@ -253,10 +220,12 @@ extern "C" moe_status_t moe_grouped_fp4_forward(const int32_t* padded_offsets, c
       MOE_CUDA(cudaEventRecord(ev, s));
     return MOE_OK;
   };
+  moe_status_t st = MOE_OK;
   if ((st = mark(0)) != MOE_OK) return st;
-  st = launch_permute(padded_offsets, static_cast<int>(d.El), row_to_slot, top_k, L.cap, xq, xsf,
-                      static_cast<int>(d.H), b.aq, b.asf, b.sched, accum ? out : nullptr, acc,
-                      accum ? static_cast<int64_t>(M) * d.H : 0, s);
+  if (run_permute)
+    st = launch_permute(padded_offsets, static_cast<int>(d.El), row_to_slot, top_k, L.cap, xq, xsf,
+                        static_cast<int>(d.H), b.aq, b.asf, b.sched, accum ? out : nullptr, acc,
+                        accum ? static_cast<int64_t>(M) * d.H : 0, s);
   if (st != MOE_OK) return st;
   if ((st = mark(1)) != MOE_OK) return st;
   GemmLaunch g1 = gemm1_launch(d, L, b, pw, padded_offsets, row_to_slot, xs, top_k, dev_status);
@@ -305,6 +274,61 @@ extern "C" moe_status_t moe_grouped_fp4_forward(const int32_t* padded_offsets, c
     if (st != MOE_OK) return st;
   }
   return mark(4);
+}
+
+}  // namespace moe
+
+extern "C" moe_status_t moe_grouped_fp4_forward(const int32_t* padded_offsets, const int32_t* row_to_slot,
+                                                const int32_t* token_to_row, int32_t M, int32_t top_k,
+                                                const uint8_t* xq, const uint8_t* xsf, const float* xs,
+                                                const moe_nvfp4_weights_t* w, const void* prepared,
+                                                size_t prepared_bytes, const void* topk_weights,
+                                                int32_t topk_weights_dtype, float routed_scaling_factor,
+                                                float fc2_input_scale, int32_t do_finalize, uint16_t* out,
+                                                uint16_t* gemm2_out, void* workspace, size_t workspace_bytes,
+                                                int32_t* dev_status, void* const* step_events,
+                                                int32_t num_step_events, moe_stream_t stream) {
+  moe_status_t st = check_weights(w);
+  if (st != MOE_OK) return st;
+  MOE_CHECK(M >= 0 && top_k >= 1 && valid_output_mode(do_finalize), MOE_ERR_INVALID_ARGUMENT);
+  const Dims d = make_dims(w);
+  const bool fin = do_finalize == MOE_OUTPUT_FINALIZED;
+  const bool accum = do_finalize == MOE_OUTPUT_ACCUMULATE;
+  const WorkspaceLayout L = workspace_layout(d, M, top_k, do_finalize);
+  st = check_forward_common(padded_offsets, row_to_slot, M, top_k, xq, xsf, xs, w, prepared, prepared_bytes,
+                            workspace, workspace_bytes, dev_status, L.total);
+  if (st != MOE_OK) return st;
+  MOE_CHECK(isfinite(fc2_input_scale) && fc2_input_scale > 0.0f, MOE_ERR_INVALID_ARGUMENT);
+  MOE_CHECK(isfinite(routed_scaling_factor), MOE_ERR_INVALID_ARGUMENT);
+  MOE_CHECK(topk_weights_dtype >= MOE_WEIGHTS_F32 && topk_weights_dtype <= MOE_WEIGHTS_PACKED,
+            MOE_ERR_INVALID_ARGUMENT);
+  const size_t wbytes = static_cast<size_t>(M) * top_k * (topk_weights_dtype == MOE_WEIGHTS_BF16 ? 2 : 4);
+  MOE_CHECK(num_step_events == 0 || (num_step_events == 5 && step_events != nullptr), MOE_ERR_INVALID_ARGUMENT);
+  if (M == 0) return MOE_OK;
+  MOE_CHECK(token_to_row && topk_weights, MOE_ERR_INVALID_ARGUMENT);
+  MOE_CHECK(aligned16(token_to_row) && aligned16(topk_weights), MOE_ERR_MISALIGNED);
+  if (fin || accum) {
+    MOE_CHECK(out != nullptr, MOE_ERR_INVALID_ARGUMENT);
+    MOE_CHECK(aligned16(out), MOE_ERR_MISALIGNED);
+    const size_t ob = static_cast<size_t>(M) * d.H * 2;
+    MOE_CHECK(!overlaps(out, ob, xq, static_cast<size_t>(M) * d.H / 2) &&
+                  !overlaps(out, ob, xsf, static_cast<size_t>(M) * d.H / 16) &&
+                  !overlaps(out, ob, xs, static_cast<size_t>(M) * 4) &&
+                  !overlaps(out, ob, topk_weights, wbytes) &&
+                  !overlaps(out, ob, token_to_row, static_cast<size_t>(M) * top_k * 4) &&
+                  !overlaps(out, ob, workspace, L.total) && !overlaps(out, ob, prepared, prepared_bytes),
+              MOE_ERR_OVERLAP);
+  } else {
+    MOE_CHECK(gemm2_out != nullptr, MOE_ERR_INVALID_ARGUMENT);
+    MOE_CHECK(aligned16(gemm2_out), MOE_ERR_MISALIGNED);
+    const size_t gb = static_cast<size_t>(L.cap) * d.H * 2;
+    MOE_CHECK(!overlaps(gemm2_out, gb, workspace, L.total) && !overlaps(gemm2_out, gb, prepared, prepared_bytes) &&
+                  !overlaps(gemm2_out, gb, xq, static_cast<size_t>(M) * d.H / 2),
+              MOE_ERR_OVERLAP);
+  }
+  return forward_chain(padded_offsets, row_to_slot, token_to_row, M, top_k, xq, xsf, xs, w, prepared, topk_weights,
+                       topk_weights_dtype, routed_scaling_factor, fc2_input_scale, do_finalize, out, gemm2_out,
+                       workspace, dev_status, step_events, num_step_events, true, as_stream(stream));
 }
 
 extern "C" moe_status_t moe_debug_gemm1(const int32_t* padded_offsets, const int32_t* row_to_slot, int32_t M,

@@ -94,6 +94,26 @@ __device__ __forceinline__ uint32_t quantize_block16(const float* x, float g, ui
   return q;
 }
 
+constexpr float kGlobalNumerator = 2688.0f;  // FLOAT8_E4M3_MAX * FLOAT4_E2M1_MAX: g_enc = 2688 / amax
+
+// 16 BF16 values (two 16-byte loads) -> FP32
+__device__ __forceinline__ void load_block16(const uint16_t* src, float* v) {
+  const uint4 a = *reinterpret_cast<const uint4*>(src);
+  const uint4 b = *reinterpret_cast<const uint4*>(src + 8);
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
 // Route weight of slot i stored as FP32, BF16 or packed (BF16 score in bits 31..16),
 // times the routed scaling factor: fp32(w * rsf).
 __device__ __forceinline__ float route_weight(const void* w, int dtype, int64_t i, float rsf) {

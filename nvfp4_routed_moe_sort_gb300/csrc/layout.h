@@ -136,6 +136,16 @@ moe_status_t launch_permute(const int32_t* padded_offsets, int El, const int32_t
 moe_status_t launch_finalize(const uint16_t* rows, const void* topk_weights, int weights_dtype, float rsf,
                              const int32_t* token_to_row, int M, int top_k, int H, uint16_t* out, cudaStream_t s);
 moe_status_t launch_store_acc(const float* acc, int64_t elems, uint16_t* out, cudaStream_t s);
+// sizes, activation and expert count of a weights descriptor (api.cu)
+moe_status_t check_weights(const moe_nvfp4_weights_t* w);
+// permute (optional), GEMM1, GEMM2 and the combine of one validated forward (api.cu)
+moe_status_t forward_chain(const int32_t* padded_offsets, const int32_t* row_to_slot, const int32_t* token_to_row,
+                           int32_t M, int32_t top_k, const uint8_t* xq, const uint8_t* xsf, const float* xs,
+                           const moe_nvfp4_weights_t* w, const void* prepared, const void* topk_weights,
+                           int32_t topk_weights_dtype, float routed_scaling_factor, float fc2_input_scale,
+                           int32_t do_finalize, uint16_t* out, uint16_t* gemm2_out, void* workspace,
+                           int32_t* dev_status, void* const* step_events, int32_t num_step_events, bool run_permute,
+                           cudaStream_t s);
 moe_status_t launch_prepare_matrix(const uint8_t* src, const uint8_t* src_sf, int E, int rows, int rows_p, int K,
                                    int gated_inter, uint8_t* dst, uint8_t* dst_sf, cudaStream_t s);
 

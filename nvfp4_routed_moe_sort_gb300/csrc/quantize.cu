@@ -19,26 +19,7 @@
 namespace moe {
 namespace {
 
-constexpr float kGlobalNumerator = 2688.0f;  // FLOAT8_E4M3_MAX * FLOAT4_E2M1_MAX
-
 enum GScale : int { kGOne = 0, kGPerRow = 1, kGPerMatrix = 2 };
-
-__device__ __forceinline__ void load_block16(const uint16_t* src, float* v) {
-  const uint4 a = *reinterpret_cast<const uint4*>(src);
-  const uint4 b = *reinterpret_cast<const uint4*>(src + 8);
-  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    v[2 * i] = __uint_as_float(w[i] << 16);
-    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-  }
-}
-
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
 
 // rows [0, rows_total) of a [rows_total, ld] BF16 matrix -> data [rows_total, cols/2],
 // sf [rows_total, cols/16]. Global encode scale per `gmode`; the decode scale goes to

@@ -1,0 +1,315 @@
+// The whole layer in one call: BF16 hidden states and routing in, the combined BF16 output
+// (or the unfinalized rows) out.
+//
+// Sources: Megatron-Core core.inference.moe.flashinfer_nvfp4 (flashinfer_routed_nvfp4_moe:
+// hidden states, routing map and probabilities in, the layer output out;
+// quantize_routed_nvfp4_input); FlashInfer flashinfer.fused_moe.CudnnGroupedGemmNvfp4Config
+// (Pipeline: NVFP4 activation pack, expert-sorted permutation, GEMM1, typed activation,
+// GEMM2, finalize).
+//
+// Small batches (decode: at most 2048 routed slots and 2^17 hidden values) run the
+// quantiser, the plan and the permutation in one kernel of one 1024-thread CTA, so the step
+// is four launches (prologue, GEMM1, GEMM2, combine) instead of six; each of those steps is
+// latency-bound at these sizes. Larger batches run the separate kernels of
+// moe_quantize_input, moe_plan and moe_grouped_fp4_forward. Both paths compute the same
+// bytes: the prologue's quantiser and plan follow the same arithmetic and order as the
+// separate kernels.
+#include <math.h>
+
+#include "common.cuh"
+#include "host_util.h"
+#include "layout.h"
+#include "plan_device.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kPrologueThreads = kPlanThreads;               // 1024
+constexpr int64_t kPrologueMaxSlots = kSlotsPerBlock;        // the one-block plan
+constexpr int64_t kPrologueMaxValues = int64_t(1) << 17;     // M * H
+
+// Routed-call workspace: activation pack, plan arrays and scratch, then the forward workspace.
+struct RoutedLayout {
+  size_t xq, xsf, xs, counts, padded, r2s, plan_ws, fwd, total;
+  int64_t cap;
+};
+
+RoutedLayout routed_layout(const Dims& d, int64_t M, int64_t k, int out_mode) {
+  RoutedLayout R;
+  size_t c = 0;
+  R.cap = plan_capacity_rows(M, k, d.El);
+  R.xq = take(c, M * d.H / 2);
+  R.xsf = take(c, M * d.H / 16);
+  R.xs = take(c, M * 4);
+  R.counts = take(c, d.El * 4);
+  R.padded = take(c, (d.El + 1) * 4);
+  R.r2s = take(c, (R.cap > 0 ? R.cap : 1) * 4);
+  R.plan_ws = take(c, moe_plan_workspace_bytes(static_cast<int32_t>(M), static_cast<int32_t>(k),
+                                               static_cast<int32_t>(d.El)));
+  R.fwd = take(c, workspace_layout(d, M, k, out_mode).total);
+  R.total = c;
+  return R;
+}
+
+bool small_batch(int64_t M, int64_t k, int64_t H) {
+  return M * k <= kPrologueMaxSlots && M * H <= kPrologueMaxValues;
+}
+
+constexpr int kPrologueMaxRows = static_cast<int>(kPrologueMaxValues / 128);  // H >= 128
+constexpr int kCopyBatch = 4;  // loads in flight per thread in the copy loops
+
+// One CTA, every phase spread over all 1024 threads:
+//  (0) the routed-slot histogram;
+//  (1) NVFP4 quantisation: thread per 16-value block of the M x H input (per-token amax by a
+//      shared-memory max over the row's blocks, then the blocks are read again from L2), with
+//      the arithmetic of quantize_rows_kernel;
+//  (2) the one-block plan of plan_single_kernel;
+//  (3) the permutation: thread per (routed slot, 16-byte chunk) of the quantised row and
+//      per (slot, 4-scale group) of its scale row, the slot's plan row taken from the plan.
+// Also the zeroed GEMM tile counters and, for an accumulated output, the FP32 copy of out.
+// Data written in one phase is read in the next by other threads of the CTA after a
+// barrier, through L2 (ld.global.cg), never through the read-only path.
+__global__ void __launch_bounds__(kPrologueThreads) small_prologue_kernel(
+    const uint16_t* __restrict__ x, int M, int H, int64_t ld, int per_token, const int32_t* __restrict__ ids,
+    int id_mask, int top_k, int off, int El, int64_t cap, uint8_t* xq, uint8_t* xsf, float* __restrict__ xs,
+    int32_t* __restrict__ counts, int32_t* __restrict__ padded_offsets, int32_t* row_to_slot, int32_t* token_to_row,
+    int32_t* dev_status, uint8_t* __restrict__ aq, uint8_t* __restrict__ asf, int32_t* __restrict__ tile_counters,
+    const uint16_t* __restrict__ acc_init, float* __restrict__ acc) {
+  __shared__ PlanSmem sm;
+  __shared__ unsigned s_amax[kPrologueMaxRows];      // per-row max |x| (bits of a non-negative float)
+  __shared__ int32_t s_row[kPrologueMaxSlots];       // plan row of each slot
+  pdl_trigger();
+  zero_tables(sm, El);
+  for (int i = threadIdx.x; i < M; i += kPrologueThreads) s_amax[i] = 0u;
+  pdl_wait();
+  if (threadIdx.x < 2) tile_counters[threadIdx.x] = 0;
+  const int n = M * top_k;
+  __syncthreads();
+  // (0) histogram of the routed slots per local expert
+  for (int s = threadIdx.x; s < n; s += kPrologueThreads) {
+    const int l = local_of(entry_id(ids, s, id_mask), off, El);
+    if (l >= 0) atomicAdd(&sm.cnt[l], 1);
+  }
+  __syncthreads();
+  // (1) quantise
+  const int nblk = H / kBlock;
+  const int nb_all = M * nblk;
+  if (per_token) {
+    for (int bi = threadIdx.x; bi < nb_all; bi += kPrologueThreads) {
+      const int r = bi / nblk, b = bi - r * nblk;
+      float v[16];
+      load_block16(x + static_cast<int64_t>(r) * ld + b * kBlock, v);
+      float amax = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+      atomicMax(&s_amax[r], __float_as_uint(amax));
+    }
+    __syncthreads();
+  }
+  for (int bi = threadIdx.x; bi < nb_all; bi += kPrologueThreads) {
+    const int r = bi / nblk, b = bi - r * nblk;
+    float g = 1.0f, dec = 1.0f;
+    if (per_token) {
+      const float amax = __uint_as_float(s_amax[r]);
+      if (amax > 0.0f) {
+        g = __fdiv_rn(kGlobalNumerator, amax);
+        dec = __fdiv_rn(amax, kGlobalNumerator);
+      }
+    }
+    float v[16];
+    load_block16(x + static_cast<int64_t>(r) * ld + b * kBlock, v);
+    uint32_t codes[2];
+    const uint32_t q = quantize_block16(v, g, codes);
+    *reinterpret_cast<uint2*>(xq + static_cast<int64_t>(r) * (H / 2) + b * 8) = make_uint2(codes[0], codes[1]);
+    xsf[static_cast<int64_t>(r) * nblk + b] = static_cast<uint8_t>(q);
+    if (b == 0) xs[r] = dec;
+  }
+  // (2) plan (the histogram is already in sm.cnt)
+  __syncthreads();
+  scan_padded(sm, El);
+  __syncthreads();
+  for (int l = threadIdx.x; l <= El; l += kPrologueThreads) {
+    padded_offsets[l] = sm.cursor[l];
+    if (l < El) counts[l] = sm.cnt[l];
+  }
+  // -1 on the segments' padding rows; rows past the padded total are never read by the
+  // GEMMs, so (unlike moe_plan's output) this internal row_to_slot leaves them unwritten
+  fill_padding(sm.cursor, sm.cnt, El, sm.cursor[El], sm.cursor[El], row_to_slot);
+  __syncthreads();
+  place_range(ids, id_mask, 0, n, top_k, off, El, sm, row_to_slot, token_to_row, dev_status);
+  for (int s = threadIdx.x; s < n; s += kPrologueThreads) s_row[s] = __ldcg(token_to_row + s);
+  __syncthreads();
+  // (3) permute the routed slots' rows and scale rows; kCopyBatch loads in flight per thread
+  const int cpr = H / 32;  // 16-byte chunks of a quantised row
+  for (int i0 = 0; i0 < n * cpr; i0 += kPrologueThreads * kCopyBatch) {
+    uint4 v[kCopyBatch];
+    int row[kCopyBatch];
+#pragma unroll
+    for (int u = 0; u < kCopyBatch; ++u) {
+      const int i = i0 + u * kPrologueThreads + threadIdx.x;
+      const int s = i / cpr;
+      row[u] = i < n * cpr ? s_row[s] : -1;
+      if (row[u] >= 0)
+        v[u] = __ldcg(reinterpret_cast<const uint4*>(xq + static_cast<int64_t>(s / top_k) * (H / 2)) + (i - s * cpr));
+    }
+#pragma unroll
+    for (int u = 0; u < kCopyBatch; ++u) {
+      const int i = i0 + u * kPrologueThreads + threadIdx.x;
+      if (row[u] >= 0) reinterpret_cast<uint4*>(aq + static_cast<int64_t>(row[u]) * (H / 2))[i - (i / cpr) * cpr] = v[u];
+    }
+  }
+  const int kcols = H / 16;
+  const int kcols_p = static_cast<int>(roundup64(H, kTileK) / 16);
+  const int gpr = kcols_p / 4;  // 4-scale groups of a scale row, K padding included
+  for (int i0 = 0; i0 < n * gpr; i0 += kPrologueThreads * kCopyBatch) {
+    unsigned v[kCopyBatch];
+    int row[kCopyBatch];
+#pragma unroll
+    for (int u = 0; u < kCopyBatch; ++u) {
+      const int i = i0 + u * kPrologueThreads + threadIdx.x;
+      const int s = i / gpr, c4 = i - s * gpr;
+      row[u] = i < n * gpr ? s_row[s] : -1;
+      v[u] = 0u;
+      if (row[u] >= 0 && c4 < kcols / 4)
+        v[u] = __ldcg(reinterpret_cast<const unsigned*>(xsf + static_cast<int64_t>(s / top_k) * kcols) + c4);
+    }
+#pragma unroll
+    for (int u = 0; u < kCopyBatch; ++u) {
+      const int i = i0 + u * kPrologueThreads + threadIdx.x;
+      if (row[u] >= 0) *reinterpret_cast<unsigned*>(asf + sf_tile_offset(row[u], 4 * (i - (i / gpr) * gpr), kcols_p)) = v[u];
+    }
+  }
+  // accumulated output: acc = fp32(out)
+  if (acc != nullptr) {
+    const int64_t n8 = static_cast<int64_t>(M) * H / 8;
+    for (int64_t i = threadIdx.x; i < n8; i += kPrologueThreads) {
+      const uint4 v = reinterpret_cast<const uint4*>(acc_init)[i];
+      float4* d = reinterpret_cast<float4*>(acc) + 2 * i;
+      d[0] = make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u), __uint_as_float(v.y << 16),
+                         __uint_as_float(v.y & 0xFFFF0000u));
+      d[1] = make_float4(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xFFFF0000u), __uint_as_float(v.w << 16),
+                         __uint_as_float(v.w & 0xFFFF0000u));
+    }
+  }
+}
+
+moe_status_t record_mark(void* ev, cudaStream_t s) {
+  cudaStreamCaptureStatus capturing = cudaStreamCaptureStatusNone;
+  MOE_CUDA(cudaStreamIsCapturing(s, &capturing));
+  if (capturing == cudaStreamCaptureStatusActive)
+    MOE_CUDA(cudaEventRecordWithFlags(static_cast<cudaEvent_t>(ev), s, cudaEventRecordExternal));
+  else
+    MOE_CUDA(cudaEventRecord(static_cast<cudaEvent_t>(ev), s));
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" size_t moe_routed_forward_workspace_bytes(int32_t M, int32_t top_k, const moe_nvfp4_weights_t* w,
+                                                     int32_t do_finalize) {
+  if (check_weights(w) != MOE_OK || M < 0 || top_k < 1) return 0;
+  if (do_finalize < MOE_OUTPUT_UNFINALIZED || do_finalize > MOE_OUTPUT_ACCUMULATE) return 0;
+  return routed_layout(make_dims(w), M, top_k, do_finalize).total;
+}
+
+extern "C" moe_status_t moe_routed_forward(const uint16_t* x, int32_t M, int64_t ld_x, int32_t act_scale_mode,
+                                           const int32_t* topk_ids, int32_t topk_ids_format, int32_t top_k,
+                                           int32_t num_experts, int32_t local_expert_offset, const void* topk_weights,
+                                           int32_t topk_weights_dtype, float routed_scaling_factor,
+                                           const moe_nvfp4_weights_t* w, const void* prepared, size_t prepared_bytes,
+                                           float fc2_input_scale, int32_t do_finalize, uint16_t* out,
+                                           uint16_t* gemm2_out, int32_t* token_to_row, void* workspace,
+                                           size_t workspace_bytes, int32_t* dev_status, void* const* step_events,
+                                           int32_t num_step_events, moe_stream_t stream) {
+  moe_status_t st = check_weights(w);
+  if (st != MOE_OK) return st;
+  MOE_CHECK(M >= 0 && top_k >= 1, MOE_ERR_INVALID_ARGUMENT);
+  MOE_CHECK(do_finalize >= MOE_OUTPUT_UNFINALIZED && do_finalize <= MOE_OUTPUT_ACCUMULATE, MOE_ERR_INVALID_ARGUMENT);
+  MOE_CHECK(act_scale_mode == MOE_SCALE_GLOBAL_ONE || act_scale_mode == MOE_SCALE_PER_TOKEN,
+            MOE_ERR_INVALID_ARGUMENT);
+  MOE_CHECK(topk_ids_format == MOE_IDS_INT32 || topk_ids_format == MOE_IDS_PACKED, MOE_ERR_INVALID_ARGUMENT);
+  MOE_CHECK(topk_weights_dtype >= MOE_WEIGHTS_F32 && topk_weights_dtype <= MOE_WEIGHTS_PACKED,
+            MOE_ERR_INVALID_ARGUMENT);
+  MOE_CHECK(isfinite(routed_scaling_factor) && isfinite(fc2_input_scale) && fc2_input_scale > 0.0f,
+            MOE_ERR_INVALID_ARGUMENT);
+  MOE_CHECK(num_step_events == 0 || (num_step_events == 5 && step_events != nullptr), MOE_ERR_INVALID_ARGUMENT);
+  const Dims d = make_dims(w);
+  MOE_CHECK(num_experts >= 1 && local_expert_offset >= 0 && local_expert_offset + d.El <= num_experts,
+            MOE_ERR_INVALID_ARGUMENT);
+  MOE_CHECK(ld_x >= d.H && ld_x % 8 == 0, MOE_ERR_INVALID_ARGUMENT);
+  MOE_CHECK(static_cast<int64_t>(M) * top_k < (int64_t(1) << 30), MOE_ERR_UNSUPPORTED_SHAPE);
+  MOE_CHECK(prepared != nullptr && prepared_bytes >= prepared_layout(d).total, MOE_ERR_INVALID_ARGUMENT);
+  MOE_CHECK(aligned16(prepared), MOE_ERR_MISALIGNED);
+  const RoutedLayout R = routed_layout(d, M, top_k, do_finalize);
+  MOE_CHECK(workspace_bytes >= R.total, MOE_ERR_WORKSPACE_TOO_SMALL);
+  if (M == 0) return MOE_OK;
+  const bool finalized = do_finalize != MOE_OUTPUT_UNFINALIZED;
+  MOE_CHECK(x && topk_ids && topk_weights && token_to_row && workspace && dev_status, MOE_ERR_INVALID_ARGUMENT);
+  MOE_CHECK(finalized ? out != nullptr : gemm2_out != nullptr, MOE_ERR_INVALID_ARGUMENT);
+  MOE_CHECK(aligned16(x) && aligned16(topk_ids) && aligned16(topk_weights) && aligned16(token_to_row) &&
+                aligned16(workspace) && aligned16(dev_status) && aligned16(finalized ? out : gemm2_out),
+            MOE_ERR_MISALIGNED);
+  const size_t xb = static_cast<size_t>(M - 1) * ld_x * 2 + d.H * 2;
+  const size_t ib = static_cast<size_t>(M) * top_k * 4;
+  const size_t wb = static_cast<size_t>(M) * top_k * (topk_weights_dtype == MOE_WEIGHTS_BF16 ? 2 : 4);
+  const size_t pb = prepared_bytes;
+  // outputs overlap no input and no other output
+  void* const o = finalized ? static_cast<void*>(out) : static_cast<void*>(gemm2_out);
+  const size_t ob = finalized ? static_cast<size_t>(M) * d.H * 2 : static_cast<size_t>(R.cap) * d.H * 2;
+  MOE_CHECK(!overlaps(o, ob, x, xb) && !overlaps(o, ob, topk_ids, ib) && !overlaps(o, ob, topk_weights, wb) &&
+                !overlaps(o, ob, token_to_row, ib) && !overlaps(o, ob, workspace, R.total) &&
+                !overlaps(o, ob, prepared, pb),
+            MOE_ERR_OVERLAP);
+  MOE_CHECK(!overlaps(token_to_row, ib, x, xb) && !overlaps(token_to_row, ib, topk_ids, ib) &&
+                !overlaps(token_to_row, ib, topk_weights, wb) && !overlaps(token_to_row, ib, workspace, R.total) &&
+                !overlaps(token_to_row, ib, prepared, pb),
+            MOE_ERR_OVERLAP);
+  MOE_CHECK(!overlaps(workspace, R.total, x, xb) && !overlaps(workspace, R.total, topk_ids, ib) &&
+                !overlaps(workspace, R.total, topk_weights, wb) && !overlaps(workspace, R.total, prepared, pb),
+            MOE_ERR_OVERLAP);
+
+  cudaStream_t s = as_stream(stream);
+  uint8_t* b = static_cast<uint8_t*>(workspace);
+  uint8_t* xq = b + R.xq;
+  uint8_t* xsf = b + R.xsf;
+  float* xs = reinterpret_cast<float*>(b + R.xs);
+  int32_t* counts = reinterpret_cast<int32_t*>(b + R.counts);
+  int32_t* padded = reinterpret_cast<int32_t*>(b + R.padded);
+  int32_t* r2s = reinterpret_cast<int32_t*>(b + R.r2s);
+  void* fwd = b + R.fwd;
+  // step marks: before the prologue (quantise + plan + permute), GEMM1, GEMM2, the combine,
+  // and at the end; the forward's "before permute" and "before GEMM1" marks share one event
+  void* fwd_events[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
+  if (num_step_events == 5) {
+    if ((st = record_mark(step_events[0], s)) != MOE_OK) return st;
+    fwd_events[0] = step_events[1];
+    for (int i = 1; i < 5; ++i) fwd_events[i] = step_events[i];
+  }
+  const int id_mask = topk_ids_format == MOE_IDS_PACKED ? 0xFFFF : -1;
+  const bool small = small_batch(M, top_k, d.H);
+  if (small) {
+    const WorkspaceLayout L = workspace_layout(d, M, top_k, do_finalize);
+    uint8_t* fb = static_cast<uint8_t*>(fwd);
+    const bool accum = do_finalize == MOE_OUTPUT_ACCUMULATE;
+    st = launch_pdl(small_prologue_kernel, dim3(1), dim3(kPrologueThreads), 0, s, x, static_cast<int>(M),
+                    static_cast<int>(d.H), ld_x, act_scale_mode == MOE_SCALE_PER_TOKEN ? 1 : 0, topk_ids, id_mask,
+                    static_cast<int>(top_k), static_cast<int>(local_expert_offset), static_cast<int>(d.El), R.cap, xq,
+                    xsf, xs, counts, padded, r2s, token_to_row, dev_status, fb + L.aq, fb + L.asf,
+                    reinterpret_cast<int32_t*>(fb + L.sched), accum ? static_cast<const uint16_t*>(out) : nullptr,
+                    accum ? reinterpret_cast<float*>(fb + L.g) : nullptr);
+    if (st != MOE_OK) return st;
+  } else {
+    st = moe_quantize_input(x, M, static_cast<int32_t>(d.H), ld_x, act_scale_mode, xq, xsf, xs, stream);
+    if (st != MOE_OK) return st;
+    st = moe_plan(topk_ids, topk_ids_format, M, top_k, num_experts, local_expert_offset,
+                  static_cast<int32_t>(d.El), counts, padded, r2s, token_to_row, b + R.plan_ws,
+                  moe_plan_workspace_bytes(M, top_k, static_cast<int32_t>(d.El)), dev_status, stream);
+    if (st != MOE_OK) return st;
+  }
+  return forward_chain(padded, r2s, token_to_row, M, top_k, xq, xsf, xs, w, prepared, topk_weights,
+                       topk_weights_dtype, routed_scaling_factor, fc2_input_scale, do_finalize, out, gemm2_out, fwd,
+                       dev_status, num_step_events == 5 ? fwd_events : nullptr, num_step_events, !small, s);
+}

@@ -1,9 +1,10 @@
-"""User-facing wrapper: owns the capacity-sized buffers and chains the C-ABI calls.
+"""User-facing wrapper: owns the capacity-sized buffers and makes the C-ABI calls.
 
-``NVFP4RoutedMoE.forward`` runs moe_quantize_input -> moe_plan ->
-moe_grouped_fp4_forward on torch's current stream; every step runs in the
-library's kernels. torch only allocates device memory (once per batch shape)
-and supplies the stream.
+``NVFP4RoutedMoE.forward`` is one moe_routed_forward call (the whole layer from BF16
+hidden states); ``forward_steps`` makes the separate calls moe_quantize_input ->
+moe_plan -> moe_grouped_fp4_forward and keeps every intermediate buffer. Both run on
+torch's current stream and every step runs in the library's kernels; torch only
+allocates device memory (once per batch shape) and supplies the stream.
 """
 from __future__ import annotations
 
@@ -59,9 +60,31 @@ class NVFP4RoutedMoE:
         """Re-prepare from the (updated) linear weights into the same buffer."""
         L.moe_prepare_weights(self.w, self.prepared)
 
+    def routed_buffers(self, M: int, top_k: int, do_finalize) -> dict:
+        """Buffers of the one-call path for one batch shape (workspace, token_to_row, outputs)."""
+        mode = int(do_finalize)
+        key = ("routed", M, top_k, mode)
+        if key in self._bufs:
+            return self._bufs[key]
+        dev = self.device
+        cap = L.moe_plan_capacity(M, top_k, self.El)
+        b = {
+            "ws": torch.empty(max(L.moe_routed_forward_workspace_bytes(M, top_k, self.w, mode), 16),
+                              dtype=torch.uint8, device=dev),
+            "token_to_row": torch.empty(M, top_k, dtype=torch.int32, device=dev),
+            "dev_status": torch.zeros(4, dtype=torch.int32, device=dev),
+            "out": torch.empty(M, self.H, dtype=torch.bfloat16, device=dev)
+            if mode == L.MOE_OUTPUT_FINALIZED else None,
+            "gemm2_out": torch.empty(max(cap, 1), self.H, dtype=torch.bfloat16, device=dev)
+            if mode == L.MOE_OUTPUT_UNFINALIZED else None,
+            "capacity": cap,
+        }
+        self._bufs[key] = b
+        return b
+
     def buffers(self, M: int, top_k: int, do_finalize) -> dict:
-        """Buffers of one batch shape. do_finalize: False/0 unfinalized rows, True/1 finalized
-        output, 2 accumulated output (the caller's out)."""
+        """Buffers of the separate-call path for one batch shape. do_finalize: False/0
+        unfinalized rows, True/1 finalized output, 2 accumulated output (the caller's out)."""
         mode = int(do_finalize)
         key = (M, top_k, mode)
         if key in self._bufs:
@@ -105,10 +128,53 @@ class NVFP4RoutedMoE:
                                   b["ws"], b["dev_status"], step_events=step_events,
                                   routed_scaling_factor=self.routed_scaling_factor)
 
+    def routed(self, x: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor, b: dict, do_finalize,
+               packed: bool = False, step_events=None, out=None):
+        """One moe_routed_forward call into the buffers ``b`` of routed_buffers()."""
+        L.moe_routed_forward(x.view(torch.int16), self.scale_mode, topk_ids, self.num_experts,
+                             self.local_expert_offset, topk_weights, self.w, self.prepared, self.fc2_input_scale,
+                             int(do_finalize), out if out is not None else b["out"], b["gemm2_out"],
+                             b["token_to_row"], b["ws"], b["dev_status"], step_events=step_events,
+                             routed_scaling_factor=self.routed_scaling_factor, packed=packed)
+
+    @staticmethod
+    def _prefix(x, topk_ids, topk_weights, out, token_capacity):
+        if token_capacity is None:
+            return x, topk_ids, topk_weights, out
+        T = int(token_capacity)
+        if not 0 <= T <= x.shape[0]:
+            raise ValueError("token_capacity must lie in [0, M]")
+        return x[:T], topk_ids[:T], topk_weights[:T], (out[:T] if out is not None else None)
+
     def forward(self, x: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor | None,
                 do_finalize=True, step_events=None, out: torch.Tensor | None = None,
                 token_capacity: int | None = None):
         """x [M, H] bf16, topk_ids [M, k] int32, topk_weights [M, k] f32 or bf16 (all on the GPU).
+
+        One moe_routed_forward call (the small-batch prologue fuses quantiser, plan and
+        permutation). Arguments and results as forward_steps; ``step_events`` (5 recorded
+        events) mark the prologue, GEMM1, GEMM2, the combine and the end.
+        """
+        packed = topk_weights is None
+        if packed:
+            topk_weights = topk_ids
+        mode = int(do_finalize)
+        if mode == L.MOE_OUTPUT_ACCUMULATE and out is None:
+            raise ValueError("do_finalize=2 (accumulate) needs the caller's out tensor")
+        x, topk_ids, topk_weights, out = self._prefix(x, topk_ids, topk_weights, out, token_capacity)
+        M, k = topk_ids.shape
+        b = self.routed_buffers(M, k, mode)
+        self.routed(x, topk_ids, topk_weights, b, mode, packed, step_events, out)
+        if mode == L.MOE_OUTPUT_UNFINALIZED:
+            return b["gemm2_out"], topk_weights, b["token_to_row"]
+        return out if out is not None else b["out"]
+
+    def forward_steps(self, x: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor | None,
+                      do_finalize=True, step_events=None, out: torch.Tensor | None = None,
+                      token_capacity: int | None = None):
+        """The separate calls: moe_quantize_input, moe_plan, moe_grouped_fp4_forward.
+
+        x [M, H] bf16, topk_ids [M, k] int32, topk_weights [M, k] f32 or bf16 (all on the GPU).
 
         topk_weights None: topk_ids holds packed routing slots (int32: BF16 score in bits
         31..16, expert id in bits 15..0) and supplies both the ids and the scores.
@@ -126,13 +192,7 @@ class NVFP4RoutedMoE:
         mode = int(do_finalize)
         if mode == L.MOE_OUTPUT_ACCUMULATE and out is None:
             raise ValueError("do_finalize=2 (accumulate) needs the caller's out tensor")
-        if token_capacity is not None:
-            T = int(token_capacity)
-            if not 0 <= T <= x.shape[0]:
-                raise ValueError("token_capacity must lie in [0, M]")
-            x, topk_ids, topk_weights = x[:T], topk_ids[:T], topk_weights[:T]
-            if out is not None:
-                out = out[:T]
+        x, topk_ids, topk_weights, out = self._prefix(x, topk_ids, topk_weights, out, token_capacity)
         M, k = topk_ids.shape
         b = self.buffers(M, k, mode)
         self.quantize(x, b)
@@ -144,20 +204,20 @@ class NVFP4RoutedMoE:
 
     def capture(self, x: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor | None,
                 do_finalize=True, step_events=None, out: torch.Tensor | None = None) -> torch.cuda.CUDAGraph:
-        """Capture one forward (quantize, plan, permute, GEMM1, GEMM2, finalize) in a CUDA graph.
+        """Capture one forward (the one-call path) in a CUDA graph.
 
         The graph reads x, topk_ids and topk_weights at their current addresses and writes the
         layer's buffers; refill the inputs in place and call ``replay()``. Any routing of the
         same (M, top_k) replays correctly: the kernels size their work from the device-side
-        plan. ``step_events`` (8 recorded torch events, optional) mark the step boundaries
-        inside the graph: before quantize, plan, permute, gemm1, gemm2, finalize, and the end.
+        plan. ``step_events`` (5 recorded torch events, optional) mark the step boundaries
+        inside the graph: before the prologue, GEMM1, GEMM2, the combine, and the end.
         """
         M, k = topk_ids.shape
         mode = int(do_finalize)
         packed = topk_weights is None
         if packed:
             topk_weights = topk_ids
-        b = self.buffers(M, k, mode)
+        b = self.routed_buffers(M, k, mode)
         if mode == L.MOE_OUTPUT_ACCUMULATE and out is None:
             raise ValueError("do_finalize=2 (accumulate) needs the caller's out tensor")
         # warm-up outside the capture (an accumulating warm-up writes a copy of out)
@@ -169,16 +229,9 @@ class NVFP4RoutedMoE:
         torch.cuda.current_stream().wait_stream(side)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            if step_events:
-                step_events[0].record()
-            self.quantize(x, b)
-            if step_events:
-                step_events[1].record()
-            self.plan(topk_ids, b, packed)
-            self.experts(topk_weights, b, mode, step_events[2:7] if step_events else None, out)
-            if step_events:
-                step_events[7].record()
+            self.routed(x, topk_ids, topk_weights, b, mode, packed, step_events, out)
         return g
 
-    def device_status(self, M: int, top_k: int, do_finalize) -> int:
-        return int(self.buffers(M, top_k, do_finalize)["dev_status"][0].item())
+    def device_status(self, M: int, top_k: int, do_finalize, routed: bool = True) -> int:
+        b = self.routed_buffers(M, top_k, do_finalize) if routed else self.buffers(M, top_k, do_finalize)
+        return int(b["dev_status"][0].item())

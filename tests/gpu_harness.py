@@ -85,6 +85,13 @@ class Problem:
                                         w1_gate_alpha=None if gate_factor is None else self.gate_alpha_t)
 
     def run(self, do_finalize=True):
+        """The separate calls (quantize, plan, forward): every intermediate stays in bufs()."""
+        res = self.layer.forward_steps(self.x, self.ids_t, self.tw_t, do_finalize=do_finalize)
+        torch.cuda.synchronize()
+        return res
+
+    def run_routed(self, do_finalize=True):
+        """The one-call path (moe_routed_forward), as the benchmark times it."""
         res = self.layer.forward(self.x, self.ids_t, self.tw_t, do_finalize=do_finalize)
         torch.cuda.synchronize()
         return res

@@ -148,6 +148,31 @@ def test_forward_validation(lib):
 
 
 @host_only
+def test_routed_forward_validation(lib):
+    w = _w()
+    f = lib.moe_routed_forward
+    pb = pkg.moe_prepared_weights_bytes(w)
+    ws = pkg.moe_routed_forward_workspace_bytes(4, 2, w, 1)
+    assert ws > pkg.moe_forward_workspace_bytes(4, 2, w, 1)
+    assert pkg.moe_routed_forward_workspace_bytes(4, 2, w, 5) == 0
+
+    def call(x=1 << 20, ld=128, mode=1, ids=2 << 20, fmt=0, E=4, off=0, wt=3 << 20, dt=0, g2=1.0, fin=1,
+             out=4 << 20, t2r=5 << 20, wsp=1 << 36, wsb=ws, nev=0):
+        return f(x, 4, ld, mode, ids, fmt, 2, E, off, wt, dt, 1.0, ctypes.byref(w), 6 << 20, pb, g2, fin, out, None,
+                 t2r, wsp, wsb, 7 << 20, None, nev, None)
+    assert call(ld=120) == 1                 # ld_x < H
+    assert call(mode=3) == 1                 # bad activation-scale mode
+    assert call(fmt=4) == 1                  # bad id format
+    assert call(E=3) == 1                    # local range past the expert count
+    assert call(g2=0.0) == 1                 # fc2_input_scale must be positive
+    assert call(nev=2) == 1                  # step events: 0 or 5
+    assert call(wsb=ws - 1) == 4             # workspace too small
+    assert call(x=(1 << 20) + 8) == 3        # misaligned hidden states
+    assert call(out=1 << 20) == 6            # out overlaps the hidden states
+    assert call(t2r=(4 << 20) + 64) == 6     # token_to_row overlaps out
+
+
+@host_only
 def test_finalize_validation(lib):
     f = lib.moe_finalize
     assert f(16, 32, 0, 1.0, 48, 4, 2, 100, 64, None) == 2         # H % 128

@@ -32,7 +32,11 @@ def _sample_tokens(cfg, ids, n):
 def test_full_size_sampled(name, ntok):
     cfg = mi.CONFIGS[name]
     p = Problem(cfg)
-    out = bf16_np(p.run(True))
+    # the benchmark's path: one moe_routed_forward call; it equals the separate calls (whose
+    # intermediates are checked below) bit for bit
+    out = bf16_np(p.run_routed(True)).copy()
+    assert p.layer.device_status(cfg.M, cfg.top_k, True) == 0
+    assert np.array_equal(bf16_np(p.run(True)), out)
     b = p.bufs(True)
     assert int(to_np(b["dev_status"])[0]) == 0
     # plan, bit-exact over the whole batch

@@ -201,7 +201,7 @@ def test_cuda_graph_replay_with_new_routing():
     tw.copy_(torch.from_numpy(tw2))
     g.replay()
     torch.cuda.synchronize()
-    got = bf16_np(p.bufs(True)["out"]).copy()
+    got = bf16_np(p.layer.routed_buffers(cfg.M, cfg.top_k, True)["out"]).copy()
     ref = bf16_np(p.layer.forward(x.clone(), ids.clone(), tw.clone()))
     torch.cuda.synchronize()
     assert np.array_equal(got, ref)

@@ -1,0 +1,103 @@
+"""The one-call path (moe_routed_forward, the small-batch fused prologue and the large-batch
+chain of separate kernels) against the separate calls, bit for bit, and against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+from gpu_harness import DEV, Problem, assert_close_output, bf16_np, mi, pkg, to_np
+
+pytestmark = pytest.mark.gpu
+
+CASES = {
+    # fused prologue (M * top_k <= 2048 and M * H <= 2^17)
+    "tiny": mi.CONFIGS["tiny"],
+    "decode_t8": mi.CONFIGS["decode_t8"],
+    "decode_ep": mi.MoEConfig("decode_ep", M=12, H=1024, I=256, E=32, top_k=6, seed=31, weight_seed=31,
+                              local_offset=8, num_local=16),
+    "relu2_small": mi.MoEConfig("relu2_small", M=64, H=512, I=384, E=12, top_k=3, act="relu2", seed=32,
+                                weight_seed=32, local_offset=4, num_local=6),
+    "geglu_small": mi.MoEConfig("geglu_small", M=40, H=768, I=256, E=16, top_k=4, act="geglu", seed=33,
+                                weight_seed=33),
+    # separate kernels (too large for the prologue)
+    "swiglu_ragged": mi.MoEConfig("swiglu_ragged", M=300, H=512, I=256, E=8, top_k=2, seed=11, weight_seed=11),
+}
+
+
+def _unrouted(cfg):
+    ids, tw = mi.routing(cfg)
+    ids = mi.with_unrouted(ids, 0.15, 7, cfg.E)
+    tw = tw.copy()
+    tw[(ids < 0) | (ids >= cfg.E)] = np.nan
+    return ids, tw
+
+
+@pytest.mark.parametrize("name", list(CASES))
+@pytest.mark.parametrize("do_finalize", [True, False])
+def test_routed_equals_separate_calls(name, do_finalize):
+    cfg = CASES[name]
+    ids, tw = _unrouted(cfg) if name in ("decode_ep", "relu2_small") else (None, None)
+    p = Problem(cfg, ids, tw)
+    if do_finalize:
+        a = bf16_np(p.run_routed(True)).copy()
+        b = bf16_np(p.run(True))
+        assert np.array_equal(a, b)
+        assert_close_output(a, p.oracle_forward()["out"], name)
+    else:
+        g2, tw_r, t2r = p.run_routed(False)
+        g2 = bf16_np(g2).copy()
+        t2r = to_np(t2r).copy()
+        g2s, _, t2rs = p.run(False)
+        assert np.array_equal(t2r, to_np(t2rs))
+        real = t2r[t2r >= 0]
+        assert np.array_equal(g2[real], bf16_np(g2s)[real])
+        assert tw_r.data_ptr() == p.tw_t.data_ptr()
+    assert p.layer.device_status(cfg.M, cfg.top_k, do_finalize) == 0
+
+
+def test_routed_row_stride_and_packed_routing():
+    cfg = CASES["decode_ep"]
+    p = Problem(cfg)
+    wide = torch.zeros(cfg.M, cfg.H + 64, dtype=torch.bfloat16, device=DEV)
+    wide[:, :cfg.H] = p.x
+    x = wide[:, :cfg.H]                                   # ld_x = H + 64
+    a = bf16_np(p.layer.forward(x, p.ids_t, p.tw_t)).copy()
+    assert np.array_equal(a, bf16_np(p.run(True)))
+    hi = p.tw_t.to(torch.bfloat16).view(torch.int16).to(torch.int32) & 0xFFFF
+    packed = ((hi << 16) | (p.ids_t & 0xFFFF)).contiguous()
+    b = bf16_np(p.layer.forward(p.x, packed, None)).copy()
+    c = bf16_np(p.layer.forward(p.x, p.ids_t, p.tw_t.to(torch.bfloat16)))
+    assert np.array_equal(b, c)
+
+
+@pytest.mark.parametrize("name", ["decode_t8", "swiglu_ragged"])
+def test_routed_accumulate(name):
+    cfg = CASES[name].with_(routed_scaling_factor=0.5)
+    p = Problem(cfg)
+    rng = np.random.default_rng(2)
+    prev = torch.from_numpy(rng.standard_normal((cfg.M, cfg.H)).astype(np.float32) * 0.01).to(torch.bfloat16).to(DEV)
+    out = prev.clone()
+    p.layer.forward(p.x, p.ids_t, p.tw_t, do_finalize=2, out=out)
+    torch.cuda.synchronize()
+    ref = p.oracle_forward(out_prev=bf16_np(prev))["out_acc"]
+    assert_close_output(bf16_np(out), ref, "routed accumulate")
+
+
+def test_routed_graph_replay_new_routing_small_batch():
+    cfg = CASES["decode_t8"]
+    p = Problem(cfg)
+    x, ids, tw = p.x.clone(), p.ids_t.clone(), p.tw_t.clone()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    for e in evs:
+        e.record()
+    g = p.layer.capture(x, ids, tw, True, step_events=evs)
+    cfg2 = cfg.with_(seed=77)
+    ids2, tw2 = mi.routing(cfg2)
+    x.copy_(mi.hidden_bf16(cfg2, DEV))
+    ids.copy_(torch.from_numpy(ids2))
+    tw.copy_(torch.from_numpy(tw2))
+    g.replay()
+    torch.cuda.synchronize()
+    got = bf16_np(p.layer.routed_buffers(cfg.M, cfg.top_k, True)["out"]).copy()
+    assert all(evs[i].elapsed_time(evs[i + 1]) >= 0 for i in range(4))
+    p2 = Problem(cfg2)
+    assert np.array_equal(got, bf16_np(p2.run(True)))
