@@ -258,7 +258,13 @@ def run_gpu(args, cfg, rank, world):
         ms = float(tt.item())
     work, stepw, R, active = kernel_work(cfg, ids)
     kern_ms = {n: float(np.mean(v)) for n, v in per.items()}
-    dom = max(["gemm1", "gemm2"], key=lambda n: kern_ms[n])
+    if M * k <= 2048:
+        # GEMM1 and GEMM2 run as one chained launch (its time is the gemm1 interval)
+        kern_ms["gemm1+gemm2 (chained)"] = kern_ms.pop("gemm1") + kern_ms.pop("gemm2")
+        work["gemm1+gemm2 (chained)"] = {key: work["gemm1"][key] + work["gemm2"][key] for key in ("bytes", "flops")}
+        dom = "gemm1+gemm2 (chained)"
+    else:
+        dom = max(["gemm1", "gemm2"], key=lambda n: kern_ms[n])
     peaks = load_peaks()
     fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
     t_dom = kern_ms[dom] * 1e-3
@@ -279,7 +285,7 @@ def run_gpu(args, cfg, rank, world):
     # end to end through the public API with host buffers
     e2e = None if args.no_e2e else run_e2e(layer, x, ids, tw, dev, max(3, min(K, 50)))
     small = M * k <= 2048 and M * cfg.H <= (1 << 17)
-    launches_per_step = 4 if small else 6 + (2 if M * k > 2048 else 0)
+    launches_per_step = (3 if small else 5) + (2 if M * k > 2048 else 0) + (0 if M * k <= 2048 else 1)
     res = {
         "metric": METRIC, "value": world * M / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,

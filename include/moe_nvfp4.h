@@ -262,8 +262,13 @@ MOE_API moe_status_t moe_prepare_weights(const moe_nvfp4_weights_t* w, void* pre
  *                      their value; gemm2_out may be NULL
  *   workspace          moe_forward_workspace_bytes(...) bytes of device scratch
  *   step_events        optional array of `num_step_events` (0 or 5) cudaEvent_t recorded on
- *                      `stream` before permute, gemm1, gemm2, finalize and at the end
+ *                      `stream` before permute, gemm1, gemm2, finalize and at the end; batches
+ *                      of at most MOE_CHAIN_MAX_SLOTS routed slots run GEMM1 and GEMM2 as one
+ *                      chained launch, whose time falls between the gemm1 and gemm2 marks
  * ---------------------------------------------------------------------------------------- */
+/* M * top_k at or below which GEMM1 and GEMM2 run as one chained launch (the GEMM2 tiles of
+ * a 128-row tile start as soon as its GEMM1 tiles are written). */
+#define MOE_CHAIN_MAX_SLOTS 2048
 MOE_API size_t moe_forward_workspace_bytes(int32_t M, int32_t top_k, const moe_nvfp4_weights_t* w,
                                    int32_t do_finalize);
 /* Byte offsets inside the forward workspace of: [0] permuted activations [cap, H/2],

@@ -33,6 +33,7 @@ namespace {
 
 struct Bufs {
   int32_t* sched;
+  int32_t* mtd;
   uint8_t *aq, *asf, *iq, *isf;
   uint16_t* g;
 };
@@ -41,6 +42,7 @@ Bufs carve(void* ws, const WorkspaceLayout& L) {
   uint8_t* b = static_cast<uint8_t*>(ws);
   Bufs r;
   r.sched = reinterpret_cast<int32_t*>(b + L.sched);
+  r.mtd = reinterpret_cast<int32_t*>(b + L.mtd);
   r.aq = b + L.aq;
   r.asf = b + L.asf;
   r.iq = b + L.iq;
@@ -224,15 +226,19 @@ moe_status_t forward_chain(const int32_t* padded_offsets, const int32_t* row_to_
   if ((st = mark(0)) != MOE_OK) return st;
   if (run_permute)
     st = launch_permute(padded_offsets, static_cast<int>(d.El), row_to_slot, top_k, L.cap, xq, xsf,
-                        static_cast<int>(d.H), b.aq, b.asf, b.sched, accum ? out : nullptr, acc,
-                        accum ? static_cast<int64_t>(M) * d.H : 0, s);
+                        static_cast<int>(d.H), b.aq, b.asf, b.sched, b.mtd, L.cap / kTileM, accum ? out : nullptr,
+                        acc, accum ? static_cast<int64_t>(M) * d.H : 0, s);
   if (st != MOE_OK) return st;
   if ((st = mark(1)) != MOE_OK) return st;
   GemmLaunch g1 = gemm1_launch(d, L, b, pw, padded_offsets, row_to_slot, xs, top_k, dev_status);
   g1.g2 = fc2_input_scale;
-  st = launch_gemm(g1, s);
-  if (st != MOE_OK) return st;
-  if ((st = mark(2)) != MOE_OK) return st;
+  // small batches: GEMM1 and GEMM2 in one chained launch (the GEMM2 mark then follows it)
+  const bool chained = static_cast<int64_t>(M) * top_k <= kChainMaxSlots;
+  if (!chained) {
+    st = launch_gemm(g1, s);
+    if (st != MOE_OK) return st;
+    if ((st = mark(2)) != MOE_OK) return st;
+  }
   GemmLaunch g2;
   g2.mode = accum ? kG2Reduce : kG2Rows;
   g2.a = b.iq;
@@ -262,8 +268,14 @@ moe_status_t forward_chain(const int32_t* padded_offsets, const int32_t* row_to_
   g2.rsf = routed_scaling_factor;
   g2.dev_status = dev_status;
   g2.tile_counter = b.sched + 1;
-  st = launch_gemm(g2, s);
-  if (st != MOE_OK) return st;
+  if (chained) {
+    st = launch_gemm_chain(g1, g2, b.mtd, s);
+    if (st != MOE_OK) return st;
+    if ((st = mark(2)) != MOE_OK) return st;
+  } else {
+    st = launch_gemm(g2, s);
+    if (st != MOE_OK) return st;
+  }
   if ((st = mark(3)) != MOE_OK) return st;
   if (fin) {
     st = launch_finalize(rows_out, topk_weights, topk_weights_dtype, routed_scaling_factor, token_to_row, M, top_k,
@@ -351,7 +363,7 @@ extern "C" moe_status_t moe_debug_gemm1(const int32_t* padded_offsets, const int
   const Bufs b = carve(workspace, L);
   const Prepared pw = prepared_ptrs(prepared, prepared_layout(d));
   st = launch_permute(padded_offsets, static_cast<int>(d.El), row_to_slot, top_k, L.cap, xq, xsf,
-                      static_cast<int>(d.H), b.aq, b.asf, b.sched, nullptr, nullptr, 0, s);
+                      static_cast<int>(d.H), b.aq, b.asf, b.sched, b.mtd, L.cap / kTileM, nullptr, nullptr, 0, s);
   if (st != MOE_OK) return st;
   GemmLaunch g1 = gemm1_launch(d, L, b, pw, padded_offsets, row_to_slot, xs, top_k, dev_status);
   g1.mode = mode == 0 ? kG1Preact : kG1Act;

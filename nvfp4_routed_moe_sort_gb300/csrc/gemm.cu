@@ -69,53 +69,91 @@ bool encode_rows(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t 
 
 }  // namespace
 
-moe_status_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
-  if (g.cap == 0) return MOE_OK;
-  GemmParams prm;
-  memset(&prm, 0, sizeof(prm));
-  if (!encode_rows(&prm.tmap_a, g.a, g.K / 2, g.cap, kTileM)) return MOE_ERR_CUDA;
-  if (!encode_rows(&prm.tmap_a32, g.a, g.K / 2, g.cap, 32)) return MOE_ERR_CUDA;
-  if (!encode_rows(&prm.tmap_b, g.b, g.K / 2, g.El * g.Np, kTileN)) return MOE_ERR_CUDA;
-  prm.sfa = g.a_sf;
-  prm.sfb = g.b_sf;
+namespace {
+
+bool fill_phase(Phase& ph, const GemmLaunch& g) {
+  if (!encode_rows(&ph.tmap_a, g.a, g.K / 2, g.cap, kTileM)) return false;
+  if (!encode_rows(&ph.tmap_a32, g.a, g.K / 2, g.cap, 32)) return false;
+  if (!encode_rows(&ph.tmap_b, g.b, g.K / 2, g.El * g.Np, kTileN)) return false;
+  ph.b_raw = g.b;
+  ph.sfa = g.a_sf;
+  ph.sfb = g.b_sf;
+  ph.alpha = g.alpha;
+  ph.alpha_gate = g.alpha_gate;
+  ph.out = g.out;
+  ph.out_sf = g.out_sf;
+  ph.K = static_cast<int32_t>(g.K);
+  ph.Kp = static_cast<int32_t>(g.Kp);
+  ph.nkb = static_cast<int32_t>(g.Kp / kTileK);
+  ph.N = static_cast<int32_t>(g.N);
+  ph.Np = static_cast<int32_t>(g.Np);
+  ph.n_tiles = static_cast<int32_t>(g.Np / kTileN);
+  return true;
+}
+
+void fill_common(GemmParams& prm, const GemmLaunch& g) {
   prm.padded_offsets = g.padded_offsets;
   prm.row_to_slot = g.row_to_slot;
   prm.xs = g.xs;
-  prm.alpha = g.alpha;
-  prm.alpha_gate = g.alpha_gate;
-  prm.route_w = g.route_w;
-  prm.route_w_dtype = g.route_w_dtype;
-  prm.rsf = g.rsf;
-  prm.out = g.out;
-  prm.out_sf = g.out_sf;
   prm.dev_status = g.dev_status;
   prm.tile_counter = g.tile_counter;
   prm.El = static_cast<int32_t>(g.El);
-  prm.Kp = static_cast<int32_t>(g.Kp);
-  prm.nkb = static_cast<int32_t>(g.Kp / kTileK);
-  prm.N = static_cast<int32_t>(g.N);
-  prm.Np = static_cast<int32_t>(g.Np);
-  prm.n_tiles = static_cast<int32_t>(g.Np / kTileN);
   prm.top_k = g.top_k;
   prm.inter = g.inter;
   prm.gated = g.gated ? 1 : 0;
   prm.act = g.act;
   prm.g2 = g.g2;
-  const int64_t units_max = (g.cap / kTileM) * prm.n_tiles;
-  prm.sparse = (g.mode == kG1Fused || g.mode == kG2Rows || g.mode == kG2Reduce) && g.El <= kSparseMaxExperts;
-  const size_t smem = static_cast<size_t>(kStages) * kStageBytes + kSmemExtra + roundup64((g.El + 1) * 4, 16) +
-                      (prm.sparse ? kSparseStageBytes : 0);
-  if (g.mode == kG2Rows || g.mode == kG2Reduce) return gemm::launch_rows(g.mode, prm, units_max, smem, s);
-  switch (g.act) {
+  prm.route_w = g.route_w;
+  prm.route_w_dtype = g.route_w_dtype;
+  prm.rsf = g.rsf;
+}
+
+size_t smem_bytes(int64_t El, bool sparse) {
+  return static_cast<size_t>(kStages) * kStageBytes + kSmemExtra + roundup64((El + 1) * 4, 16) +
+         (sparse ? kSparseStageBytes : 0);
+}
+
+moe_status_t dispatch(int mode, int act, const GemmParams& prm, int64_t units_max, size_t smem, cudaStream_t s) {
+  if (mode == kG2Rows || mode == kG2Reduce) return gemm::launch_rows(mode, prm, units_max, smem, s);
+  switch (act) {
     case MOE_ACT_SWIGLU:
-    case MOE_ACT_GEGLU: return gemm::launch_gated(g.mode, g.act, prm, units_max, smem, s);
+    case MOE_ACT_GEGLU: return gemm::launch_gated(mode, act, prm, units_max, smem, s);
     case MOE_ACT_RELU2:
     case MOE_ACT_GELU:
-    case MOE_ACT_RELU: return gemm::launch_plain_a(g.mode, g.act, prm, units_max, smem, s);
+    case MOE_ACT_RELU: return gemm::launch_plain_a(mode, act, prm, units_max, smem, s);
     case MOE_ACT_SILU:
-    case MOE_ACT_IDENTITY: return gemm::launch_plain_b(g.mode, g.act, prm, units_max, smem, s);
+    case MOE_ACT_IDENTITY: return gemm::launch_plain_b(mode, act, prm, units_max, smem, s);
     default: return MOE_ERR_INVALID_ARGUMENT;
   }
+}
+
+}  // namespace
+
+moe_status_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
+  if (g.cap == 0) return MOE_OK;
+  GemmParams prm;
+  memset(&prm, 0, sizeof(prm));
+  if (!fill_phase(prm.ph[0], g)) return MOE_ERR_CUDA;
+  fill_common(prm, g);
+  prm.sparse = (g.mode == kG1Fused || g.mode == kG2Rows || g.mode == kG2Reduce) && g.El <= kSparseMaxExperts;
+  const int64_t units_max = (g.cap / kTileM) * prm.ph[0].n_tiles;
+  return dispatch(g.mode, g.act, prm, units_max, smem_bytes(g.El, prm.sparse), s);
+}
+
+moe_status_t launch_gemm_chain(const GemmLaunch& g1, const GemmLaunch& g2, int32_t* mt_done, cudaStream_t s) {
+  if (g1.cap == 0) return MOE_OK;
+  GemmParams prm;
+  memset(&prm, 0, sizeof(prm));
+  if (!fill_phase(prm.ph[0], g1) || !fill_phase(prm.ph[1], g2)) return MOE_ERR_CUDA;
+  fill_common(prm, g1);
+  prm.route_w = g2.route_w;  // the combine scalars are GEMM2's
+  prm.route_w_dtype = g2.route_w_dtype;
+  prm.rsf = g2.rsf;
+  prm.mt_done = mt_done;
+  prm.sparse = g1.El <= kSparseMaxExperts;
+  const int mode = g2.mode == kG2Reduce ? kChainReduce : kChainRows;
+  const int64_t units_max = (g1.cap / kTileM) * (prm.ph[0].n_tiles + prm.ph[1].n_tiles);
+  return dispatch(mode, g1.act, prm, units_max, smem_bytes(g1.El, prm.sparse), s);
 }
 
 }  // namespace moe

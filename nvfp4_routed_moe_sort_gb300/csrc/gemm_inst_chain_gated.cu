@@ -1,0 +1,22 @@
+// Instantiations of the grouped GEMM kernel: GEMM1 and GEMM2 chained in one launch, with the
+// SWIGLU, GEGLU activations.
+#include "gemm_kernel.cuh"
+
+namespace moe {
+namespace gemm {
+
+moe_status_t launch_chain_gated(int mode, int act, const GemmParams& prm, int64_t units_max, size_t smem,
+                              cudaStream_t s) {
+  switch (act) {
+    case MOE_ACT_SWIGLU:
+      return mode == kChainReduce ? launch_kernel<kChainReduce, MOE_ACT_SWIGLU>(prm, units_max, smem, s)
+                                  : launch_kernel<kChainRows, MOE_ACT_SWIGLU>(prm, units_max, smem, s);
+    case MOE_ACT_GEGLU:
+      return mode == kChainReduce ? launch_kernel<kChainReduce, MOE_ACT_GEGLU>(prm, units_max, smem, s)
+                                  : launch_kernel<kChainRows, MOE_ACT_GEGLU>(prm, units_max, smem, s);
+    default: return MOE_ERR_INVALID_ARGUMENT;
+  }
+}
+
+}  // namespace gemm
+}  // namespace moe

@@ -5,6 +5,7 @@ namespace moe {
 namespace gemm {
 
 moe_status_t launch_gated(int mode, int act, const GemmParams& prm, int64_t units_max, size_t smem, cudaStream_t s) {
+  if (is_chain(mode)) return launch_chain_gated(mode, act, prm, units_max, smem, s);
   switch (act) {
     case MOE_ACT_SWIGLU:
       if (mode == kG1Fused) return launch_kernel<kG1Fused, MOE_ACT_SWIGLU>(prm, units_max, smem, s);

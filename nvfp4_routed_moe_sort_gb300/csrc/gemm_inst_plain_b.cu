@@ -5,6 +5,7 @@ namespace moe {
 namespace gemm {
 
 moe_status_t launch_plain_b(int mode, int act, const GemmParams& prm, int64_t units_max, size_t smem, cudaStream_t s) {
+  if (is_chain(mode)) return launch_chain_plain_b(mode, act, prm, units_max, smem, s);
   switch (act) {
     case MOE_ACT_SILU:
       if (mode == kG1Fused) return launch_kernel<kG1Fused, MOE_ACT_SILU>(prm, units_max, smem, s);

@@ -41,22 +41,30 @@ constexpr int kRingConsumers = 1 + kEpiThreads / 32;  // MMA thread + one lane p
 static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
 static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
 
-struct GemmParams {
+// One GEMM of the launch: operands, scales, per-expert scalars and output.
+struct Phase {
   CUtensorMap tmap_a;     // 128-row activation boxes
   CUtensorMap tmap_a32;   // 32-row boxes, for tiles whose real rows all lie in the first 32
   CUtensorMap tmap_b;
+  const uint8_t* b_raw;   // the weight rows behind tmap_b (K/2 bytes each), for the L2 prefetch
   const uint8_t* sfa;
   const uint8_t* sfb;
-  const int32_t* padded_offsets;
-  const int32_t* row_to_slot;
-  const float* xs;
   const float* alpha;
   const float* alpha_gate;  // gate rows of a gated GEMM1
   void* out;
   uint8_t* out_sf;
+  int32_t K, Kp, nkb, N, Np, n_tiles;
+};
+
+struct GemmParams {
+  Phase ph[2];            // [1] only in the chained modes (GEMM2 after GEMM1 in one launch)
+  const int32_t* padded_offsets;
+  const int32_t* row_to_slot;
+  const float* xs;
   int32_t* dev_status;
   int32_t* tile_counter;  // zeroed before the launch (by the permute kernel)
-  int32_t El, Kp, nkb, N, Np, n_tiles, top_k, inter, gated, act;
+  int32_t* mt_done;       // chained modes: per 128-row tile, GEMM1 epilogue warps done (zeroed too)
+  int32_t El, top_k, inter, gated, act;
   float g2;
   const void* route_w;  // kG2Reduce: route weights, their storage and the routed scaling factor
   int32_t route_w_dtype;
@@ -65,6 +73,10 @@ struct GemmParams {
 };
 
 __host__ __device__ constexpr bool is_g2(int mode) { return mode == kG2Rows || mode == kG2Reduce; }
+__host__ __device__ constexpr bool is_chain(int mode) { return mode == kChainRows || mode == kChainReduce; }
+// epilogue of the first / second GEMM of a launch in `mode`
+__host__ __device__ constexpr int first_epilogue(int mode) { return is_chain(mode) ? kG1Fused : mode; }
+__host__ __device__ constexpr int second_epilogue(int mode) { return mode == kChainReduce ? kG2Reduce : kG2Rows; }
 
 __device__ __forceinline__ void red_add_f32(float* out, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(out), "f"(v) : "memory");
@@ -155,15 +167,16 @@ __device__ __forceinline__ void store_bf16x32(uint16_t* dst, const float* v) {
 }
 
 template <int MODE, int ACT>
-__device__ __forceinline__ void epilogue_compute(const GemmParams& p, uint32_t* r, int half, int e, int nt,
+__device__ __forceinline__ void epilogue_compute(const GemmParams& p, const Phase& ph, uint32_t* r, int half,
+                                                 int e, int nt,
                                                  int64_t prow, int slot, float xs_t) {
   constexpr bool kGated = is_gated(ACT);
   const bool real = slot >= 0;
   if constexpr (MODE == kG2Rows) {
-    const float d2 = __fmul_rn(p.alpha[e], __fdiv_rn(1.0f, p.g2));
+    const float d2 = __fmul_rn(ph.alpha[e], __fdiv_rn(1.0f, p.g2));
     const int col0 = nt * kTileN + half * 128;
-    if (!real || col0 >= p.N) return;
-    uint16_t* orow = static_cast<uint16_t*>(p.out) + prow * p.N + col0;
+    if (!real || col0 >= ph.N) return;
+    uint16_t* orow = static_cast<uint16_t*>(ph.out) + prow * ph.N + col0;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       float v[32];
@@ -173,11 +186,11 @@ __device__ __forceinline__ void epilogue_compute(const GemmParams& p, uint32_t* 
     }
   } else if constexpr (MODE == kG2Reduce) {
     // acc[t, :] += (y2 * w') for this row's token t, w' = fp32(w * rsf)
-    const float d2 = __fmul_rn(p.alpha[e], __fdiv_rn(1.0f, p.g2));
+    const float d2 = __fmul_rn(ph.alpha[e], __fdiv_rn(1.0f, p.g2));
     const int col0 = nt * kTileN + half * 128;
-    if (!real || col0 >= p.N) return;
+    if (!real || col0 >= ph.N) return;
     const float w = route_weight(p.route_w, p.route_w_dtype, slot, p.rsf);
-    float* orow = static_cast<float*>(p.out) + static_cast<int64_t>(slot / p.top_k) * p.N + col0;
+    float* orow = static_cast<float*>(ph.out) + static_cast<int64_t>(slot / p.top_k) * ph.N + col0;
 #pragma unroll
     for (int c = 0; c < 32; ++c) {
       float v[4];
@@ -187,8 +200,8 @@ __device__ __forceinline__ void epilogue_compute(const GemmParams& p, uint32_t* 
     }
   } else {
     if (!real) return;
-    const float a1 = p.alpha[e];
-    const float a1g = kGated ? p.alpha_gate[e] : a1;  // gate rows' scalar
+    const float a1 = ph.alpha[e];
+    const float a1g = kGated ? ph.alpha_gate[e] : a1;  // gate rows' scalar
     const int I = p.inter;
     const int ip16 = static_cast<int>(roundup64(I, kTileK) / 16);  // scale columns of the intermediate
     // intermediate columns [i0, i0 + nout) come from this thread's registers
@@ -197,7 +210,7 @@ __device__ __forceinline__ void epilogue_compute(const GemmParams& p, uint32_t* 
     if (i0 >= I) return;
     if constexpr (MODE == kG1Preact) {
       const int ld = kGated ? 2 * I : I;
-      float* o = static_cast<float*>(p.out) + prow * ld;
+      float* o = static_cast<float*>(ph.out) + prow * ld;
 #pragma unroll
       for (int i = 0; i < 128; ++i) {
         const float y = __fmul_rn(__fmul_rn(__uint_as_float(r[i]), xs_t), i < nout ? a1g : a1);
@@ -238,13 +251,13 @@ __device__ __forceinline__ void epilogue_compute(const GemmParams& p, uint32_t* 
 #undef MOE_YG
       const int ic = i0 + 32 * c;
       if constexpr (MODE == kG1Act) {
-        store_bf16x32(static_cast<uint16_t*>(p.out) + prow * I + ic, h);
+        store_bf16x32(static_cast<uint16_t*>(ph.out) + prow * I + ic, h);
       } else {
-        uint8_t* dst = static_cast<uint8_t*>(p.out) + prow * (I / 2) + ic / 2;
+        uint8_t* dst = static_cast<uint8_t*>(ph.out) + prow * (I / 2) + ic / 2;
         const uint32_t q2 = requant32_store(h, p.g2, dst);
         // two 32-value chunks make one 4-scale group of the 128x4 tile layout
         if (c & 1) {
-          *reinterpret_cast<uint32_t*>(p.out_sf + sf_tile_offset(prow, (ic >> 4) - 2, ip16)) = sfw | (q2 << 16);
+          *reinterpret_cast<uint32_t*>(ph.out_sf + sf_tile_offset(prow, (ic >> 4) - 2, ip16)) = sfw | (q2 << 16);
         } else {
           sfw = q2;
         }
@@ -252,9 +265,9 @@ __device__ __forceinline__ void epilogue_compute(const GemmParams& p, uint32_t* 
     }
     if constexpr (MODE == kG1Fused) {
       // zero the scale columns of the K padding once per row (last column tile, first half)
-      if (nt == p.n_tiles - 1 && half == 0) {
+      if (nt == ph.n_tiles - 1 && half == 0) {
         for (int c4 = I / 64; c4 < ip16 / 4; ++c4)
-          *reinterpret_cast<uint32_t*>(p.out_sf + sf_tile_offset(prow, 4 * c4, ip16)) = 0u;
+          *reinterpret_cast<uint32_t*>(ph.out_sf + sf_tile_offset(prow, 4 * c4, ip16)) = 0u;
       }
     }
   }
@@ -274,6 +287,77 @@ __device__ __forceinline__ float activation_f32(float yg, float yu) {
   else return yg;
 }
 
+// The arithmetic of the sparse epilogue on the staged rows (nrows leading real rows). With
+// `dry` it runs one pass on whatever the stage holds and stores nothing: a kernel runs it
+// once before its first tile arrives, so the code and the expert scalars are cached by then.
+template <int MODE, int ACT>
+__device__ __noinline__ void sparse_compute(const GemmParams& p, const Phase& ph, int etid, int e, int nt,
+                                            int64_t row0, int nrows, const float* s_stage, const int32_t* s_slot,
+                                            const float* s_scal, bool dry) {
+  constexpr bool kGated = is_gated(ACT);
+  const float a1 = ph.alpha[e];
+  const float a1g = (!is_g2(MODE) && kGated) ? ph.alpha_gate[e] : a1;
+  if constexpr (is_g2(MODE)) {
+    const float d2 = __fmul_rn(a1, __fdiv_rn(1.0f, p.g2));
+    const int n_out = nrows * kTileN;
+    for (int o = etid; o < n_out; o += kEpiThreads) {
+      const int row = o >> 8, j = o & (kTileN - 1);
+      const int col = nt * kTileN + j;
+      if (col >= ph.N) continue;
+      const float y = __fmul_rn(s_stage[row * kTileN + j], d2);
+      if constexpr (MODE == kG2Rows) {
+        const uint16_t v = __bfloat16_as_ushort(__float2bfloat16_rn(y));
+        if (!dry) static_cast<uint16_t*>(ph.out)[(row0 + row) * ph.N + col] = v;
+      } else {
+        const int t = s_slot[row] / p.top_k;
+        const float v = __fmul_rn(y, s_scal[row]);
+        if (!dry) red_add_f32(static_cast<float*>(ph.out) + static_cast<int64_t>(t) * ph.N + col, v);
+      }
+    }
+  } else {
+    const int I = p.inter;
+    const int ip16 = static_cast<int>(roundup64(I, kTileK) / 16);
+    constexpr int kOut = kGated ? 128 : kTileN;  // intermediate columns per row of the tile
+    const int n_out = nrows * kOut;
+    uint8_t* out = static_cast<uint8_t*>(ph.out);
+    // every lane runs every pass (the block max is a warp shuffle); 16-lane groups are
+    // wholly valid or wholly not
+    for (int o0 = 0; o0 < n_out; o0 += kEpiThreads) {
+      const int o = o0 + etid;
+      const int row = (o / kOut) & (kSparseRows - 1);
+      const int j = o % kOut;
+      const int ic = kGated ? nt * 128 + j : nt * kTileN + j;
+      const bool valid = o < n_out && ic < I;
+      float h = 0.0f;
+      if (valid) {
+        const float xs_t = s_scal[row];
+        const float* st = s_stage + row * kTileN;
+        const float yg = __fmul_rn(__fmul_rn(st[j], xs_t), kGated ? a1g : a1);
+        const float yu = kGated ? __fmul_rn(__fmul_rn(st[128 + j], xs_t), a1) : 0.0f;
+        h = bf16_round_f32(activation_f32<ACT>(yg, yu));
+      }
+      float amax = fmaxf(0.0f, fabsf(h));
+#pragma unroll
+      for (int m = 8; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+      const float sc = __fmul_rn(__fdiv_rn(amax, 6.0f), p.g2);
+      const uint32_t qs = f32_to_e4m3(sc);
+      const float qf = e4m3_to_f32(qs);
+      const float inv = (qf == 0.0f) ? 0.0f : __fdiv_rn(p.g2, qf);
+      const float hn = __shfl_down_sync(0xffffffffu, h, 1);
+      if (valid && !dry) {
+        const int64_t prow = row0 + row;
+        if ((j & 1) == 0) out[prow * (I / 2) + ic / 2] = static_cast<uint8_t>(f32x2_to_e2m1(__fmul_rn(h, inv), __fmul_rn(hn, inv)));
+        if ((j & 15) == 0) ph.out_sf[sf_tile_offset(prow, ic >> 4, ip16)] = static_cast<uint8_t>(qs);
+      }
+    }
+    // zero the scale columns of the K padding once per real row (last column tile)
+    if (!dry && nt == ph.n_tiles - 1 && etid < nrows) {
+      for (int c4 = I / 64; c4 < ip16 / 4; ++c4)
+        *reinterpret_cast<uint32_t*>(ph.out_sf + sf_tile_offset(row0 + etid, 4 * c4, ip16)) = 0u;
+    }
+  }
+}
+
 // Sparse epilogue of one work unit (all its real rows among the first kSparseRows rows).
 // The two warps that own TMEM lanes 0-31 copy the real rows' 256 accumulator columns into
 // the shared stage and release the accumulator; then all 256 epilogue threads share the
@@ -281,15 +365,12 @@ __device__ __forceinline__ float activation_f32(float yg, float yu) {
 // of a row), so a 16-value requant block is 16 lanes of one warp (block max by shuffles).
 // The arithmetic per value is the dense epilogue's. Returns false after an aborted wait.
 template <int MODE, int ACT>
-__device__ __noinline__ bool sparse_epilogue(const GemmParams& p, uint32_t tmem_row, int q, int half, int lane,
+__device__ __noinline__ bool sparse_epilogue(const GemmParams& p, const Phase& ph, uint32_t tmem_row, int q, int half,
+                                             int lane,
                                                 int etid, int e, int nt, int64_t row0, int slot, float scal,
                                                 float* s_stage, int32_t* s_slot, float* s_scal, uint64_t* acc_empty,
                                                 uint64_t* stage_full, uint64_t* stage_empty, uint32_t& sphase,
                                                 volatile int* abort_flag) {
-  constexpr bool kGated = is_gated(ACT);
-  // scalars of the expert, loaded while the stage fills
-  const float a1 = p.alpha[e];
-  const float a1g = (!is_g2(MODE) && kGated) ? p.alpha_gate[e] : a1;
   if (q == 0) {
     bool ok = mbar_wait(stage_empty, sphase ^ 1, abort_flag, p.dev_status);
     if (!__all_sync(0xffffffffu, ok)) return false;
@@ -327,70 +408,90 @@ __device__ __noinline__ bool sparse_epilogue(const GemmParams& p, uint32_t tmem_
   int nrows = 0;  // real rows lead the tile
 #pragma unroll
   for (int i = 0; i < kSparseRows; ++i) nrows += s_slot[i] >= 0 ? 1 : 0;
-  if constexpr (is_g2(MODE)) {
-    const float d2 = __fmul_rn(a1, __fdiv_rn(1.0f, p.g2));
-    const int n_out = nrows * kTileN;
-    for (int o = etid; o < n_out; o += kEpiThreads) {
-      const int row = o >> 8, j = o & (kTileN - 1);
-      const int col = nt * kTileN + j;
-      if (col >= p.N) continue;
-      const float y = __fmul_rn(s_stage[row * kTileN + j], d2);
-      if constexpr (MODE == kG2Rows) {
-        static_cast<uint16_t*>(p.out)[(row0 + row) * p.N + col] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
-      } else {
-        const int t = s_slot[row] / p.top_k;
-        red_add_f32(static_cast<float*>(p.out) + static_cast<int64_t>(t) * p.N + col, __fmul_rn(y, s_scal[row]));
-      }
-    }
-  } else {
-    const int I = p.inter;
-    const int ip16 = static_cast<int>(roundup64(I, kTileK) / 16);
-    constexpr int kOut = kGated ? 128 : kTileN;  // intermediate columns per row of the tile
-    const int n_out = nrows * kOut;
-    uint8_t* out = static_cast<uint8_t*>(p.out);
-    // every lane runs every pass (the block max is a warp shuffle); 16-lane groups are
-    // wholly valid or wholly not
-    for (int o0 = 0; o0 < n_out; o0 += kEpiThreads) {
-      const int o = o0 + etid;
-      const int row = (o / kOut) & (kSparseRows - 1);
-      const int j = o % kOut;
-      const int ic = kGated ? nt * 128 + j : nt * kTileN + j;
-      const bool valid = o < n_out && ic < I;
-      float h = 0.0f;
-      if (valid) {
-        const float xs_t = s_scal[row];
-        const float* st = s_stage + row * kTileN;
-        const float yg = __fmul_rn(__fmul_rn(st[j], xs_t), kGated ? a1g : a1);
-        const float yu = kGated ? __fmul_rn(__fmul_rn(st[128 + j], xs_t), a1) : 0.0f;
-        h = bf16_round_f32(activation_f32<ACT>(yg, yu));
-      }
-      float amax = fmaxf(0.0f, fabsf(h));
-#pragma unroll
-      for (int m = 8; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
-      const float sc = __fmul_rn(__fdiv_rn(amax, 6.0f), p.g2);
-      const uint32_t qs = f32_to_e4m3(sc);
-      const float qf = e4m3_to_f32(qs);
-      const float inv = (qf == 0.0f) ? 0.0f : __fdiv_rn(p.g2, qf);
-      const float hn = __shfl_down_sync(0xffffffffu, h, 1);
-      if (valid) {
-        const int64_t prow = row0 + row;
-        if ((j & 1) == 0) out[prow * (I / 2) + ic / 2] = static_cast<uint8_t>(f32x2_to_e2m1(__fmul_rn(h, inv), __fmul_rn(hn, inv)));
-        if ((j & 15) == 0) p.out_sf[sf_tile_offset(prow, ic >> 4, ip16)] = static_cast<uint8_t>(qs);
-      }
-    }
-    // zero the scale columns of the K padding once per real row (last column tile)
-    if (nt == p.n_tiles - 1 && etid < nrows) {
-      for (int c4 = I / 64; c4 < ip16 / 4; ++c4)
-        *reinterpret_cast<uint32_t*>(p.out_sf + sf_tile_offset(row0 + etid, 4 * c4, ip16)) = 0u;
-    }
-  }
+  sparse_compute<MODE, ACT>(p, ph, etid, e, nt, row0, nrows, s_stage, s_slot, s_scal, false);
   __syncwarp();
   if (lane == 0) mbar_arrive(stage_empty);
   return true;
 }
 
+// Bounded wait until *counter >= target (acquire): the GEMM2 half of a chained launch waits
+// here for the GEMM1 tiles it reads. Gives up like mbar_wait.
+__device__ __forceinline__ bool wait_counter(const int32_t* counter, int target, volatile int* abort_flag,
+                                             int32_t* dev_status) {
+  uint64_t t0 = 0;
+  while (true) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
+    if (v >= target) return true;
+    if (*abort_flag) return false;
+    const uint64_t now = globaltimer_ns();
+    if (t0 == 0) {
+      t0 = now;
+    } else if (now - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      if (dev_status) atomicOr(dev_status, MOE_DEV_TIMEOUT);
+      return false;
+    }
+    __nanosleep(64);
+  }
+}
+
+// *counter += v with release semantics at GPU scope: the warp's earlier writes (ordered before
+// this lane's by __syncwarp) are visible to whoever acquires the new count
+__device__ __forceinline__ void red_release_add(int32_t* counter, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(counter), "r"(v) : "memory");
+}
+
+// orders this thread's generic-proxy global accesses with its async-proxy (TMA) ones
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+// L2 prefetch of a contiguous range (16-byte aligned, multiple of 16 bytes) in 64 KB requests
+__device__ __forceinline__ void prefetch_l2(const uint8_t* ptr, int64_t bytes) {
+  for (int64_t o = 0; o < bytes; o += 65536) {
+    const int64_t n = bytes - o < 65536 ? bytes - o : 65536;
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr + o), "r"(static_cast<uint32_t>(n))
+                 : "memory");
+  }
+}
+
+// Epilogue of one work unit `uu` of GEMM `ph` (epilogue kind EK): wait for the accumulator,
+// then the sparse or the dense epilogue. Returns false after an aborted wait; row0 = the
+// unit's first plan row.
+template <int EK, int ACT>
+__device__ __forceinline__ bool epilogue_unit(const GemmParams& p, const Phase& ph, int uu, const int32_t* s_off,
+                                              uint32_t tmem_row, int q, int half, int lane, int r, int etid,
+                                              uint32_t& acc_phase, uint32_t& sphase, float* s_stage, int32_t* s_slot,
+                                              float* s_scal, uint64_t* acc_full, uint64_t* acc_empty,
+                                              uint64_t* stage_full, uint64_t* stage_empty, volatile int* abort_flag,
+                                              int64_t& row0) {
+  int e, nt, mi;
+  decode_unit(uu, s_off, p.El, ph.n_tiles, e, nt, mi);
+  row0 = s_off[e] + mi * kTileM;
+  const int64_t prow = row0 + r;
+  const int slot = p.row_to_slot[prow];
+  const float xs_t = (!is_g2(EK) && slot >= 0) ? p.xs[slot / p.top_k] : 0.0f;
+  const bool sparse = (EK == kG1Fused || is_g2(EK)) && p.sparse && p.row_to_slot[row0 + kSparseRows] < 0;
+  float scal = xs_t;
+  if constexpr (EK == kG2Reduce) scal = slot >= 0 ? route_weight(p.route_w, p.route_w_dtype, slot, p.rsf) : 0.0f;
+  bool ok = mbar_wait(acc_full, acc_phase, abort_flag, p.dev_status);
+  ok = __all_sync(0xffffffffu, ok);
+  if (!ok) return false;
+  tc_fence_after();
+  acc_phase ^= 1;
+  if (sparse)
+    return sparse_epilogue<EK, ACT>(p, ph, tmem_row, q, half, lane, etid, e, nt, row0, slot, scal, s_stage, s_slot,
+                                    s_scal, acc_empty, stage_full, stage_empty, sphase, abort_flag);
+  uint32_t acc[128];
+  load_acc<EK, ACT>(tmem_row, half, acc, acc_empty);
+  if (__any_sync(0xffffffffu, slot >= 0)) epilogue_compute<EK, ACT>(p, ph, acc, half, e, nt, prow, slot, xs_t);
+  return true;
+}
+
 template <int MODE, int ACT>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmParams p) {
+  constexpr bool kChain = is_chain(MODE);
+  constexpr int kEpi0 = first_epilogue(MODE);
+  constexpr int kEpi1 = second_epilogue(MODE);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
@@ -431,13 +532,23 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    prefetch_tensormap(&p.tmap_a);
-    prefetch_tensormap(&p.tmap_a32);
-    prefetch_tensormap(&p.tmap_b);
+    for (int i = 0; i < (kChain ? 2 : 1); ++i) {
+      prefetch_tensormap(&p.ph[i].tmap_a);
+      prefetch_tensormap(&p.ph[i].tmap_a32);
+      prefetch_tensormap(&p.ph[i].tmap_b);
+    }
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
+  }
+  if (warp >= 2 && p.sparse) {
+    // while the previous kernel finishes: one dry pass of the sparse epilogue (expert 0),
+    // which brings its code and the scalar tables into the caches
+    if constexpr (kEpi0 == kG1Fused || is_g2(kEpi0))
+      sparse_compute<kEpi0, ACT>(p, p.ph[0], threadIdx.x - 64, 0, 0, 0, 1, s_stage, s_slot, s_scal, true);
+    if constexpr (kChain)
+      sparse_compute<kEpi1, MOE_ACT_IDENTITY>(p, p.ph[1], threadIdx.x - 64, 0, 0, 0, 1, s_stage, s_slot, s_scal, true);
   }
   pdl_wait();  // the plan, activations and tile counter come from earlier kernels
   for (int i = threadIdx.x; i <= p.El; i += blockDim.x) s_off[i] = p.padded_offsets[i];
@@ -445,7 +556,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int total_units = (s_off[p.El] >> 7) * p.n_tiles;
+  // units [0, units0) belong to the first GEMM, [units0, total_units) to the second (chained)
+  const int mtiles = s_off[p.El] >> 7;
+  const int units0 = mtiles * p.ph[0].n_tiles;
+  const int total_units = units0 + (kChain ? mtiles * p.ph[1].n_tiles : 0);
   // the producer claims work units and hands their ids to the MMA and epilogue warps
   auto take_unit = [&](uint32_t& rslot, uint32_t& rphase, bool one_lane) -> int {
     bool got = mbar_wait(&unit_full[rslot], rphase, abort_flag, p.dev_status);
@@ -473,25 +587,39 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         mbar_arrive(&unit_full[rslot]);
         if (++rslot == kUnitRing) { rslot = 0; rphase ^= 1; }
         if (u < 0) break;
+        const bool second = kChain && u >= units0;
+        const Phase& ph = p.ph[second ? 1 : 0];
         int e, nt, mi;
-        decode_unit(u, s_off, p.El, p.n_tiles, e, nt, mi);
+        decode_unit(second ? u - units0 : u, s_off, p.El, ph.n_tiles, e, nt, mi);
         const int row0 = s_off[e] + mi * kTileM;
-        const int brow0 = e * p.Np + nt * kTileN;
-        const int64_t kt = p.Kp >> 6;  // 512-byte scale tiles per 128 rows
-        const uint8_t* sfa = p.sfa + static_cast<int64_t>(row0 >> 7) * kt * 512;
-        const uint8_t* sfb0 = p.sfb + (static_cast<int64_t>(e) * (p.Np >> 7) + nt * 2) * kt * 512;
+        const int brow0 = e * ph.Np + nt * kTileN;
+        const int64_t kt = ph.Kp >> 6;  // 512-byte scale tiles per 128 rows
+        const uint8_t* sfa = ph.sfa + static_cast<int64_t>(row0 >> 7) * kt * 512;
+        const uint8_t* sfb0 = ph.sfb + (static_cast<int64_t>(e) * (ph.Np >> 7) + nt * 2) * kt * 512;
         const uint8_t* sfb1 = sfb0 + kt * 512;
+        if (second) {
+          // the weight tile and its scales do not depend on GEMM1: start them towards L2,
+          // then wait until every GEMM1 tile of these rows has been written
+          prefetch_l2(ph.b_raw + static_cast<int64_t>(brow0) * (ph.K / 2), static_cast<int64_t>(kTileN) * (ph.K / 2));
+          prefetch_l2(sfb0, 2 * kt * 512);
+          if (!wait_counter(p.mt_done + (row0 >> 7), (kEpiThreads / 32) * p.ph[0].n_tiles, abort_flag,
+                            p.dev_status)) {
+            ok = false;
+            break;
+          }
+          fence_proxy_async_global();  // the TMA reads below follow the observed generic writes
+        }
         // a tile whose row 32 is padding has all its real rows in the first 32 (padding rows
         // end a segment): load only those; the MMA rows fed by stale shared memory are
         // padding rows, whose results are never stored
         const bool short_tile = p.row_to_slot[row0 + 32] < 0;
         const uint32_t tx = short_tile ? kStageTx - (kABytes - 32 * 128) : kStageTx;
-        for (int kb = 0; kb < p.nkb; ++kb) {
+        for (int kb = 0; kb < ph.nkb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.dev_status)) { ok = false; break; }
           uint8_t* st = smem + stage * kStageBytes;
           mbar_arrive_expect_tx(&full[stage], tx);
-          tma_load_2d(st, short_tile ? &p.tmap_a32 : &p.tmap_a, kb * 128, row0, &full[stage]);
-          tma_load_2d(st + kOffB, &p.tmap_b, kb * 128, brow0, &full[stage]);
+          tma_load_2d(st, short_tile ? &ph.tmap_a32 : &ph.tmap_a, kb * 128, row0, &full[stage]);
+          tma_load_2d(st + kOffB, &ph.tmap_b, kb * 128, brow0, &full[stage]);
           bulk_load(st + kOffSfa, sfa + kb * 2048, 2048, &full[stage]);
           bulk_load(st + kOffSfb, sfb0 + kb * 2048, 2048, &full[stage]);
           bulk_load(st + kOffSfb + 2048, sfb1 + kb * 2048, 2048, &full[stage]);
@@ -517,7 +645,8 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         if (u < 0) break;
         if (!mbar_wait(acc_empty, acc_phase ^ 1, abort_flag, p.dev_status)) { ok = false; break; }
         tc_fence_after();
-        for (int kb = 0; kb < p.nkb; ++kb) {
+        const int nkb = p.ph[kChain && u >= units0 ? 1 : 0].nkb;
+        for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag, p.dev_status)) { ok = false; break; }
           tc_fence_after();
           const uint32_t st = smem_u32(smem + stage * kStageBytes);
@@ -561,30 +690,25 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     while (true) {
       const int u = take_unit(rslot, rphase, false);
       if (u < 0) break;
-      int e, nt, mi;
-      decode_unit(u, s_off, p.El, p.n_tiles, e, nt, mi);
-      const int64_t row0 = s_off[e] + mi * kTileM;
-      const int64_t prow = row0 + r;
-      const int slot = p.row_to_slot[prow];
-      const float xs_t = (!is_g2(MODE) && slot >= 0) ? p.xs[slot / p.top_k] : 0.0f;
-      const bool sparse = (MODE == kG1Fused || is_g2(MODE)) && p.sparse && p.row_to_slot[row0 + kSparseRows] < 0;
-      float scal = xs_t;
-      if constexpr (MODE == kG2Reduce) scal = slot >= 0 ? route_weight(p.route_w, p.route_w_dtype, slot, p.rsf) : 0.0f;
-      bool ok = mbar_wait(acc_full, acc_phase, abort_flag, p.dev_status);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      if (sparse) {
-        acc_phase ^= 1;
-        if (!sparse_epilogue<MODE, ACT>(p, tmem_row, q, half, lane, etid, e, nt, row0, slot, scal, s_stage, s_slot,
-                                        s_scal, acc_empty, stage_full, stage_empty, sphase, abort_flag))
+      int64_t row0 = 0;
+      bool first = true;
+      if constexpr (kChain) first = u < units0;
+      if (first) {
+        if (!epilogue_unit<kEpi0, ACT>(p, p.ph[0], u, s_off, tmem_row, q, half, lane, r, etid, acc_phase, sphase,
+                                       s_stage, s_slot, s_scal, acc_full, acc_empty, stage_full, stage_empty,
+                                       abort_flag, row0))
           break;
-        continue;
+        if (kChain) {
+          // this warp's share of a GEMM1 tile is written: publish it to the GEMM2 tiles
+          __syncwarp();
+          if (lane == 0) red_release_add(p.mt_done + (row0 >> 7), 1);
+        }
+      } else if constexpr (kChain) {
+        if (!epilogue_unit<kEpi1, MOE_ACT_IDENTITY>(p, p.ph[1], u - units0, s_off, tmem_row, q, half, lane, r, etid,
+                                                    acc_phase, sphase, s_stage, s_slot, s_scal, acc_full, acc_empty,
+                                                    stage_full, stage_empty, abort_flag, row0))
+          break;
       }
-      uint32_t acc[128];
-      load_acc<MODE, ACT>(tmem_row, half, acc, acc_empty);
-      acc_phase ^= 1;
-      if (__any_sync(0xffffffffu, slot >= 0)) epilogue_compute<MODE, ACT>(p, acc, half, e, nt, prow, slot, xs_t);
     }
   }
   tc_fence_before();
@@ -611,6 +735,12 @@ moe_status_t launch_plain_a(int mode, int act, const GemmParams& prm, int64_t un
 moe_status_t launch_plain_b(int mode, int act, const GemmParams& prm, int64_t units_max, size_t smem,
                             cudaStream_t s);
 moe_status_t launch_rows(int mode, const GemmParams& prm, int64_t units_max, size_t smem, cudaStream_t s);
+moe_status_t launch_chain_gated(int mode, int act, const GemmParams& prm, int64_t units_max, size_t smem,
+                                cudaStream_t s);
+moe_status_t launch_chain_plain_a(int mode, int act, const GemmParams& prm, int64_t units_max, size_t smem,
+                                  cudaStream_t s);
+moe_status_t launch_chain_plain_b(int mode, int act, const GemmParams& prm, int64_t units_max, size_t smem,
+                                  cudaStream_t s);
 
 }  // namespace gemm
 }  // namespace moe

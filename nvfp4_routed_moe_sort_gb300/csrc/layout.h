@@ -67,7 +67,7 @@ inline PreparedLayout prepared_layout(const Dims& d) {
 // intermediate [cap, I/2] + scale tiles [cap/128][Ip/64][512], and the BF16 expert rows
 // [cap, H] (finalized output) or the FP32 accumulator [M, H] (accumulated output).
 struct WorkspaceLayout {
-  size_t sched, aq, asf, iq, isf, g, total;
+  size_t sched, mtd, aq, asf, iq, isf, g, total;
   int64_t cap;
 };
 
@@ -82,6 +82,7 @@ inline WorkspaceLayout workspace_layout(const Dims& d, int64_t M, int64_t top_k,
   L.cap = plan_capacity_rows(M, top_k, d.El);
   size_t c = 0;
   L.sched = take(c, 256);  // GEMM tile counters, zeroed by the permute kernel
+  L.mtd = take(c, (L.cap / kTileM) * 4);  // per-row-tile GEMM1 completion counts (chained GEMMs), zeroed too
   L.aq = take(c, L.cap * d.H / 2);
   L.asf = take(c, L.cap * d.Hp / 16);
   L.iq = take(c, L.cap * d.I / 2);
@@ -100,7 +101,14 @@ enum GemmMode : int {
   kG1Act = 2,     // BF16 intermediate (test hook)
   kG2Rows = 3,    // BF16 expert rows
   kG2Reduce = 4,  // route-weighted rows added in FP32 into the [M, H] accumulator
+  kChainRows = 5,    // GEMM1 (kG1Fused) then GEMM2 (kG2Rows) in one launch
+  kChainReduce = 6,  // GEMM1 (kG1Fused) then GEMM2 (kG2Reduce) in one launch
 };
+
+// Batches of at most this many routed slots run GEMM1 and GEMM2 as one chained launch: the
+// GEMM2 tiles of a row tile start once its GEMM1 tiles are written, so the second weight
+// stream overlaps the first GEMM's tail instead of waiting for a kernel boundary.
+constexpr int64_t kChainMaxSlots = MOE_CHAIN_MAX_SLOTS;
 
 struct GemmLaunch {
   int mode;
@@ -129,10 +137,13 @@ struct GemmLaunch {
 };
 
 moe_status_t launch_gemm(const GemmLaunch& g, cudaStream_t s);
+// GEMM1 (g1, kG1Fused) and GEMM2 (g2, kG2Rows or kG2Reduce) in one launch; mt_done holds
+// cap / 128 zeroed counters
+moe_status_t launch_gemm_chain(const GemmLaunch& g1, const GemmLaunch& g2, int32_t* mt_done, cudaStream_t s);
 moe_status_t launch_permute(const int32_t* padded_offsets, int El, const int32_t* row_to_slot, int top_k,
                             int64_t cap, const uint8_t* xq, const uint8_t* xsf, int H, uint8_t* aq, uint8_t* asf,
-                            int32_t* tile_counters, const uint16_t* acc_init, float* acc, int64_t acc_elems,
-                            cudaStream_t s);
+                            int32_t* tile_counters, int32_t* mt_done, int64_t n_mt, const uint16_t* acc_init,
+                            float* acc, int64_t acc_elems, cudaStream_t s);
 moe_status_t launch_finalize(const uint16_t* rows, const void* topk_weights, int weights_dtype, float rsf,
                              const int32_t* token_to_row, int M, int top_k, int H, uint16_t* out, cudaStream_t s);
 moe_status_t launch_store_acc(const float* acc, int64_t elems, uint16_t* out, cudaStream_t s);

@@ -26,6 +26,7 @@ __global__ void __launch_bounds__(256) permute_kernel(const int32_t* __restrict_
                                                       const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xsf,
                                                       int H, uint8_t* __restrict__ aq, uint8_t* __restrict__ asf,
                                                       int32_t* __restrict__ tile_counters,
+                                                      int32_t* __restrict__ mt_done, int64_t n_mt,
                                                       const uint16_t* __restrict__ acc_init, float* __restrict__ acc,
                                                       int64_t acc_elems) {
   pdl_trigger();
@@ -33,6 +34,9 @@ __global__ void __launch_bounds__(256) permute_kernel(const int32_t* __restrict_
   const int lane = threadIdx.x & 31;
   // the GEMMs that follow claim their work units from these counters
   if (blockIdx.x == 0 && threadIdx.x < 2) tile_counters[threadIdx.x] = 0;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_mt;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    mt_done[i] = 0;
   const int64_t P = padded_offsets[El];
   const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -207,15 +211,15 @@ int warp_grid(int64_t rows) {
 
 moe_status_t launch_permute(const int32_t* padded_offsets, int El, const int32_t* row_to_slot, int top_k,
                             int64_t cap, const uint8_t* xq, const uint8_t* xsf, int H, uint8_t* aq, uint8_t* asf,
-                            int32_t* tile_counters, const uint16_t* acc_init, float* acc, int64_t acc_elems,
-                            cudaStream_t s) {
+                            int32_t* tile_counters, int32_t* mt_done, int64_t n_mt, const uint16_t* acc_init,
+                            float* acc, int64_t acc_elems, cudaStream_t s) {
   if (cap == 0) return MOE_OK;
   int grid = warp_grid(cap);
   const int64_t acc_blocks = (acc_elems / 8 + 255) / 256;
   const int64_t acc_cap = static_cast<int64_t>(num_sms()) * 8;
   if (acc_blocks > grid) grid = static_cast<int>(acc_blocks < acc_cap ? acc_blocks : acc_cap);
   return launch_pdl(permute_kernel, dim3(grid), dim3(256), 0, s, padded_offsets, El, row_to_slot, top_k, xq, xsf, H,
-                    aq, asf, tile_counters, acc_init, acc, acc_elems);
+                    aq, asf, tile_counters, mt_done, n_mt, acc_init, acc, acc_elems);
 }
 
 moe_status_t launch_store_acc(const float* acc, int64_t elems, uint16_t* out, cudaStream_t s) {

@@ -66,7 +66,8 @@ constexpr int kCopyBatch = 4;  // loads in flight per thread in the copy loops
 //  (2) the one-block plan of plan_single_kernel;
 //  (3) the permutation: thread per (routed slot, 16-byte chunk) of the quantised row and
 //      per (slot, 4-scale group) of its scale row, the slot's plan row taken from the plan.
-// Also the zeroed GEMM tile counters and, for an accumulated output, the FP32 copy of out.
+// Also the zeroed GEMM tile and row-tile counters and, for an accumulated output, the FP32
+// copy of out.
 // Data written in one phase is read in the next by other threads of the CTA after a
 // barrier, through L2 (ld.global.cg), never through the read-only path.
 __global__ void __launch_bounds__(kPrologueThreads) small_prologue_kernel(
@@ -74,7 +75,7 @@ __global__ void __launch_bounds__(kPrologueThreads) small_prologue_kernel(
     int id_mask, int top_k, int off, int El, int64_t cap, uint8_t* xq, uint8_t* xsf, float* __restrict__ xs,
     int32_t* __restrict__ counts, int32_t* __restrict__ padded_offsets, int32_t* row_to_slot, int32_t* token_to_row,
     int32_t* dev_status, uint8_t* __restrict__ aq, uint8_t* __restrict__ asf, int32_t* __restrict__ tile_counters,
-    const uint16_t* __restrict__ acc_init, float* __restrict__ acc) {
+    int32_t* __restrict__ mt_done, int n_mt, const uint16_t* __restrict__ acc_init, float* __restrict__ acc) {
   __shared__ PlanSmem sm;
   __shared__ unsigned s_amax[kPrologueMaxRows];      // per-row max |x| (bits of a non-negative float)
   __shared__ int32_t s_row[kPrologueMaxSlots];       // plan row of each slot
@@ -83,6 +84,7 @@ __global__ void __launch_bounds__(kPrologueThreads) small_prologue_kernel(
   for (int i = threadIdx.x; i < M; i += kPrologueThreads) s_amax[i] = 0u;
   pdl_wait();
   if (threadIdx.x < 2) tile_counters[threadIdx.x] = 0;
+  for (int i = threadIdx.x; i < n_mt; i += kPrologueThreads) mt_done[i] = 0;
   const int n = M * top_k;
   __syncthreads();
   // (0) histogram of the routed slots per local expert
@@ -298,7 +300,8 @@ extern "C" moe_status_t moe_routed_forward(const uint16_t* x, int32_t M, int64_t
                     static_cast<int>(d.H), ld_x, act_scale_mode == MOE_SCALE_PER_TOKEN ? 1 : 0, topk_ids, id_mask,
                     static_cast<int>(top_k), static_cast<int>(local_expert_offset), static_cast<int>(d.El), R.cap, xq,
                     xsf, xs, counts, padded, r2s, token_to_row, dev_status, fb + L.aq, fb + L.asf,
-                    reinterpret_cast<int32_t*>(fb + L.sched), accum ? static_cast<const uint16_t*>(out) : nullptr,
+                    reinterpret_cast<int32_t*>(fb + L.sched), reinterpret_cast<int32_t*>(fb + L.mtd),
+                    static_cast<int>(L.cap / kTileM), accum ? static_cast<const uint16_t*>(out) : nullptr,
                     accum ? reinterpret_cast<float*>(fb + L.g) : nullptr);
     if (st != MOE_OK) return st;
   } else {
