@@ -170,6 +170,7 @@ def traffic_from_profiles(kernel: str, workload: str):
     """DRAM bytes per launch of `kernel` from the committed ncu summary
     (profiles/dram_traffic.txt), or None when the kernel's source has changed since the
     counters were taken (sha256 of gemm_kernel.cuh followed by common.cuh)."""
+    kernel = {"gemm1+gemm2 (chained)": "gemm_chained"}.get(kernel, kernel)
     p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(p):
         return None
