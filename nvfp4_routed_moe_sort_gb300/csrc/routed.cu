@@ -8,9 +8,9 @@
 // GEMM2, finalize).
 //
 // Small batches (decode: at most 2048 routed slots and 2^17 hidden values) run the
-// quantiser, the plan and the permutation in one kernel of one 1024-thread CTA, so the step
-// is four launches (prologue, GEMM1, GEMM2, combine) instead of six; each of those steps is
-// latency-bound at these sizes. Larger batches run the separate kernels of
+// quantiser, the plan and the permutation in one kernel of one 1024-thread CTA, and GEMM1
+// and GEMM2 as one chained launch, so the step is three launches (prologue, GEMMs, combine)
+// instead of six; each of those steps is latency-bound at these sizes. Larger batches run the separate kernels of
 // moe_quantize_input, moe_plan and moe_grouped_fp4_forward. Both paths compute the same
 // bytes: the prologue's quantiser and plan follow the same arithmetic and order as the
 // separate kernels.
@@ -56,25 +56,22 @@ bool small_batch(int64_t M, int64_t k, int64_t H) {
 }
 
 constexpr int kPrologueMaxRows = static_cast<int>(kPrologueMaxValues / 128);  // H >= 128
-constexpr int kCopyBatch = 4;  // loads in flight per thread in the copy loops
 
 // One CTA, every phase spread over all 1024 threads:
-//  (0) the routed-slot histogram;
-//  (1) NVFP4 quantisation: thread per 16-value block of the M x H input (per-token amax by a
-//      shared-memory max over the row's blocks, then the blocks are read again from L2), with
-//      the arithmetic of quantize_rows_kernel;
-//  (2) the one-block plan of plan_single_kernel;
-//  (3) the permutation: thread per (routed slot, 16-byte chunk) of the quantised row and
-//      per (slot, 4-scale group) of its scale row, the slot's plan row taken from the plan.
-// Also the zeroed GEMM tile and row-tile counters and, for an accumulated output, the FP32
-// copy of out.
-// Data written in one phase is read in the next by other threads of the CTA after a
-// barrier, through L2 (ld.global.cg), never through the read-only path.
+//  (0) the routed-slot histogram and, for per-token scales, each token's max |x| (thread per
+//      16-value block, maximum through shared memory);
+//  (1) the one-block plan of plan_single_kernel;
+//  (2) NVFP4 quantisation of each 16-value block (the arithmetic of quantize_rows_kernel),
+//      its 8 code bytes and its scale byte stored straight into every plan row of the
+//      token (the permuted operand of GEMM1 and its 128x4 scale tiles): the quantised
+//      activations never make a round trip through memory.
+// Also the per-token scales, the zeroed GEMM tile and row-tile counters and, for an
+// accumulated output, the FP32 copy of out.
 __global__ void __launch_bounds__(kPrologueThreads) small_prologue_kernel(
     const uint16_t* __restrict__ x, int M, int H, int64_t ld, int per_token, const int32_t* __restrict__ ids,
-    int id_mask, int top_k, int off, int El, int64_t cap, uint8_t* xq, uint8_t* xsf, float* __restrict__ xs,
-    int32_t* __restrict__ counts, int32_t* __restrict__ padded_offsets, int32_t* row_to_slot, int32_t* token_to_row,
-    int32_t* dev_status, uint8_t* __restrict__ aq, uint8_t* __restrict__ asf, int32_t* __restrict__ tile_counters,
+    int id_mask, int top_k, int off, int El, float* __restrict__ xs, int32_t* __restrict__ counts,
+    int32_t* __restrict__ padded_offsets, int32_t* row_to_slot, int32_t* token_to_row, int32_t* dev_status,
+    uint8_t* __restrict__ aq, uint8_t* __restrict__ asf, int32_t* __restrict__ tile_counters,
     int32_t* __restrict__ mt_done, int n_mt, const uint16_t* __restrict__ acc_init, float* __restrict__ acc) {
   __shared__ PlanSmem sm;
   __shared__ unsigned s_amax[kPrologueMaxRows];      // per-row max |x| (bits of a non-negative float)
@@ -86,16 +83,14 @@ __global__ void __launch_bounds__(kPrologueThreads) small_prologue_kernel(
   if (threadIdx.x < 2) tile_counters[threadIdx.x] = 0;
   for (int i = threadIdx.x; i < n_mt; i += kPrologueThreads) mt_done[i] = 0;
   const int n = M * top_k;
+  const int nblk = H / kBlock;
+  const int nb_all = M * nblk;
   __syncthreads();
-  // (0) histogram of the routed slots per local expert
+  // (0) histogram of the routed slots per local expert; per-token maxima
   for (int s = threadIdx.x; s < n; s += kPrologueThreads) {
     const int l = local_of(entry_id(ids, s, id_mask), off, El);
     if (l >= 0) atomicAdd(&sm.cnt[l], 1);
   }
-  __syncthreads();
-  // (1) quantise
-  const int nblk = H / kBlock;
-  const int nb_all = M * nblk;
   if (per_token) {
     for (int bi = threadIdx.x; bi < nb_all; bi += kPrologueThreads) {
       const int r = bi / nblk, b = bi - r * nblk;
@@ -106,8 +101,24 @@ __global__ void __launch_bounds__(kPrologueThreads) small_prologue_kernel(
       for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
       atomicMax(&s_amax[r], __float_as_uint(amax));
     }
-    __syncthreads();
   }
+  __syncthreads();
+  // (1) plan
+  scan_padded(sm, El);
+  __syncthreads();
+  for (int l = threadIdx.x; l <= El; l += kPrologueThreads) {
+    padded_offsets[l] = sm.cursor[l];
+    if (l < El) counts[l] = sm.cnt[l];
+  }
+  // -1 on the segments' padding rows; rows past the padded total are never read by the
+  // GEMMs, so (unlike moe_plan's output) this internal row_to_slot leaves them unwritten
+  fill_padding(sm.cursor, sm.cnt, El, sm.cursor[El], sm.cursor[El], row_to_slot);
+  __syncthreads();
+  place_range(ids, id_mask, 0, n, top_k, off, El, sm, row_to_slot, token_to_row, dev_status);
+  for (int s = threadIdx.x; s < n; s += kPrologueThreads) s_row[s] = __ldcg(token_to_row + s);
+  __syncthreads();
+  // (2) quantise each block once and store it into every plan row of its token
+  const int kcols_p = static_cast<int>(roundup64(H, kTileK) / 16);  // scale columns incl. K padding
   for (int bi = threadIdx.x; bi < nb_all; bi += kPrologueThreads) {
     const int r = bi / nblk, b = bi - r * nblk;
     float g = 1.0f, dec = 1.0f;
@@ -122,64 +133,20 @@ __global__ void __launch_bounds__(kPrologueThreads) small_prologue_kernel(
     load_block16(x + static_cast<int64_t>(r) * ld + b * kBlock, v);
     uint32_t codes[2];
     const uint32_t q = quantize_block16(v, g, codes);
-    *reinterpret_cast<uint2*>(xq + static_cast<int64_t>(r) * (H / 2) + b * 8) = make_uint2(codes[0], codes[1]);
-    xsf[static_cast<int64_t>(r) * nblk + b] = static_cast<uint8_t>(q);
+    for (int j = 0; j < top_k; ++j) {
+      const int row = s_row[r * top_k + j];
+      if (row < 0) continue;
+      *reinterpret_cast<uint2*>(aq + static_cast<int64_t>(row) * (H / 2) + b * 8) = make_uint2(codes[0], codes[1]);
+      asf[sf_tile_offset(row, b, kcols_p)] = static_cast<uint8_t>(q);
+    }
     if (b == 0) xs[r] = dec;
   }
-  // (2) plan (the histogram is already in sm.cnt)
-  __syncthreads();
-  scan_padded(sm, El);
-  __syncthreads();
-  for (int l = threadIdx.x; l <= El; l += kPrologueThreads) {
-    padded_offsets[l] = sm.cursor[l];
-    if (l < El) counts[l] = sm.cnt[l];
-  }
-  // -1 on the segments' padding rows; rows past the padded total are never read by the
-  // GEMMs, so (unlike moe_plan's output) this internal row_to_slot leaves them unwritten
-  fill_padding(sm.cursor, sm.cnt, El, sm.cursor[El], sm.cursor[El], row_to_slot);
-  __syncthreads();
-  place_range(ids, id_mask, 0, n, top_k, off, El, sm, row_to_slot, token_to_row, dev_status);
-  for (int s = threadIdx.x; s < n; s += kPrologueThreads) s_row[s] = __ldcg(token_to_row + s);
-  __syncthreads();
-  // (3) permute the routed slots' rows and scale rows; kCopyBatch loads in flight per thread
-  const int cpr = H / 32;  // 16-byte chunks of a quantised row
-  for (int i0 = 0; i0 < n * cpr; i0 += kPrologueThreads * kCopyBatch) {
-    uint4 v[kCopyBatch];
-    int row[kCopyBatch];
-#pragma unroll
-    for (int u = 0; u < kCopyBatch; ++u) {
-      const int i = i0 + u * kPrologueThreads + threadIdx.x;
-      const int s = i / cpr;
-      row[u] = i < n * cpr ? s_row[s] : -1;
-      if (row[u] >= 0)
-        v[u] = __ldcg(reinterpret_cast<const uint4*>(xq + static_cast<int64_t>(s / top_k) * (H / 2)) + (i - s * cpr));
-    }
-#pragma unroll
-    for (int u = 0; u < kCopyBatch; ++u) {
-      const int i = i0 + u * kPrologueThreads + threadIdx.x;
-      if (row[u] >= 0) reinterpret_cast<uint4*>(aq + static_cast<int64_t>(row[u]) * (H / 2))[i - (i / cpr) * cpr] = v[u];
-    }
-  }
-  const int kcols = H / 16;
-  const int kcols_p = static_cast<int>(roundup64(H, kTileK) / 16);
-  const int gpr = kcols_p / 4;  // 4-scale groups of a scale row, K padding included
-  for (int i0 = 0; i0 < n * gpr; i0 += kPrologueThreads * kCopyBatch) {
-    unsigned v[kCopyBatch];
-    int row[kCopyBatch];
-#pragma unroll
-    for (int u = 0; u < kCopyBatch; ++u) {
-      const int i = i0 + u * kPrologueThreads + threadIdx.x;
-      const int s = i / gpr, c4 = i - s * gpr;
-      row[u] = i < n * gpr ? s_row[s] : -1;
-      v[u] = 0u;
-      if (row[u] >= 0 && c4 < kcols / 4)
-        v[u] = __ldcg(reinterpret_cast<const unsigned*>(xsf + static_cast<int64_t>(s / top_k) * kcols) + c4);
-    }
-#pragma unroll
-    for (int u = 0; u < kCopyBatch; ++u) {
-      const int i = i0 + u * kPrologueThreads + threadIdx.x;
-      if (row[u] >= 0) *reinterpret_cast<unsigned*>(asf + sf_tile_offset(row[u], 4 * (i - (i / gpr) * gpr), kcols_p)) = v[u];
-    }
+  // zero scales on the K padding columns of the routed rows (H not a multiple of 256)
+  const int npad = kcols_p - nblk;
+  for (int i = threadIdx.x; i < n * npad; i += kPrologueThreads) {
+    const int s = i / npad;
+    const int row = s_row[s];
+    if (row >= 0) asf[sf_tile_offset(row, nblk + (i - s * npad), kcols_p)] = 0;
   }
   // accumulated output: acc = fp32(out)
   if (acc != nullptr) {
@@ -298,8 +265,8 @@ extern "C" moe_status_t moe_routed_forward(const uint16_t* x, int32_t M, int64_t
     const bool accum = do_finalize == MOE_OUTPUT_ACCUMULATE;
     st = launch_pdl(small_prologue_kernel, dim3(1), dim3(kPrologueThreads), 0, s, x, static_cast<int>(M),
                     static_cast<int>(d.H), ld_x, act_scale_mode == MOE_SCALE_PER_TOKEN ? 1 : 0, topk_ids, id_mask,
-                    static_cast<int>(top_k), static_cast<int>(local_expert_offset), static_cast<int>(d.El), R.cap, xq,
-                    xsf, xs, counts, padded, r2s, token_to_row, dev_status, fb + L.aq, fb + L.asf,
+                    static_cast<int>(top_k), static_cast<int>(local_expert_offset), static_cast<int>(d.El), xs,
+                    counts, padded, r2s, token_to_row, dev_status, fb + L.aq, fb + L.asf,
                     reinterpret_cast<int32_t*>(fb + L.sched), reinterpret_cast<int32_t*>(fb + L.mtd),
                     static_cast<int>(L.cap / kTileM), accum ? static_cast<const uint16_t*>(out) : nullptr,
                     accum ? reinterpret_cast<float*>(fb + L.g) : nullptr);
