@@ -269,6 +269,11 @@ MOE_API moe_status_t moe_prepare_weights(const moe_nvfp4_weights_t* w, void* pre
 /* M * top_k at or below which GEMM1 and GEMM2 run as one chained launch (the GEMM2 tiles of
  * a 128-row tile start as soon as its GEMM1 tiles are written). */
 #define MOE_CHAIN_MAX_SLOTS 2048
+/* Chained batches of at most this many tokens run GEMM1 and GEMM2 with the operands swapped
+ * (the weight tile as the MMA's 128-row operand, each expert's token rows as its 16
+ * columns). A token naming one expert twice (MOE_DEV_DUPLICATE_EXPERT) can give an expert
+ * more than 16 rows; rows past the 16th are then not computed. */
+#define MOE_DECODE_MAX_TOKENS 16
 MOE_API size_t moe_forward_workspace_bytes(int32_t M, int32_t top_k, const moe_nvfp4_weights_t* w,
                                    int32_t do_finalize);
 /* Byte offsets inside the forward workspace of: [0] permuted activations [cap, H/2],

@@ -33,7 +33,7 @@ namespace {
 
 struct Bufs {
   int32_t* sched;
-  int32_t* mtd;
+  int32_t* mtd;  // followed by the expert counters (edone)
   uint8_t *aq, *asf, *iq, *isf;
   uint16_t* g;
 };
@@ -226,7 +226,8 @@ moe_status_t forward_chain(const int32_t* padded_offsets, const int32_t* row_to_
   if ((st = mark(0)) != MOE_OK) return st;
   if (run_permute)
     st = launch_permute(padded_offsets, static_cast<int>(d.El), row_to_slot, top_k, L.cap, xq, xsf,
-                        static_cast<int>(d.H), b.aq, b.asf, b.sched, b.mtd, L.cap / kTileM, accum ? out : nullptr,
+                        static_cast<int>(d.H), b.aq, b.asf, b.sched, b.mtd,
+                        static_cast<int64_t>((L.edone - L.mtd) / 4 + d.El), accum ? out : nullptr,
                         acc, accum ? static_cast<int64_t>(M) * d.H : 0, s);
   if (st != MOE_OK) return st;
   if ((st = mark(1)) != MOE_OK) return st;
@@ -268,7 +269,11 @@ moe_status_t forward_chain(const int32_t* padded_offsets, const int32_t* row_to_
   g2.rsf = routed_scaling_factor;
   g2.dev_status = dev_status;
   g2.tile_counter = b.sched + 1;
-  if (chained) {
+  if (chained && M <= kDecodeMaxTokens) {
+    st = launch_gemm_decode(g1, g2, reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + L.edone), s);
+    if (st != MOE_OK) return st;
+    if ((st = mark(2)) != MOE_OK) return st;
+  } else if (chained) {
     st = launch_gemm_chain(g1, g2, b.mtd, s);
     if (st != MOE_OK) return st;
     if ((st = mark(2)) != MOE_OK) return st;
@@ -363,7 +368,8 @@ extern "C" moe_status_t moe_debug_gemm1(const int32_t* padded_offsets, const int
   const Bufs b = carve(workspace, L);
   const Prepared pw = prepared_ptrs(prepared, prepared_layout(d));
   st = launch_permute(padded_offsets, static_cast<int>(d.El), row_to_slot, top_k, L.cap, xq, xsf,
-                      static_cast<int>(d.H), b.aq, b.asf, b.sched, b.mtd, L.cap / kTileM, nullptr, nullptr, 0, s);
+                      static_cast<int>(d.H), b.aq, b.asf, b.sched, b.mtd,
+                      static_cast<int64_t>((L.edone - L.mtd) / 4 + d.El), nullptr, nullptr, 0, s);
   if (st != MOE_OK) return st;
   GemmLaunch g1 = gemm1_launch(d, L, b, pw, padded_offsets, row_to_slot, xs, top_k, dev_status);
   g1.mode = mode == 0 ? kG1Preact : kG1Act;

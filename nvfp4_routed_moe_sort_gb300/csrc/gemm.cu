@@ -29,6 +29,7 @@
 // TMEM: columns [0, 256) accumulator (two N=128 halves), [256, 448) scale tiles of the four
 // stages (16 columns of A scales + 32 of B scales each). Every wait is bounded.
 #include "gemm_kernel.cuh"
+#include "gemm_decode.cuh"
 
 namespace moe {
 namespace {
@@ -154,6 +155,50 @@ moe_status_t launch_gemm_chain(const GemmLaunch& g1, const GemmLaunch& g2, int32
   const int mode = g2.mode == kG2Reduce ? kChainReduce : kChainRows;
   const int64_t units_max = (g1.cap / kTileM) * (prm.ph[0].n_tiles + prm.ph[1].n_tiles);
   return dispatch(mode, g1.act, prm, units_max, smem_bytes(g1.El, prm.sparse), s);
+}
+
+moe_status_t launch_gemm_decode(const GemmLaunch& g1, const GemmLaunch& g2, int32_t* e_done, cudaStream_t s) {
+  if (g1.cap == 0) return MOE_OK;
+  dgemm::Params prm;
+  memset(&prm, 0, sizeof(prm));
+  const GemmLaunch* gs[2] = {&g1, &g2};
+  for (int i = 0; i < 2; ++i) {
+    const GemmLaunch& g = *gs[i];
+    dgemm::Phase& ph = prm.ph[i];
+    if (!encode_rows(&ph.tmap_w, g.b, g.K / 2, g.El * g.Np, kTileN)) return MOE_ERR_CUDA;
+    if (!encode_rows(&ph.tmap_x, g.a, g.K / 2, g.cap, dgemm::kTokens)) return MOE_ERR_CUDA;
+    ph.w_raw = g.b;
+    ph.sfw = g.b_sf;
+    ph.sfx = g.a_sf;
+    ph.alpha = g.alpha;
+    ph.alpha_gate = g.alpha_gate;
+    ph.out = g.out;
+    ph.out_sf = g.out_sf;
+    ph.K = static_cast<int32_t>(g.K);
+    ph.Kp = static_cast<int32_t>(g.Kp);
+    ph.nkb = static_cast<int32_t>(g.Kp / kTileK);
+    ph.Nw = static_cast<int32_t>(g.N);
+    ph.Nwp = static_cast<int32_t>(g.Np);
+    ph.n_tiles = static_cast<int32_t>(g.Np / kTileN);
+  }
+  prm.padded_offsets = g1.padded_offsets;
+  prm.row_to_slot = g1.row_to_slot;
+  prm.xs = g1.xs;
+  prm.dev_status = g1.dev_status;
+  prm.tile_counter = g1.tile_counter;
+  prm.e_done = e_done;
+  prm.El = static_cast<int32_t>(g1.El);
+  prm.top_k = g1.top_k;
+  prm.inter = g1.inter;
+  prm.g2 = g1.g2;
+  prm.route_w = g2.route_w;
+  prm.route_w_dtype = g2.route_w_dtype;
+  prm.rsf = g2.rsf;
+  const size_t smem = static_cast<size_t>(dgemm::kStages) * dgemm::kStageBytes + dgemm::kSmemExtra +
+                      roundup64(g1.El + 1, 4) * 4 + g1.El * 4;
+  const int64_t units_max = g1.El * (prm.ph[0].n_tiles + prm.ph[1].n_tiles);
+  const int grid = static_cast<int>(units_max < num_sms() ? units_max : num_sms());
+  return dgemm::launch_act(g2.mode == kG2Rows, g1.act, prm, grid, smem, s);
 }
 
 }  // namespace moe

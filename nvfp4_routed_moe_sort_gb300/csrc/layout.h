@@ -67,7 +67,7 @@ inline PreparedLayout prepared_layout(const Dims& d) {
 // intermediate [cap, I/2] + scale tiles [cap/128][Ip/64][512], and the BF16 expert rows
 // [cap, H] (finalized output) or the FP32 accumulator [M, H] (accumulated output).
 struct WorkspaceLayout {
-  size_t sched, mtd, aq, asf, iq, isf, g, total;
+  size_t sched, mtd, edone, aq, asf, iq, isf, g, total;
   int64_t cap;
 };
 
@@ -83,6 +83,7 @@ inline WorkspaceLayout workspace_layout(const Dims& d, int64_t M, int64_t top_k,
   size_t c = 0;
   L.sched = take(c, 256);  // GEMM tile counters, zeroed by the permute kernel
   L.mtd = take(c, (L.cap / kTileM) * 4);  // per-row-tile GEMM1 completion counts (chained GEMMs), zeroed too
+  L.edone = take(c, d.El * 4);            // per-expert GEMM1 completion counts (decode GEMMs), zeroed too
   L.aq = take(c, L.cap * d.H / 2);
   L.asf = take(c, L.cap * d.Hp / 16);
   L.iq = take(c, L.cap * d.I / 2);
@@ -109,6 +110,9 @@ enum GemmMode : int {
 // GEMM2 tiles of a row tile start once its GEMM1 tiles are written, so the second weight
 // stream overlaps the first GEMM's tail instead of waiting for a kernel boundary.
 constexpr int64_t kChainMaxSlots = MOE_CHAIN_MAX_SLOTS;
+// Chained batches of at most this many tokens (so at most 16 rows per expert) run the
+// decode-shaped GEMMs: the weight tile is the MMA's M operand, the expert's rows its N = 16.
+constexpr int64_t kDecodeMaxTokens = MOE_DECODE_MAX_TOKENS;
 
 struct GemmLaunch {
   int mode;
@@ -140,10 +144,14 @@ moe_status_t launch_gemm(const GemmLaunch& g, cudaStream_t s);
 // GEMM1 (g1, kG1Fused) and GEMM2 (g2, kG2Rows or kG2Reduce) in one launch; mt_done holds
 // cap / 128 zeroed counters
 moe_status_t launch_gemm_chain(const GemmLaunch& g1, const GemmLaunch& g2, int32_t* mt_done, cudaStream_t s);
+// the same with the decode-shaped kernel (at most 16 rows per expert); e_done holds E_local
+// zeroed counters
+moe_status_t launch_gemm_decode(const GemmLaunch& g1, const GemmLaunch& g2, int32_t* e_done, cudaStream_t s);
 moe_status_t launch_permute(const int32_t* padded_offsets, int El, const int32_t* row_to_slot, int top_k,
                             int64_t cap, const uint8_t* xq, const uint8_t* xsf, int H, uint8_t* aq, uint8_t* asf,
                             int32_t* tile_counters, int32_t* mt_done, int64_t n_mt, const uint16_t* acc_init,
                             float* acc, int64_t acc_elems, cudaStream_t s);
+// (mt_done: the row-tile and expert counters of one workspace, contiguous, n_mt ints)
 moe_status_t launch_finalize(const uint16_t* rows, const void* topk_weights, int weights_dtype, float rsf,
                              const int32_t* token_to_row, int M, int top_k, int H, uint16_t* out, cudaStream_t s);
 moe_status_t launch_store_acc(const float* acc, int64_t elems, uint16_t* out, cudaStream_t s);

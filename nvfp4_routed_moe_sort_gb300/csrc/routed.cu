@@ -268,7 +268,7 @@ extern "C" moe_status_t moe_routed_forward(const uint16_t* x, int32_t M, int64_t
                     static_cast<int>(top_k), static_cast<int>(local_expert_offset), static_cast<int>(d.El), xs,
                     counts, padded, r2s, token_to_row, dev_status, fb + L.aq, fb + L.asf,
                     reinterpret_cast<int32_t*>(fb + L.sched), reinterpret_cast<int32_t*>(fb + L.mtd),
-                    static_cast<int>(L.cap / kTileM), accum ? static_cast<const uint16_t*>(out) : nullptr,
+                    static_cast<int>((L.edone - L.mtd) / 4 + d.El), accum ? static_cast<const uint16_t*>(out) : nullptr,
                     accum ? reinterpret_cast<float*>(fb + L.g) : nullptr);
     if (st != MOE_OK) return st;
   } else {

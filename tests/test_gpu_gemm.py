@@ -25,6 +25,10 @@ SMALL = {
     "relu2_ep_small": mi.MoEConfig("relu2_ep_small", M=513, H=256, I=384, E=12, top_k=3, act="relu2",
                                    seed=13, weight_seed=13, local_offset=4, num_local=6),
     "decode_t8": mi.CONFIGS["decode_t8"],
+    # decode-shaped GEMMs (at most 16 tokens): experts with many rows (up to 16), K tails
+    "decode_dense": mi.MoEConfig("decode_dense", M=16, H=384, I=256, E=4, top_k=3, seed=14, weight_seed=14),
+    "relu2_decode": mi.MoEConfig("relu2_decode", M=13, H=512, I=384, E=10, top_k=4, act="relu2", seed=15,
+                                 weight_seed=15, local_offset=2, num_local=6),
 }
 
 
