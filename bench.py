@@ -6,8 +6,9 @@
 One step = one pass of the whole hot path over one batch: moe_quantize_input,
 moe_plan and moe_grouped_fp4_forward (permute, GEMM1 + SwiGLU/ReLU^2 + NVFP4
 requant, GEMM2, finalize). Inputs (BF16 hidden states, routing) and the prepared
-NVFP4 weights are resident in HBM; L2 is flushed between steps (a 256 MB write
-outside the timed events). Rank 0 prints one JSON line.
+NVFP4 weights are resident in HBM; L2 is flushed between steps outside the timed events
+(a 256 MB write, then a 256 MB read of a second buffer so the lines left in L2 are clean;
+`--l2-flush write` skips the read). Rank 0 prints one JSON line.
 
 --impl reference times the CPU oracle (oracle/) on the machine's host cores on a
 bounded sample of the same workload (this repository's reference arm).
@@ -166,23 +167,46 @@ def setup_gpu(cfg, dev):
     return layer, x, ids, tw
 
 
+def kernel_source_hash() -> str:
+    """sha256 prefix of the GEMM kernel sources (gemm_kernel.cuh, gemm_decode.cuh, common.cuh)."""
+    csrc = os.path.join(ROOT, "nvfp4_routed_moe_sort_gb300", "csrc")
+    data = b"".join(open(os.path.join(csrc, f), "rb").read()
+                    for f in ("gemm_kernel.cuh", "gemm_decode.cuh", "common.cuh"))
+    return hashlib.sha256(data).hexdigest()[:16]
+
+
 def traffic_from_profiles(kernel: str, workload: str):
     """DRAM bytes per launch of `kernel` from the committed ncu summary
     (profiles/dram_traffic.txt), or None when the kernel's source has changed since the
-    counters were taken (sha256 of gemm_kernel.cuh followed by common.cuh)."""
+    counters were taken (kernel_source_hash)."""
     kernel = {"gemm1+gemm2 (chained)": "gemm_chained"}.get(kernel, kernel)
     p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(p):
         return None
-    csrc = os.path.join(ROOT, "nvfp4_routed_moe_sort_gb300", "csrc")
-    h = hashlib.sha256(open(os.path.join(csrc, "gemm_kernel.cuh"), "rb").read()
-                       + open(os.path.join(csrc, "common.cuh"), "rb").read()).hexdigest()[:16]
+    h = kernel_source_hash()
     with open(p) as f:
         for ln in f:
             parts = ln.split()
             if len(parts) == 5 and not ln.startswith("#") and parts[0] == workload and parts[1] == kernel:
                 return int(parts[2]) if parts[4] == h else None
     return None
+
+
+class L2Flush:
+    """Evicts the step's data from the 129 MB L2 between steps: a 256 MB write and, unless
+    write-only, a 256 MB read of a second buffer, so that the lines left in L2 are clean
+    and the timed step does not pay for writing the flush buffer back."""
+
+    def __init__(self, dev, clean: bool):
+        import torch
+        self.w = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(256 << 20, dtype=torch.uint8, device=dev).view(torch.int64) if clean else None
+        self.sink = None
+
+    def __call__(self):
+        self.w.zero_()
+        if self.r is not None:
+            self.sink = self.r.sum()
 
 
 def run_gpu(args, cfg, rank, world):
@@ -200,14 +224,14 @@ def run_gpu(args, cfg, rank, world):
     b = layer.routed_buffers(M, k, mode)
     # accumulated output: every step adds into this caller-owned tensor
     acc_out = torch.zeros(M, cfg.H, dtype=torch.bfloat16, device=dev) if mode == 2 else None
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev, clean=args.l2_flush == "write+read")
     n_ev = 5
     K, W = args.steps, args.warmup
 
     # the timed step: one CUDA-graph replay of the whole path
     graph = layer.capture(x, ids_t, tw_t, mode, out=acc_out)
     for i in range(W):
-        flush.zero_()
+        flush()
         graph.replay()
     torch.cuda.synchronize()
     if world > 1:
@@ -219,7 +243,7 @@ def run_gpu(args, cfg, rank, world):
     t0 = time.perf_counter()
     step_times = []
     for i in range(K):
-        flush.zero_()
+        flush()
         s_ev.record()
         graph.replay()
         e_ev.record()
@@ -237,12 +261,12 @@ def run_gpu(args, cfg, rank, world):
         for e in row:
             e.record()
     for _ in range(W):
-        flush.zero_()
+        flush()
         layer.forward(x, ids_t, tw_t, mode, out=acc_out)
     torch.cuda.synchronize()
     torch.cuda._sleep(int(60e6))   # ~30 ms at 2 GHz
     for e in evs:
-        flush.zero_()
+        flush()
         layer.routed(x, ids_t, tw_t, b, mode, step_events=e, out=acc_out)
     torch.cuda.synchronize()
     kern_times = [[e[j].elapsed_time(e[j + 1]) for j in range(n_ev - 1)] for e in evs]
@@ -284,7 +308,18 @@ def run_gpu(args, cfg, rank, world):
     roof["traffic"] = traffic_from_profiles(dom, cfg.name)
     step_roof_s = max(stepw["bytes"] / (peaks["hbm_gbs"] * 1e9), stepw["flops"] / (fp4_peak * 1e12))
     # end to end through the public API with host buffers
-    e2e = None if args.no_e2e else run_e2e(layer, x, ids, tw, dev, max(3, min(K, 50)))
+    e2e = None if args.no_e2e else run_e2e(layer, x, ids, tw, dev, max(3, min(K, 50)), flush)
+    # the same graph with a write-only flush (its dirty lines are written back during the step)
+    wo = L2Flush(dev, clean=False)
+    wo_times = []
+    for i in range(min(K, 50)):
+        wo()
+        s_ev.record()
+        graph.replay()
+        e_ev.record()
+        e_ev.synchronize()
+        wo_times.append(s_ev.elapsed_time(e_ev))
+    del wo
     small = M * k <= 2048 and M * cfg.H <= (1 << 17)
     launches_per_step = (3 if small else 5) + (2 if M * k > 2048 else 0) + (0 if M * k <= 2048 else 1)
     res = {
@@ -293,7 +328,8 @@ def run_gpu(args, cfg, rank, world):
         "dtype": "nvfp4 (e2m1 x e2m1, e4m3 block scales, fp32 accumulate)", "data": "synthetic",
         "config": {"workload": workload_name(cfg), "tokens": M, "hidden": cfg.H, "inter": cfg.I,
                    "experts": cfg.E, "top_k": k, "routed_rows": R, "active_experts": active,
-                   "l2": "flushed between steps (256 MB write outside the timed events)",
+                   "l2": ("flushed between steps outside the timed events: 256 MB write"
+                          + (", then 256 MB read of a second buffer (clean lines)" if flush.r is not None else "")),
                    "output": args.output,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roof,
@@ -305,6 +341,7 @@ def run_gpu(args, cfg, rank, world):
                   "queued behind a device sleep so no host gap is timed; "
                   f"an eager step takes {eager_ms:.4f} ms",
         "eager_ms_per_step": eager_ms,
+        "write_only_flush_ms_per_step": float(np.mean(wo_times)),
         "e2e": e2e,
         "gpu_launches": launches_per_step * K,
         "clocks": clk,
@@ -313,7 +350,7 @@ def run_gpu(args, cfg, rank, world):
     return res
 
 
-def run_e2e(layer, x, ids, tw, dev, steps):
+def run_e2e(layer, x, ids, tw, dev, steps, flush):
     """Host buffers in, host buffer out: pinned H2D copies of the step's inputs, the layer's
     captured graph (NVFP4RoutedMoE.capture), and the D2H copy of the output, all timed."""
     import torch
@@ -330,10 +367,9 @@ def run_e2e(layer, x, ids, tw, dev, steps):
     dtw.copy_(htw)
     graph = layer.capture(dx, did, dtw, True)
     out = layer.routed_buffers(M, k, True)["out"]
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     times = []
     for i in range(steps + 3):
-        flush.zero_()
+        flush()
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s.record()
         dx.copy_(hx, non_blocking=True)
@@ -465,6 +501,8 @@ def main():
     ap.add_argument("--workload", default="decode_t8", choices=sorted(mi.CONFIGS))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--l2-flush", default="write+read", choices=["write+read", "write"],
+                    help="between steps: a 256 MB write, then (default) a 256 MB read leaving clean lines")
     ap.add_argument("--output", default="finalized", choices=sorted(OUTPUT_MODES),
                     help="finalized: ordered combine into a fresh out; accumulate: FP32 reduction into out")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer run (profiling)")

@@ -273,9 +273,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm_kernel(const __grid_c
         const uint8_t* sfw0 = ph.sfw + (static_cast<int64_t>(e) * (ph.Nwp >> 7) + nt * 2) * kt * 512;
         const uint8_t* sfw1 = sfw0 + kt * 512;
         const uint8_t* sfx = ph.sfx + static_cast<int64_t>(seg >> 7) * kt * 512;
-        if (second) {
-          // the weight tile does not depend on GEMM1: start it towards L2, then wait until
-          // every GEMM1 unit of this expert has written its rows
+        // A GEMM2 unit depends on every GEMM1 unit of its expert, its weights do not. When
+        // the unit fits in the pipeline, its weight tiles are loaded first, then the wait,
+        // then the token rows (each stage's barrier expects both parts); otherwise the
+        // weight tile is started towards L2 before the wait.
+        int pre = 0;
+        uint32_t pre_stage = stage;
+        if (second && ph.nkb > kStages) {
           prefetch_l2(ph.w_raw + static_cast<int64_t>(wrow0) * (ph.K / 2), static_cast<int64_t>(256) * (ph.K / 2));
           prefetch_l2(sfw0, 2 * kt * 512);
           if (!wait_counter(p.e_done + e, kEpiWarps * p.ph[0].n_tiles, abort_flag, p.dev_status)) {
@@ -283,8 +287,33 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm_kernel(const __grid_c
             break;
           }
           fence_proxy_async_global();  // the TMA reads below follow the observed generic writes
+        } else if (second) {
+          pre = ph.nkb;
+          for (int kb = 0; kb < pre; ++kb) {
+            if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.dev_status)) { ok = false; break; }
+            uint8_t* st = smem + stage * kStageBytes;
+            mbar_arrive_expect_tx(&full[stage], kStageBytes);
+            tma_load_2d(st, &ph.tmap_w, kb * 128, wrow0, &full[stage]);
+            bulk_load(st + kOffSfw, sfw0 + kb * 2048, 2048, &full[stage]);
+            bulk_load(st + kOffSfw + 2048, sfw1 + kb * 2048, 2048, &full[stage]);
+            issued_mask |= 1u << stage;
+            issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+            if (++stage == kStages) { stage = 0; phase ^= 1; }
+          }
+          if (!ok) break;
+          if (!wait_counter(p.e_done + e, kEpiWarps * p.ph[0].n_tiles, abort_flag, p.dev_status)) {
+            ok = false;
+            break;
+          }
+          fence_proxy_async_global();  // the TMA reads below follow the observed generic writes
+          for (int kb = 0; kb < pre; ++kb) {
+            uint8_t* st = smem + pre_stage * kStageBytes;
+            tma_load_2d(st + kOffX, &ph.tmap_x, kb * 128, seg, &full[pre_stage]);
+            bulk_load(st + kOffSfx, sfx + kb * 2048, 2048, &full[pre_stage]);
+            if (++pre_stage == kStages) pre_stage = 0;
+          }
         }
-        for (int kb = 0; kb < ph.nkb; ++kb) {
+        for (int kb = pre; kb < ph.nkb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.dev_status)) { ok = false; break; }
           uint8_t* st = smem + stage * kStageBytes;
           mbar_arrive_expect_tx(&full[stage], kStageBytes);
