@@ -321,7 +321,12 @@ def run_gpu(args, cfg, rank, world):
         wo_times.append(s_ev.elapsed_time(e_ev))
     del wo
     small = M * k <= 2048 and M * cfg.H <= (1 << 17)
-    launches_per_step = (3 if small else 5) + (2 if M * k > 2048 else 0) + (0 if M * k <= 2048 else 1)
+    # small: prologue, chained GEMMs, combine; otherwise quantise, plan (1 or 3), permute,
+    # GEMM1 + GEMM2 (one chained launch up to 2048 slots), combine
+    if small:
+        launches_per_step = 3
+    else:
+        launches_per_step = 5 + (2 if M * k > 2048 else 0) + (0 if M * k <= 2048 else 1)
     res = {
         "metric": METRIC, "value": world * M / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,

@@ -118,8 +118,10 @@ def test_forward_matches_oracle(name, do_finalize):
         assert_close_output(bf16_np(g2)[real], ref["rows"][real], name + " rows")
 
 
-@pytest.mark.parametrize("name", ["swiglu_ragged", "relu2_ep_small"])
+@pytest.mark.parametrize("name", ["swiglu_ragged", "relu2_ep_small", "decode_t8", "decode_dense", "relu2_decode"])
 def test_finalize_of_unfinalized_equals_finalized(name):
+    # decode-sized batches combine inside the GEMM launch; the standalone combine of their
+    # unfinalized rows must give the same bytes
     p = Problem(SMALL[name])
     cfg = p.cfg
     fin = bf16_np(p.run(True)).copy()
