@@ -11,9 +11,9 @@
 // quantiser, the plan and the permutation in one kernel of one 1024-thread CTA, and GEMM1
 // and GEMM2 as one chained launch, so the step is three launches (prologue, GEMMs, combine)
 // instead of six; each of those steps is latency-bound at these sizes. Larger batches run the separate kernels of
-// moe_quantize_input, moe_plan and moe_grouped_fp4_forward. Both paths compute the same
-// bytes: the prologue's quantiser and plan follow the same arithmetic and order as the
-// separate kernels.
+// moe_plan, a quantiser that stores straight into the plan rows, and the GEMMs and combine
+// of moe_grouped_fp4_forward. Both paths compute the same bytes as the separate calls: the
+// quantisers and the plan follow the same arithmetic and order as the separate kernels.
 #include <math.h>
 
 #include "common.cuh"
@@ -162,6 +162,79 @@ __global__ void __launch_bounds__(kPrologueThreads) small_prologue_kernel(
   }
 }
 
+// Larger batches, after the plan: one warp per token computes its scale (per-token max |x|
+// over the row, then the row is read again from L1/L2), quantises each 16-value block once
+// (the arithmetic of quantize_rows_kernel) and stores its codes and scale straight into
+// every plan row of the token, so the quantised activations are never written token-major
+// and read back by a permutation. Block 0 zeroes the GEMM counters; an accumulated output's
+// FP32 copy of out is made by all threads.
+__global__ void __launch_bounds__(256) quantize_scatter_kernel(
+    const uint16_t* __restrict__ x, int M, int H, int64_t ld, int per_token, int top_k,
+    const int32_t* __restrict__ token_to_row, float* __restrict__ xs, uint8_t* __restrict__ aq,
+    uint8_t* __restrict__ asf, int32_t* __restrict__ counters, int n_counters, const uint16_t* __restrict__ acc_init,
+    float* __restrict__ acc) {
+  pdl_trigger();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < n_counters; i += blockDim.x) counters[i] = 0;
+  const int nblk = H / kBlock;
+  const int kcols_p = static_cast<int>(roundup64(H, kTileK) / 16);
+  for (int64_t t = warp0; t < M; t += nwarps) {
+    const uint16_t* row = x + t * ld;
+    float g = 1.0f, dec = 1.0f;
+    if (per_token) {
+      float amax = 0.0f;
+      for (int b = lane; b < nblk; b += 32) {
+        float v[16];
+        load_block16(row + b * kBlock, v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
+      }
+      amax = warp_max(amax);
+      if (amax > 0.0f) {
+        g = __fdiv_rn(kGlobalNumerator, amax);
+        dec = __fdiv_rn(amax, kGlobalNumerator);
+      }
+    }
+    // the token's plan rows (lane j holds slot j's row)
+    const int my_row = lane < top_k ? token_to_row[t * top_k + lane] : -1;
+    for (int b = lane; b < nblk; b += 32) {
+      float v[16];
+      load_block16(row + b * kBlock, v);
+      uint32_t codes[2];
+      const uint32_t q = quantize_block16(v, g, codes);
+      for (int j = 0; j < top_k; ++j) {
+        const int prow = j < 32 ? __shfl_sync(0xffffffffu, my_row, j) : token_to_row[t * top_k + j];
+        if (prow < 0) continue;
+        *reinterpret_cast<uint2*>(aq + static_cast<int64_t>(prow) * (H / 2) + b * 8) = make_uint2(codes[0], codes[1]);
+        asf[sf_tile_offset(prow, b, kcols_p)] = static_cast<uint8_t>(q);
+      }
+    }
+    // scale columns of the K padding (H not a multiple of 256) are zero
+    for (int c = nblk + lane; c < kcols_p; c += 32)
+      for (int j = 0; j < top_k; ++j) {
+        const int prow = token_to_row[t * top_k + j];
+        if (prow >= 0) asf[sf_tile_offset(prow, c, kcols_p)] = 0;
+      }
+    if (lane == 0) xs[t] = dec;
+  }
+  if (acc != nullptr) {
+    const int64_t n8 = static_cast<int64_t>(M) * H / 8;
+    const int64_t nth = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8; i += nth) {
+      const uint4 v = reinterpret_cast<const uint4*>(acc_init)[i];
+      float4* d = reinterpret_cast<float4*>(acc) + 2 * i;
+      d[0] = make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u), __uint_as_float(v.y << 16),
+                         __uint_as_float(v.y & 0xFFFF0000u));
+      d[1] = make_float4(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xFFFF0000u), __uint_as_float(v.w << 16),
+                         __uint_as_float(v.w & 0xFFFF0000u));
+    }
+  }
+}
+
 moe_status_t record_mark(void* ev, cudaStream_t s) {
   cudaStreamCaptureStatus capturing = cudaStreamCaptureStatusNone;
   MOE_CUDA(cudaStreamIsCapturing(s, &capturing));
@@ -272,14 +345,26 @@ extern "C" moe_status_t moe_routed_forward(const uint16_t* x, int32_t M, int64_t
                     accum ? reinterpret_cast<float*>(fb + L.g) : nullptr);
     if (st != MOE_OK) return st;
   } else {
-    st = moe_quantize_input(x, M, static_cast<int32_t>(d.H), ld_x, act_scale_mode, xq, xsf, xs, stream);
-    if (st != MOE_OK) return st;
+    // the plan, then the quantiser storing straight into the plan rows (no permute launch)
     st = moe_plan(topk_ids, topk_ids_format, M, top_k, num_experts, local_expert_offset,
                   static_cast<int32_t>(d.El), counts, padded, r2s, token_to_row, b + R.plan_ws,
                   moe_plan_workspace_bytes(M, top_k, static_cast<int32_t>(d.El)), dev_status, stream);
     if (st != MOE_OK) return st;
+    const WorkspaceLayout L = workspace_layout(d, M, top_k, do_finalize);
+    uint8_t* fb = static_cast<uint8_t*>(fwd);
+    const bool accum = do_finalize == MOE_OUTPUT_ACCUMULATE;
+    const int64_t blocks = (static_cast<int64_t>(M) + 7) / 8;  // 8 warps (tokens) per block
+    const int64_t max_blocks = static_cast<int64_t>(num_sms()) * 16;
+    st = launch_pdl(quantize_scatter_kernel, dim3(static_cast<unsigned>(blocks < max_blocks ? blocks : max_blocks)),
+                    dim3(256), 0, s, x, static_cast<int>(M), static_cast<int>(d.H), ld_x,
+                    act_scale_mode == MOE_SCALE_PER_TOKEN ? 1 : 0, static_cast<int>(top_k),
+                    static_cast<const int32_t*>(token_to_row), xs, fb + L.aq, fb + L.asf,
+                    reinterpret_cast<int32_t*>(fb + L.sched),
+                    static_cast<int>((L.edone - L.sched) / 4 + d.El), accum ? static_cast<const uint16_t*>(out) : nullptr,
+                    accum ? reinterpret_cast<float*>(fb + L.g) : nullptr);
+    if (st != MOE_OK) return st;
   }
   return forward_chain(padded, r2s, token_to_row, M, top_k, xq, xsf, xs, w, prepared, topk_weights,
                        topk_weights_dtype, routed_scaling_factor, fc2_input_scale, do_finalize, out, gemm2_out, fwd,
-                       dev_status, num_step_events == 5 ? fwd_events : nullptr, num_step_events, !small, s);
+                       dev_status, num_step_events == 5 ? fwd_events : nullptr, num_step_events, false, s);
 }
