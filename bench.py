@@ -179,7 +179,7 @@ def traffic_from_profiles(kernel: str, workload: str):
     """DRAM bytes per launch of `kernel` from the committed ncu summary
     (profiles/dram_traffic.txt), or None when the kernel's source has changed since the
     counters were taken (kernel_source_hash)."""
-    kernel = {"gemm1+gemm2 (chained)": "gemm_chained"}.get(kernel, kernel)
+    kernel = {"gemm1+gemm2 (chained)": "gemm_chained", "gemm1+gemm2 (decode)": "gemm_decode"}.get(kernel, kernel)
     p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(p):
         return None
@@ -284,10 +284,11 @@ def run_gpu(args, cfg, rank, world):
     work, stepw, R, active = kernel_work(cfg, ids)
     kern_ms = {n: float(np.mean(v)) for n, v in per.items()}
     if M * k <= 2048:
-        # GEMM1 and GEMM2 run as one chained launch (its time is the gemm1 interval)
-        kern_ms["gemm1+gemm2 (chained)"] = kern_ms.pop("gemm1") + kern_ms.pop("gemm2")
-        work["gemm1+gemm2 (chained)"] = {key: work["gemm1"][key] + work["gemm2"][key] for key in ("bytes", "flops")}
-        dom = "gemm1+gemm2 (chained)"
+        # GEMM1 and GEMM2 run as one launch (its time is the gemm1 interval): the decode
+        # kernel (weights as the 128-row MMA operand) up to 16 tokens, else the chained one
+        dom = "gemm1+gemm2 (decode)" if M <= 16 else "gemm1+gemm2 (chained)"
+        kern_ms[dom] = kern_ms.pop("gemm1") + kern_ms.pop("gemm2")
+        work[dom] = {key: work["gemm1"][key] + work["gemm2"][key] for key in ("bytes", "flops")}
     else:
         dom = max(["gemm1", "gemm2"], key=lambda n: kern_ms[n])
     peaks = load_peaks()

@@ -314,7 +314,7 @@ MOE_API moe_status_t moe_finalize(const uint16_t* gemm2_out, const void* topk_we
  * exactly what moe_quantize_input, moe_plan and moe_grouped_fp4_forward compute in sequence
  * (bit for bit, except the order of the FP32 additions of MOE_OUTPUT_ACCUMULATE). For small
  * batches (M * top_k <= 2048 and M * H <= 131072) the quantiser, the plan and the
- * permutation run as one kernel of one CTA.
+ * permutation run as one kernel.
  *   x             [M, ld_x] BF16 hidden states (first H columns used), ld_x >= H, ld_x % 8 == 0
  *   act_scale_mode  moe_act_scale_t, as moe_quantize_input
  *   topk_ids, topk_ids_format, num_experts, local_expert_offset  as moe_plan
@@ -354,6 +354,18 @@ MOE_API moe_status_t moe_debug_gemm1(const int32_t* padded_offsets, const int32_
                              const moe_nvfp4_weights_t* w, const void* prepared,
                              size_t prepared_bytes, int32_t mode, void* dbg_out, void* workspace,
                              size_t workspace_bytes, int32_t* dev_status, moe_stream_t stream);
+
+/* ----------------------------------------------------------------------------------------
+ * Test hook of the decode GEMM's scheduling (the one-call path, at most 16 tokens): each CTA
+ * loads its first unit's weight stages before waiting for the prologue, guessing the expert
+ * from the routing ids, and takes that unit through an ownership flag; the results never
+ * depend on either. flags = 0 (the default) leaves the scheduling alone; bit 0 makes every
+ * guess wrong (the next routed expert), so the stages are reloaded; bit 1 makes the odd CTAs
+ * leave their first unit untaken, so other CTAs take it before any GEMM2 unit. Applies to
+ * launches made after the call (a captured graph keeps the flags it was captured with).
+ * Process-wide; not thread-safe. Returns the previous flags.
+ * ---------------------------------------------------------------------------------------- */
+MOE_API int32_t moe_debug_set_decode_hooks(int32_t flags);
 
 #ifdef __cplusplus
 }

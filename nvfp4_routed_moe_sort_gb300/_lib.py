@@ -29,7 +29,7 @@ EXPORTED = [
     "moe_plan_workspace_bytes", "moe_plan", "moe_quantize_weights", "moe_prepared_weights_bytes",
     "moe_prepare_weights", "moe_forward_workspace_bytes", "moe_forward_workspace_layout",
     "moe_grouped_fp4_forward", "moe_finalize", "moe_debug_gemm1", "moe_plan_noalloc",
-    "moe_routed_forward_workspace_bytes", "moe_routed_forward",
+    "moe_routed_forward_workspace_bytes", "moe_routed_forward", "moe_debug_set_decode_hooks",
 ]
 MOE_PLAN_NOALLOC_SCRATCH_BYTES = 1 << 20
 
@@ -76,6 +76,7 @@ def _declare(lib):
                                          P, P, P, P, c_size_t, P, ctypes.POINTER(c_void_p), c_int32, P]),
         "moe_debug_gemm1": (c_int32, [P, P, c_int32, c_int32, P, P, P, ctypes.POINTER(WeightsT), P,
                                       c_size_t, c_int32, P, P, c_size_t, P, P]),
+        "moe_debug_set_decode_hooks": (c_int32, [c_int32]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -255,6 +256,12 @@ def moe_finalize(gemm2_out, topk_weights, token_to_row, out, stream=None, routed
     _check(lib().moe_finalize(_ptr(gemm2_out), _ptr(topk_weights), _weights_dtype(topk_weights),
                               float(routed_scaling_factor), _ptr(token_to_row), M, k, H, _ptr(out),
                               _stream(stream)), "moe_finalize")
+
+
+def moe_debug_set_decode_hooks(flags: int) -> int:
+    """Test hook of the decode GEMM's scheduling (bit 0: wrong expert guesses, bit 1: odd CTAs
+    leave their first unit to others); returns the previous flags."""
+    return int(lib().moe_debug_set_decode_hooks(int(flags)))
 
 
 def moe_debug_gemm1(padded_offsets, row_to_slot, M, top_k, xq, xsf, xs, w: WeightsT, prepared, mode,

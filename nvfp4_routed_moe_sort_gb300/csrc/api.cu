@@ -200,7 +200,7 @@ moe_status_t forward_chain(const int32_t* padded_offsets, const int32_t* row_to_
                            int32_t topk_weights_dtype, float routed_scaling_factor, float fc2_input_scale,
                            int32_t do_finalize, uint16_t* out, uint16_t* gemm2_out, void* workspace,
                            int32_t* dev_status, void* const* step_events, int32_t num_step_events, bool run_permute,
-                           cudaStream_t s) {
+                           const RoutingHint& hint, cudaStream_t s) {
   const Dims d = make_dims(w);
   const bool fin = do_finalize == MOE_OUTPUT_FINALIZED;
   const bool accum = do_finalize == MOE_OUTPUT_ACCUMULATE;
@@ -226,8 +226,7 @@ moe_status_t forward_chain(const int32_t* padded_offsets, const int32_t* row_to_
   if ((st = mark(0)) != MOE_OK) return st;
   if (run_permute)
     st = launch_permute(padded_offsets, static_cast<int>(d.El), row_to_slot, top_k, L.cap, xq, xsf,
-                        static_cast<int>(d.H), b.aq, b.asf, b.sched, b.mtd,
-                        static_cast<int64_t>((L.edone - L.mtd) / 4 + d.El), accum ? out : nullptr,
+                        static_cast<int>(d.H), b.aq, b.asf, b.sched, b.mtd, counter_ints(L, L.mtd), accum ? out : nullptr,
                         acc, accum ? static_cast<int64_t>(M) * d.H : 0, s);
   if (st != MOE_OK) return st;
   if ((st = mark(1)) != MOE_OK) return st;
@@ -270,7 +269,8 @@ moe_status_t forward_chain(const int32_t* padded_offsets, const int32_t* row_to_
   g2.dev_status = dev_status;
   g2.tile_counter = b.sched + 1;
   if (chained && M <= kDecodeMaxTokens) {
-    st = launch_gemm_decode(g1, g2, reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + L.edone), s);
+    st = launch_gemm_decode(g1, g2, reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + L.edone),
+                            reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + L.own), hint, s);
     if (st != MOE_OK) return st;
     if ((st = mark(2)) != MOE_OK) return st;
   } else if (chained) {
@@ -345,7 +345,8 @@ extern "C" moe_status_t moe_grouped_fp4_forward(const int32_t* padded_offsets, c
   }
   return forward_chain(padded_offsets, row_to_slot, token_to_row, M, top_k, xq, xsf, xs, w, prepared, topk_weights,
                        topk_weights_dtype, routed_scaling_factor, fc2_input_scale, do_finalize, out, gemm2_out,
-                       workspace, dev_status, step_events, num_step_events, true, as_stream(stream));
+                       workspace, dev_status, step_events, num_step_events, true, RoutingHint(),
+                       as_stream(stream));
 }
 
 extern "C" moe_status_t moe_debug_gemm1(const int32_t* padded_offsets, const int32_t* row_to_slot, int32_t M,
@@ -368,8 +369,8 @@ extern "C" moe_status_t moe_debug_gemm1(const int32_t* padded_offsets, const int
   const Bufs b = carve(workspace, L);
   const Prepared pw = prepared_ptrs(prepared, prepared_layout(d));
   st = launch_permute(padded_offsets, static_cast<int>(d.El), row_to_slot, top_k, L.cap, xq, xsf,
-                      static_cast<int>(d.H), b.aq, b.asf, b.sched, b.mtd,
-                      static_cast<int64_t>((L.edone - L.mtd) / 4 + d.El), nullptr, nullptr, 0, s);
+                      static_cast<int>(d.H), b.aq, b.asf, b.sched, b.mtd, counter_ints(L, L.mtd), nullptr, nullptr, 0,
+                      s);
   if (st != MOE_OK) return st;
   GemmLaunch g1 = gemm1_launch(d, L, b, pw, padded_offsets, row_to_slot, xs, top_k, dev_status);
   g1.mode = mode == 0 ? kG1Preact : kG1Act;

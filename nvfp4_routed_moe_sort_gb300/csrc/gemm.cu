@@ -157,7 +157,12 @@ moe_status_t launch_gemm_chain(const GemmLaunch& g1, const GemmLaunch& g2, int32
   return dispatch(mode, g1.act, prm, units_max, smem_bytes(g1.El, prm.sparse), s);
 }
 
-moe_status_t launch_gemm_decode(const GemmLaunch& g1, const GemmLaunch& g2, int32_t* e_done, cudaStream_t s) {
+namespace {
+int32_t g_decode_hooks = 0;  // moe_debug_set_decode_hooks
+}  // namespace
+
+moe_status_t launch_gemm_decode(const GemmLaunch& g1, const GemmLaunch& g2, int32_t* e_done, int32_t* own,
+                                const RoutingHint& hint, cudaStream_t s) {
   if (g1.cap == 0) return MOE_OK;
   dgemm::Params prm;
   memset(&prm, 0, sizeof(prm));
@@ -187,6 +192,13 @@ moe_status_t launch_gemm_decode(const GemmLaunch& g1, const GemmLaunch& g2, int3
   prm.dev_status = g1.dev_status;
   prm.tile_counter = g1.tile_counter;
   prm.e_done = e_done;
+  prm.own = own;
+  prm.owned = g2.tile_counter;  // the second tile counter: unused by this kernel otherwise
+  prm.dbg_hooks = g_decode_hooks;
+  prm.hint_ids = hint.ids;
+  prm.hint_mask = hint.id_mask;
+  prm.hint_off = hint.off;
+  prm.hint_slots = hint.slots;
   prm.El = static_cast<int32_t>(g1.El);
   prm.top_k = g1.top_k;
   prm.inter = g1.inter;
@@ -195,10 +207,17 @@ moe_status_t launch_gemm_decode(const GemmLaunch& g1, const GemmLaunch& g2, int3
   prm.route_w_dtype = g2.route_w_dtype;
   prm.rsf = g2.rsf;
   const size_t smem = static_cast<size_t>(dgemm::kStages) * dgemm::kStageBytes + dgemm::kSmemExtra +
-                      roundup64(g1.El + 1, 4) * 4 + g1.El * 4;
+                      roundup64(g1.El + 1, 4) * 4 + g1.El * 4 + roundup64(g1.El, 16);
   const int64_t units_max = g1.El * (prm.ph[0].n_tiles + prm.ph[1].n_tiles);
   const int grid = static_cast<int>(units_max < num_sms() ? units_max : num_sms());
+  prm.n_static = hint.ids != nullptr ? static_cast<int32_t>(grid < kOwnFlags ? grid : kOwnFlags) : 0;
   return dgemm::launch_act(g2.mode == kG2Rows, g1.act, prm, grid, smem, s);
 }
 
 }  // namespace moe
+
+extern "C" int32_t moe_debug_set_decode_hooks(int32_t flags) {
+  const int32_t prev = moe::g_decode_hooks;
+  moe::g_decode_hooks = flags & 3;
+  return prev;
+}

@@ -19,9 +19,18 @@
 //              tcgen05.mma.kind::mxf4nvf4 (M=128, N=16, K=64) into one of two accumulator
 //              buffers (double-buffered: the next unit's MMAs overlap this one's epilogue);
 //   warps 2-5  epilogue, one per TMEM lane quarter.
-// Work units are (active expert, 256-row weight tile): GEMM1's first, then GEMM2's, claimed
-// from one counter; a GEMM2 unit waits (bounded) until every GEMM1 unit of its expert has
-// been written, after starting its weight tile towards L2.
+// Work units are (active expert, 256-row weight tile): GEMM1's first, then GEMM2's; a GEMM2
+// unit waits (bounded) until every GEMM1 unit of its expert has been written, after loading
+// or starting its weight tiles.
+//
+// Scheduling. When the routing ids are given (the one-call path), CTA b's first unit is unit
+// b: while the prologue still computes the plan, the CTA finds that unit's expert from the
+// routing ids (an input of the step) and loads the unit's first weight stages (the weights
+// depend on no earlier kernel), so the weight stream starts during the prologue. After the
+// dependency wait the CTA takes the unit by setting its ownership flag, and keeps the loaded
+// stages only if the plan confirms the expert. All other units come from one counter. A CTA
+// whose counter claim reaches the GEMM2 units first takes every first unit whose flag is
+// still clear, so each GEMM2 wait depends only on GEMM1 units held by running CTAs.
 #pragma once
 
 #include <cuda.h>
@@ -80,6 +89,12 @@ struct Params {
   int32_t* dev_status;
   int32_t* tile_counter;  // zeroed before the launch
   int32_t* e_done;        // per local expert: GEMM1 epilogue warps done (zeroed before the launch)
+  int32_t* own;           // ownership flags of units [0, n_static) (zeroed before the launch)
+  int32_t* owned;         // count of the flags set (zeroed before the launch)
+  int32_t dbg_hooks;      // test hook: bit 0 wrong guesses, bit 1 odd CTAs skip their offered unit
+  int32_t n_static;       // statically offered first units (0: every unit from the counter)
+  const int32_t* hint_ids;  // routing ids of the step [hint_slots] (read before the wait)
+  int32_t hint_mask, hint_off, hint_slots;
   int32_t El, top_k, inter;
   float g2;
   const void* route_w;
@@ -94,6 +109,15 @@ __device__ __forceinline__ void red_release_add(int32_t* counter, int v) {
   asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(counter), "r"(v) : "memory");
 }
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
+// how long a CTA about to take a GEMM2 unit waits for the offered units' owners
+constexpr uint64_t kSweepGraceNs = 20000;
+
+__device__ __forceinline__ int ld_acquire_s32(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
 
 __device__ __forceinline__ bool wait_counter(const int32_t* counter, int target, volatile int* abort_flag,
                                              int32_t* dev_status) {
@@ -180,12 +204,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm_kernel(const __grid_c
   uint64_t* final_bar = acc_empty + 2;
   uint64_t* unit_full = final_bar + 1;
   uint64_t* unit_empty = unit_full + kUnitRing;
-  volatile int32_t* unit_ring = reinterpret_cast<volatile int32_t*>(unit_empty + kUnitRing);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(unit_empty + kUnitRing) + kUnitRing;
+  uint64_t* pre_bar = unit_empty + kUnitRing;  // [kStages] weight stages loaded before the wait
+  volatile int32_t* unit_ring = reinterpret_cast<volatile int32_t*>(pre_bar + kStages);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pre_bar + kStages) + kUnitRing;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_nact = const_cast<int*>(abort_flag) + 1;
   int32_t* s_off = reinterpret_cast<int32_t*>(smem + kStages * kStageBytes + 256);
   int32_t* s_act = s_off + roundup64(p.El + 1, 4);  // active local experts, ascending
+  uint8_t* s_flag = reinterpret_cast<uint8_t*>(s_act + p.El);  // routed local experts (from the ids)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_trigger();
@@ -198,6 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm_kernel(const __grid_c
       mbar_init(&acc_full[b], 1);
       mbar_init(&acc_empty[b], kEpiThreads);
     }
+    for (int s = 0; s < kStages; ++s) mbar_init(&pre_bar[s], 1);
     mbar_init(final_bar, 1);
     for (int i = 0; i < kUnitRing; ++i) {
       mbar_init(&unit_full[i], 1);
@@ -215,6 +242,45 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm_kernel(const __grid_c
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
+  }
+  // The first unit's weight stages, before the wait (see the scheduling note above): the
+  // routed local experts from the ids, the expert ranked blockIdx.x / n_tiles among them.
+  int pre_n = 0, pre_e = -1;  // (producer thread) stages loaded, their expert
+  if (warp == 0 && static_cast<int>(blockIdx.x) < p.n_static) {
+    for (int i = lane; i < p.El; i += 32) s_flag[i] = 0;
+    __syncwarp();
+    for (int i = lane; i < p.hint_slots; i += 32) {
+      const int l = (p.hint_ids[i] & p.hint_mask) - p.hint_off;
+      if (l >= 0 && l < p.El) s_flag[l] = 1;
+    }
+    __syncwarp();
+    const int want = static_cast<int>(blockIdx.x) / p.ph[0].n_tiles + (p.dbg_hooks & 1);
+    int n = 0, e_first = -1;
+    for (int base = 0; base < p.El && n <= want; base += 32) {
+      const int l = base + lane;
+      const bool act = l < p.El && s_flag[l] != 0;
+      const unsigned ball = __ballot_sync(0xffffffffu, act);
+      if (act && n + __popc(ball & ((1u << lane) - 1u)) == want) e_first = l;
+      n += __popc(ball);
+    }
+    e_first = __reduce_max_sync(0xffffffffu, e_first);
+    if (lane == 0 && e_first >= 0) {
+      const Phase& ph = p.ph[0];
+      const int nt = static_cast<int>(blockIdx.x) % ph.n_tiles;
+      const int wrow0 = e_first * ph.Nwp + nt * 256;
+      const int64_t kt = ph.Kp >> 6;
+      const uint8_t* sfw0 = ph.sfw + (static_cast<int64_t>(e_first) * (ph.Nwp >> 7) + nt * 2) * kt * 512;
+      const uint8_t* sfw1 = sfw0 + kt * 512;
+      pre_n = ph.nkb < kStages ? ph.nkb : kStages;
+      pre_e = e_first;
+      for (int kb = 0; kb < pre_n; ++kb) {
+        uint8_t* st = smem + kb * kStageBytes;
+        mbar_arrive_expect_tx(&pre_bar[kb], kWBytes + kSfwBytes);
+        tma_load_2d(st, &ph.tmap_w, kb * 128, wrow0, &pre_bar[kb]);
+        bulk_load(st + kOffSfw, sfw0 + kb * 2048, 2048, &pre_bar[kb]);
+        bulk_load(st + kOffSfw + 2048, sfw1 + kb * 2048, 2048, &pre_bar[kb]);
+      }
+    }
   }
   pdl_wait();  // the plan, the token rows and the counters come from earlier kernels
   for (int i = threadIdx.x; i <= p.El; i += blockDim.x) s_off[i] = p.padded_offsets[i];
@@ -255,13 +321,62 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm_kernel(const __grid_c
       uint32_t issued_mask = 0, issued_phase = 0;
       uint32_t rslot = 0, rphase = 0;
       bool ok = true;
+      // units [0, n_first) are offered to CTAs 0..n_first-1 (GEMM1 units only), the rest
+      // come from the counter
+      const int n_first = p.n_static < units0 ? p.n_static : units0;
+      const int u_static = static_cast<int>(blockIdx.x) < n_first ? static_cast<int>(blockIdx.x) : -1;
+      int u_held = -1;  // a counter claim kept while the offered units are swept
+      int sweep = 0;    // next offered unit to check before the first GEMM2 unit
+      bool first = true;
       while (ok) {
         if (!mbar_wait(&unit_empty[rslot], rphase ^ 1, abort_flag, p.dev_status)) { ok = false; break; }
-        int u = atomicAdd(p.tile_counter, 1);
-        if (u >= total_units) u = -1;
+        int u = -1;
+        if (first) {
+          first = false;
+          const bool skip = (p.dbg_hooks & 2) && (blockIdx.x & 1);
+          if (u_static >= 0 && !skip && atomicCAS(p.own + u_static, 0, 1) == 0) {
+            u = u_static;
+            atomicAdd(p.owned, 1);
+          }
+        }
+        while (u < 0) {
+          if (u_held < 0) {
+            u_held = n_first + atomicAdd(p.tile_counter, 1);
+            if (u_held < units0) {  // GEMM1 units need no sweep
+              u = u_held;
+              u_held = -1;
+              break;
+            }
+          }
+          // before any GEMM2 unit (or the end): every offered unit is owned by a running CTA.
+          // Normally all are by now (one load); late owners get a grace period, then the
+          // units still free are taken here.
+          if (sweep < n_first) {
+            const uint64_t t0 = globaltimer_ns();
+            while (ld_acquire_s32(p.owned) < n_first && globaltimer_ns() - t0 < kSweepGraceNs) __nanosleep(128);
+            if (ld_acquire_s32(p.owned) >= n_first) sweep = n_first;
+          }
+          while (sweep < n_first && u < 0) {
+            if (__ldcg(p.own + sweep) == 0 && atomicCAS(p.own + sweep, 0, 1) == 0) {
+              u = sweep;
+              atomicAdd(p.owned, 1);
+            }
+            ++sweep;
+          }
+          if (u >= 0) break;
+          u = u_held < total_units ? u_held : -1;
+          u_held = -1;
+          break;
+        }
         unit_ring[rslot] = u;
         mbar_arrive(&unit_full[rslot]);
         if (++rslot == kUnitRing) { rslot = 0; rphase ^= 1; }
+        if (pre_n > 0) {
+          // the stages loaded before the wait land before their buffers are reused
+          for (int kb = 0; kb < pre_n; ++kb)
+            if (!mbar_wait(&pre_bar[kb], 0, abort_flag, p.dev_status)) ok = false;
+          if (!ok) break;
+        }
         if (u < 0) break;
         const bool second = u >= units0;
         const Phase& ph = p.ph[second ? 1 : 0];
@@ -279,6 +394,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm_kernel(const __grid_c
         // weight tile is started towards L2 before the wait.
         int pre = 0;
         uint32_t pre_stage = stage;
+        if (pre_n > 0) {
+          // this CTA's first unit: keep the weight stages loaded before the wait if the plan
+          // confirms their expert, else reload them in full below
+          if (u == u_static && !second && e == pre_e) {
+            for (int kb = 0; kb < pre_n; ++kb) {
+              if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.dev_status)) { ok = false; break; }
+              uint8_t* st = smem + stage * kStageBytes;
+              mbar_arrive_expect_tx(&full[stage], kXBytes + kSfxBytes);
+              tma_load_2d(st + kOffX, &ph.tmap_x, kb * 128, seg, &full[stage]);
+              bulk_load(st + kOffSfx, sfx + kb * 2048, 2048, &full[stage]);
+              issued_mask |= 1u << stage;
+              issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+              if (++stage == kStages) { stage = 0; phase ^= 1; }
+            }
+            if (!ok) break;
+            pre = pre_n;
+          }
+          pre_n = 0;
+        }
         if (second && ph.nkb > kStages) {
           prefetch_l2(ph.w_raw + static_cast<int64_t>(wrow0) * (ph.K / 2), static_cast<int64_t>(256) * (ph.K / 2));
           prefetch_l2(sfw0, 2 * kt * 512);
@@ -330,6 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm_kernel(const __grid_c
       if (!ok) {
         for (int s = 0; s < kStages; ++s)
           if (issued_mask & (1u << s)) mbar_drain(&full[s], (issued_phase >> s) & 1);
+        for (int kb = 0; kb < pre_n; ++kb) mbar_drain(&pre_bar[kb], 0);
       }
     }
   } else if (warp == 1) {

@@ -66,8 +66,11 @@ inline PreparedLayout prepared_layout(const Dims& d) {
 // Forward workspace: GEMM tile counters (256 B), permuted activations [cap, H/2] + scale tiles [cap/128][Hp/64][512],
 // intermediate [cap, I/2] + scale tiles [cap/128][Ip/64][512], and the BF16 expert rows
 // [cap, H] (finalized output) or the FP32 accumulator [M, H] (accumulated output).
+// Ownership flags of the decode GEMM's statically assigned first units (one per CTA).
+constexpr int64_t kOwnFlags = 1024;
+
 struct WorkspaceLayout {
-  size_t sched, mtd, edone, aq, asf, iq, isf, g, total;
+  size_t sched, mtd, edone, own, aq, asf, iq, isf, g, total;
   int64_t cap;
 };
 
@@ -84,6 +87,7 @@ inline WorkspaceLayout workspace_layout(const Dims& d, int64_t M, int64_t top_k,
   L.sched = take(c, 256);  // GEMM tile counters, zeroed by the permute kernel
   L.mtd = take(c, (L.cap / kTileM) * 4);  // per-row-tile GEMM1 completion counts (chained GEMMs), zeroed too
   L.edone = take(c, d.El * 4);            // per-expert GEMM1 completion counts (decode GEMMs), zeroed too
+  L.own = take(c, kOwnFlags * 4);         // first-unit ownership flags (decode GEMMs), zeroed too
   L.aq = take(c, L.cap * d.H / 2);
   L.asf = take(c, L.cap * d.Hp / 16);
   L.iq = take(c, L.cap * d.I / 2);
@@ -94,6 +98,21 @@ inline WorkspaceLayout workspace_layout(const Dims& d, int64_t M, int64_t top_k,
   L.total = c;
   return L;
 }
+
+// ints from `from` (L.sched or L.mtd) through the last ownership flag: the counters that a
+// forward zeroes before its GEMMs
+inline int64_t counter_ints(const WorkspaceLayout& L, size_t from) {
+  return static_cast<int64_t>(L.own - from) / 4 + kOwnFlags;
+}
+
+// The routing ids of the step, when the GEMMs are launched from the one-call path: the
+// decode GEMM reads them before its dependency wait to start the first unit's weights.
+struct RoutingHint {
+  const int32_t* ids = nullptr;
+  int32_t id_mask = -1;
+  int32_t off = 0;
+  int32_t slots = 0;
+};
 
 // GEMM epilogue modes
 enum GemmMode : int {
@@ -146,7 +165,8 @@ moe_status_t launch_gemm(const GemmLaunch& g, cudaStream_t s);
 moe_status_t launch_gemm_chain(const GemmLaunch& g1, const GemmLaunch& g2, int32_t* mt_done, cudaStream_t s);
 // the same with the decode-shaped kernel (at most 16 rows per expert); e_done holds E_local
 // zeroed counters
-moe_status_t launch_gemm_decode(const GemmLaunch& g1, const GemmLaunch& g2, int32_t* e_done, cudaStream_t s);
+moe_status_t launch_gemm_decode(const GemmLaunch& g1, const GemmLaunch& g2, int32_t* e_done, int32_t* own,
+                                const RoutingHint& hint, cudaStream_t s);
 moe_status_t launch_permute(const int32_t* padded_offsets, int El, const int32_t* row_to_slot, int top_k,
                             int64_t cap, const uint8_t* xq, const uint8_t* xsf, int H, uint8_t* aq, uint8_t* asf,
                             int32_t* tile_counters, int32_t* mt_done, int64_t n_mt, const uint16_t* acc_init,
@@ -164,7 +184,7 @@ moe_status_t forward_chain(const int32_t* padded_offsets, const int32_t* row_to_
                            int32_t topk_weights_dtype, float routed_scaling_factor, float fc2_input_scale,
                            int32_t do_finalize, uint16_t* out, uint16_t* gemm2_out, void* workspace,
                            int32_t* dev_status, void* const* step_events, int32_t num_step_events, bool run_permute,
-                           cudaStream_t s);
+                           const RoutingHint& hint, cudaStream_t s);
 moe_status_t launch_prepare_matrix(const uint8_t* src, const uint8_t* src_sf, int E, int rows, int rows_p, int K,
                                    int gated_inter, uint8_t* dst, uint8_t* dst_sf, cudaStream_t s);
 

@@ -70,7 +70,9 @@ __device__ void fill_padding(const int* start, const int* cnt, int El, int total
   for (int64_t p = total + threadIdx.x; p < cap; p += blockDim.x) row_to_slot[p] = -1;
 }
 
-// place slots [begin, end) in order; sm.cursor[l] holds the first free row of expert l
+// place slots [begin, end) in order; sm.cursor[l] holds the first free row of expert l.
+// row_to_slot and dev_status may be null (a block that only needs token_to_row, which may
+// then point to shared memory): the rows are the same, nothing else is written or checked.
 __device__ void place_range(const int32_t* __restrict__ ids, int id_mask, int64_t begin, int64_t end, int top_k,
                             int off, int El, PlanSmem& sm, int32_t* __restrict__ row_to_slot, int32_t* __restrict__ token_to_row,
                             int32_t* dev_status) {
@@ -81,11 +83,11 @@ __device__ void place_range(const int32_t* __restrict__ ids, int id_mask, int64_
     if (s < end) {
       const int id = entry_id(ids, s, id_mask);
       l = local_of(id, off, El);
-      if (l >= 0) {
+      if (l >= 0 && dev_status != nullptr) {
         const int64_t t0 = s - s % top_k;
         for (int64_t q = t0; q < s; ++q)
           if (entry_id(ids, q, id_mask) == id) atomicOr(dev_status, MOE_DEV_DUPLICATE_EXPERT);
-      } else {
+      } else if (l < 0) {
         token_to_row[s] = -1;
       }
     }
@@ -98,7 +100,7 @@ __device__ void place_range(const int32_t* __restrict__ ids, int id_mask, int64_
       int prefix = 0;
       for (int ww = 0; ww < w; ++ww) prefix += sm.warp_cnt[ww][l];
       const int row = sm.cursor[l] + prefix + rank;
-      row_to_slot[row] = static_cast<int32_t>(s);
+      if (row_to_slot != nullptr) row_to_slot[row] = static_cast<int32_t>(s);
       token_to_row[s] = row;
     }
     __syncthreads();

@@ -8,8 +8,9 @@
 // GEMM2, finalize).
 //
 // Small batches (decode: at most 2048 routed slots and 2^17 hidden values) run the
-// quantiser, the plan and the permutation in one kernel of one 1024-thread CTA, and GEMM1
-// and GEMM2 as one chained launch, so the step is three launches (prologue, GEMMs, combine)
+// quantiser, the plan and the permutation in one kernel (one CTA per token group, each
+// building the small plan itself), and GEMM1 and GEMM2 as one launch, so the step is
+// three launches (prologue, GEMMs, combine)
 // instead of six; each of those steps is latency-bound at these sizes. Larger batches run the separate kernels of
 // moe_plan, a quantiser that stores straight into the plan rows, and the GEMMs and combine
 // of moe_grouped_fp4_forward. Both paths compute the same bytes as the separate calls: the
@@ -56,17 +57,22 @@ bool small_batch(int64_t M, int64_t k, int64_t H) {
 }
 
 constexpr int kPrologueMaxRows = static_cast<int>(kPrologueMaxValues / 128);  // H >= 128
+constexpr int kPrologueMaxCtas = 32;
 
-// One CTA, every phase spread over all 1024 threads:
-//  (0) the routed-slot histogram and, for per-token scales, each token's max |x| (thread per
+// A grid of G <= 32 CTAs, CTA c taking tokens c, c + G, ... Every CTA builds the whole plan
+// in shared memory (at most 2048 slots: the one-block plan of plan_single_kernel, from the
+// routing ids alone), so no CTA waits for another:
+//  (0) the routed-slot histogram and, for per-token scales, its tokens' max |x| (thread per
 //      16-value block, maximum through shared memory);
-//  (1) the one-block plan of plan_single_kernel;
-//  (2) NVFP4 quantisation of each 16-value block (the arithmetic of quantize_rows_kernel),
-//      its 8 code bytes and its scale byte stored straight into every plan row of the
-//      token (the permuted operand of GEMM1 and its 128x4 scale tiles): the quantised
-//      activations never make a round trip through memory.
-// Also the per-token scales, the zeroed GEMM tile and row-tile counters and, for an
-// accumulated output, the FP32 copy of out.
+//  (1) the plan, written out in shares: CTA 0 the counts and padded offsets, CTA c the
+//      padding rows of experts c, c + G, ... and token_to_row / row_to_slot of its own
+//      tokens' slots (with the duplicate-expert check); each CTA zeroes a slice of the GEMM
+//      counters;
+//  (2) NVFP4 quantisation of its tokens' 16-value blocks (the arithmetic of
+//      quantize_rows_kernel), each block's 8 code bytes and scale byte stored straight into
+//      every plan row of the token (the permuted operand of GEMM1 and its 128x4 scale
+//      tiles): the quantised activations never make a round trip through memory.
+// Also its tokens' scales and, for an accumulated output, the FP32 copy of their rows of out.
 __global__ void __launch_bounds__(kPrologueThreads) small_prologue_kernel(
     const uint16_t* __restrict__ x, int M, int H, int64_t ld, int per_token, const int32_t* __restrict__ ids,
     int id_mask, int top_k, int off, int El, float* __restrict__ xs, int32_t* __restrict__ counts,
@@ -74,86 +80,116 @@ __global__ void __launch_bounds__(kPrologueThreads) small_prologue_kernel(
     uint8_t* __restrict__ aq, uint8_t* __restrict__ asf, int32_t* __restrict__ tile_counters,
     int32_t* __restrict__ mt_done, int n_mt, const uint16_t* __restrict__ acc_init, float* __restrict__ acc) {
   __shared__ PlanSmem sm;
-  __shared__ unsigned s_amax[kPrologueMaxRows];      // per-row max |x| (bits of a non-negative float)
+  __shared__ unsigned s_amax[kPrologueMaxRows];      // max |x| of each own token (bits of a non-negative float)
   __shared__ int32_t s_row[kPrologueMaxSlots];       // plan row of each slot
   pdl_trigger();
+  const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  const bool lead = c == 0;
+  const int n_own = (M - c + G - 1) / G;             // own tokens c + i*G, i < n_own
   zero_tables(sm, El);
-  for (int i = threadIdx.x; i < M; i += kPrologueThreads) s_amax[i] = 0u;
+  for (int i = threadIdx.x; i < n_own; i += kPrologueThreads) s_amax[i] = 0u;
   pdl_wait();
-  if (threadIdx.x < 2) tile_counters[threadIdx.x] = 0;
-  for (int i = threadIdx.x; i < n_mt; i += kPrologueThreads) mt_done[i] = 0;
+  if (lead && threadIdx.x < 2) tile_counters[threadIdx.x] = 0;
+  for (int i = c * kPrologueThreads + threadIdx.x; i < n_mt; i += G * kPrologueThreads) mt_done[i] = 0;
   const int n = M * top_k;
   const int nblk = H / kBlock;
-  const int nb_all = M * nblk;
+  const int nb_own = n_own * nblk;
   __syncthreads();
-  // (0) histogram of the routed slots per local expert; per-token maxima
+  // (0) histogram of the routed slots per local expert; own tokens' maxima
   for (int s = threadIdx.x; s < n; s += kPrologueThreads) {
     const int l = local_of(entry_id(ids, s, id_mask), off, El);
     if (l >= 0) atomicAdd(&sm.cnt[l], 1);
   }
   if (per_token) {
-    for (int bi = threadIdx.x; bi < nb_all; bi += kPrologueThreads) {
-      const int r = bi / nblk, b = bi - r * nblk;
+    for (int bi = threadIdx.x; bi < nb_own; bi += kPrologueThreads) {
+      const int i = bi / nblk, b = bi - i * nblk;
       float v[16];
-      load_block16(x + static_cast<int64_t>(r) * ld + b * kBlock, v);
+      load_block16(x + static_cast<int64_t>(c + i * G) * ld + b * kBlock, v);
       float amax = 0.0f;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(v[i]));
-      atomicMax(&s_amax[r], __float_as_uint(amax));
+      for (int q = 0; q < 16; ++q) amax = fmaxf(amax, fabsf(v[q]));
+      atomicMax(&s_amax[i], __float_as_uint(amax));
     }
   }
   __syncthreads();
   // (1) plan
   scan_padded(sm, El);
   __syncthreads();
-  for (int l = threadIdx.x; l <= El; l += kPrologueThreads) {
-    padded_offsets[l] = sm.cursor[l];
-    if (l < El) counts[l] = sm.cnt[l];
+  if (lead)
+    for (int l = threadIdx.x; l <= El; l += kPrologueThreads) {
+      padded_offsets[l] = sm.cursor[l];
+      if (l < El) counts[l] = sm.cnt[l];
+    }
+  // -1 on the padding rows of experts c, c + G, ... (one warp per expert); rows past the
+  // padded total are never read by the GEMMs, so (unlike moe_plan's output) this internal
+  // row_to_slot leaves them unwritten
+  {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int l = c + warp * G; l < El; l += G * (kPrologueThreads / 32)) {
+      const int b = sm.cursor[l] + sm.cnt[l];
+      const int e = sm.cursor[l] + (sm.cnt[l] + kSegAlign - 1) / kSegAlign * kSegAlign;
+      for (int r = b + lane; r < e; r += 32) row_to_slot[r] = -1;
+    }
   }
-  // -1 on the segments' padding rows; rows past the padded total are never read by the
-  // GEMMs, so (unlike moe_plan's output) this internal row_to_slot leaves them unwritten
-  fill_padding(sm.cursor, sm.cnt, El, sm.cursor[El], sm.cursor[El], row_to_slot);
   __syncthreads();
-  place_range(ids, id_mask, 0, n, top_k, off, El, sm, row_to_slot, token_to_row, dev_status);
-  for (int s = threadIdx.x; s < n; s += kPrologueThreads) s_row[s] = __ldcg(token_to_row + s);
+  place_range(ids, id_mask, 0, n, top_k, off, El, sm, nullptr, s_row, nullptr);
   __syncthreads();
-  // (2) quantise each block once and store it into every plan row of its token
+  // own tokens' slots: token_to_row, row_to_slot and the duplicate-expert check (as moe_plan)
+  for (int it = threadIdx.x; it < n_own * top_k; it += kPrologueThreads) {
+    const int i = it / top_k, j = it - i * top_k;
+    const int sl = (c + i * G) * top_k + j;
+    const int row = s_row[sl];
+    token_to_row[sl] = row;
+    if (row >= 0) {
+      row_to_slot[row] = sl;
+      const int id = entry_id(ids, sl, id_mask);
+      for (int q = sl - j; q < sl; ++q)
+        if (entry_id(ids, q, id_mask) == id) atomicOr(dev_status, MOE_DEV_DUPLICATE_EXPERT);
+    }
+  }
+  // (2) own tokens: one thread per (token, slot, block), consecutive threads on consecutive
+  // blocks of one plan row; each block is quantised by the same arithmetic for every slot
   const int kcols_p = static_cast<int>(roundup64(H, kTileK) / 16);  // scale columns incl. K padding
-  for (int bi = threadIdx.x; bi < nb_all; bi += kPrologueThreads) {
-    const int r = bi / nblk, b = bi - r * nblk;
+  const int per_tok = top_k * nblk;
+  for (int it = threadIdx.x; it < n_own * per_tok; it += kPrologueThreads) {
+    const int i = it / per_tok, rem = it - i * per_tok;
+    const int j = rem / nblk, b = rem - j * nblk;
+    const int r = c + i * G;
+    const int row = s_row[r * top_k + j];
+    if (row < 0 && !(j == 0 && b == 0)) continue;
     float g = 1.0f, dec = 1.0f;
     if (per_token) {
-      const float amax = __uint_as_float(s_amax[r]);
+      const float amax = __uint_as_float(s_amax[i]);
       if (amax > 0.0f) {
         g = __fdiv_rn(kGlobalNumerator, amax);
         dec = __fdiv_rn(amax, kGlobalNumerator);
       }
     }
+    if (j == 0 && b == 0) xs[r] = dec;
+    if (row < 0) continue;
     float v[16];
     load_block16(x + static_cast<int64_t>(r) * ld + b * kBlock, v);
     uint32_t codes[2];
     const uint32_t q = quantize_block16(v, g, codes);
-    for (int j = 0; j < top_k; ++j) {
-      const int row = s_row[r * top_k + j];
-      if (row < 0) continue;
-      *reinterpret_cast<uint2*>(aq + static_cast<int64_t>(row) * (H / 2) + b * 8) = make_uint2(codes[0], codes[1]);
-      asf[sf_tile_offset(row, b, kcols_p)] = static_cast<uint8_t>(q);
-    }
-    if (b == 0) xs[r] = dec;
+    *reinterpret_cast<uint2*>(aq + static_cast<int64_t>(row) * (H / 2) + b * 8) = make_uint2(codes[0], codes[1]);
+    asf[sf_tile_offset(row, b, kcols_p)] = static_cast<uint8_t>(q);
   }
-  // zero scales on the K padding columns of the routed rows (H not a multiple of 256)
+  // zero scales on the K padding columns of the own tokens' routed rows (H not a multiple of 256)
   const int npad = kcols_p - nblk;
-  for (int i = threadIdx.x; i < n * npad; i += kPrologueThreads) {
-    const int s = i / npad;
-    const int row = s_row[s];
-    if (row >= 0) asf[sf_tile_offset(row, nblk + (i - s * npad), kcols_p)] = 0;
+  for (int it = threadIdx.x; it < n_own * top_k * npad; it += kPrologueThreads) {
+    const int sl = it / npad;                           // own slot index: token i, slot j
+    const int i = sl / top_k, j = sl - i * top_k;
+    const int row = s_row[(c + i * G) * top_k + j];
+    if (row >= 0) asf[sf_tile_offset(row, nblk + (it - sl * npad), kcols_p)] = 0;
   }
-  // accumulated output: acc = fp32(out)
+  // accumulated output: acc = fp32(out) on the own tokens' rows
   if (acc != nullptr) {
-    const int64_t n8 = static_cast<int64_t>(M) * H / 8;
-    for (int64_t i = threadIdx.x; i < n8; i += kPrologueThreads) {
-      const uint4 v = reinterpret_cast<const uint4*>(acc_init)[i];
-      float4* d = reinterpret_cast<float4*>(acc) + 2 * i;
+    const int h8 = H / 8;
+    for (int it = threadIdx.x; it < n_own * h8; it += kPrologueThreads) {
+      const int i = it / h8;
+      const int64_t e = static_cast<int64_t>(c + i * G) * h8 + (it - i * h8);
+      const uint4 v = reinterpret_cast<const uint4*>(acc_init)[e];
+      float4* d = reinterpret_cast<float4*>(acc) + 2 * e;
       d[0] = make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u), __uint_as_float(v.y << 16),
                          __uint_as_float(v.y & 0xFFFF0000u));
       d[1] = make_float4(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xFFFF0000u), __uint_as_float(v.w << 16),
@@ -336,12 +372,13 @@ extern "C" moe_status_t moe_routed_forward(const uint16_t* x, int32_t M, int64_t
     const WorkspaceLayout L = workspace_layout(d, M, top_k, do_finalize);
     uint8_t* fb = static_cast<uint8_t*>(fwd);
     const bool accum = do_finalize == MOE_OUTPUT_ACCUMULATE;
-    st = launch_pdl(small_prologue_kernel, dim3(1), dim3(kPrologueThreads), 0, s, x, static_cast<int>(M),
+    const unsigned ctas = static_cast<unsigned>(M < kPrologueMaxCtas ? M : kPrologueMaxCtas);
+    st = launch_pdl(small_prologue_kernel, dim3(ctas), dim3(kPrologueThreads), 0, s, x, static_cast<int>(M),
                     static_cast<int>(d.H), ld_x, act_scale_mode == MOE_SCALE_PER_TOKEN ? 1 : 0, topk_ids, id_mask,
                     static_cast<int>(top_k), static_cast<int>(local_expert_offset), static_cast<int>(d.El), xs,
                     counts, padded, r2s, token_to_row, dev_status, fb + L.aq, fb + L.asf,
                     reinterpret_cast<int32_t*>(fb + L.sched), reinterpret_cast<int32_t*>(fb + L.mtd),
-                    static_cast<int>((L.edone - L.mtd) / 4 + d.El), accum ? static_cast<const uint16_t*>(out) : nullptr,
+                    static_cast<int>(counter_ints(L, L.mtd)), accum ? static_cast<const uint16_t*>(out) : nullptr,
                     accum ? reinterpret_cast<float*>(fb + L.g) : nullptr);
     if (st != MOE_OK) return st;
   } else {
@@ -360,11 +397,16 @@ extern "C" moe_status_t moe_routed_forward(const uint16_t* x, int32_t M, int64_t
                     act_scale_mode == MOE_SCALE_PER_TOKEN ? 1 : 0, static_cast<int>(top_k),
                     static_cast<const int32_t*>(token_to_row), xs, fb + L.aq, fb + L.asf,
                     reinterpret_cast<int32_t*>(fb + L.sched),
-                    static_cast<int>((L.edone - L.sched) / 4 + d.El), accum ? static_cast<const uint16_t*>(out) : nullptr,
+                    static_cast<int>(counter_ints(L, L.sched)), accum ? static_cast<const uint16_t*>(out) : nullptr,
                     accum ? reinterpret_cast<float*>(fb + L.g) : nullptr);
     if (st != MOE_OK) return st;
   }
+  RoutingHint hint;
+  hint.ids = topk_ids;
+  hint.id_mask = id_mask;
+  hint.off = local_expert_offset;
+  hint.slots = M * top_k;
   return forward_chain(padded, r2s, token_to_row, M, top_k, xq, xsf, xs, w, prepared, topk_weights,
                        topk_weights_dtype, routed_scaling_factor, fc2_input_scale, do_finalize, out, gemm2_out, fwd,
-                       dev_status, num_step_events == 5 ? fwd_events : nullptr, num_step_events, false, s);
+                       dev_status, num_step_events == 5 ? fwd_events : nullptr, num_step_events, false, hint, s);
 }

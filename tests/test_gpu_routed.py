@@ -54,6 +54,36 @@ def test_routed_equals_separate_calls(name, do_finalize):
     assert p.layer.device_status(cfg.M, cfg.top_k, do_finalize) == 0
 
 
+@pytest.mark.parametrize("name", ["tiny", "decode_t8", "decode_ep"])
+@pytest.mark.parametrize("hooks", [1, 2, 3])
+def test_decode_scheduling_fallbacks(name, hooks):
+    """The decode GEMM loads each CTA's first unit's weights before the plan exists, guessing
+    the expert from the routing ids, and offers that unit to the CTA through an ownership
+    flag. Wrong guesses (bit 0: the stages are reloaded) and first units left to other CTAs
+    (bit 1: taken by the sweep before any GEMM2 unit) give the same bytes as the normal
+    schedule, finalized and unfinalized."""
+    cfg = CASES[name]
+    ids, tw = _unrouted(cfg) if name == "decode_ep" else (None, None)
+    p = Problem(cfg, ids, tw)
+    ref = bf16_np(p.run_routed(True)).copy()
+    g2r, _, t2r = p.run_routed(False)
+    g2r, t2r = bf16_np(g2r).copy(), to_np(t2r).copy()
+    prev = pkg._lib.moe_debug_set_decode_hooks(hooks)
+    try:
+        got = bf16_np(p.run_routed(True)).copy()
+        g2, _, t2 = p.run_routed(False)
+        g2, t2 = bf16_np(g2).copy(), to_np(t2).copy()
+    finally:
+        pkg._lib.moe_debug_set_decode_hooks(prev)
+    assert prev == 0
+    assert np.array_equal(got, ref)
+    assert np.array_equal(t2, t2r)
+    real = t2r[t2r >= 0]
+    assert np.array_equal(g2[real], g2r[real])
+    for mode in (True, False):
+        assert p.layer.device_status(cfg.M, cfg.top_k, mode) == 0
+
+
 def test_routed_row_stride_and_packed_routing():
     cfg = CASES["decode_ep"]
     p = Problem(cfg)
