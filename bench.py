@@ -283,14 +283,11 @@ def run_gpu(args, cfg, rank, world):
         ms = float(tt.item())
     work, stepw, R, active = kernel_work(cfg, ids)
     kern_ms = {n: float(np.mean(v)) for n, v in per.items()}
-    if M * k <= 2048:
-        # GEMM1 and GEMM2 run as one launch (its time is the gemm1 interval): the decode
-        # kernel (weights as the 128-row MMA operand) up to 16 tokens, else the chained one
-        dom = "gemm1+gemm2 (decode)" if M <= 16 else "gemm1+gemm2 (chained)"
-        kern_ms[dom] = kern_ms.pop("gemm1") + kern_ms.pop("gemm2")
-        work[dom] = {key: work["gemm1"][key] + work["gemm2"][key] for key in ("bytes", "flops")}
-    else:
-        dom = max(["gemm1", "gemm2"], key=lambda n: kern_ms[n])
+    # GEMM1 and GEMM2 run as one launch (its time is the gemm1 interval): the decode kernel
+    # (weights as the 128-row MMA operand) up to 16 tokens, else the chained one
+    dom = "gemm1+gemm2 (decode)" if M <= 16 else "gemm1+gemm2 (chained)"
+    kern_ms[dom] = kern_ms.pop("gemm1") + kern_ms.pop("gemm2")
+    work[dom] = {key: work["gemm1"][key] + work["gemm2"][key] for key in ("bytes", "flops")}
     peaks = load_peaks()
     fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
     t_dom = kern_ms[dom] * 1e-3
@@ -322,12 +319,12 @@ def run_gpu(args, cfg, rank, world):
         wo_times.append(s_ev.elapsed_time(e_ev))
     del wo
     small = M * k <= 2048 and M * cfg.H <= (1 << 17)
-    # small: prologue, chained GEMMs, combine; otherwise quantise, plan (1 or 3), permute,
-    # GEMM1 + GEMM2 (one chained launch up to 2048 slots), combine
+    # small: prologue, GEMMs (one launch), combine; otherwise the plan (one kernel up to 2048
+    # slots, else three), the quantiser storing into the plan rows, GEMMs, combine
     if small:
         launches_per_step = 3
     else:
-        launches_per_step = 5 + (2 if M * k > 2048 else 0) + (0 if M * k <= 2048 else 1)
+        launches_per_step = (1 if M * k <= 2048 else 3) + 3
     res = {
         "metric": METRIC, "value": world * M / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,

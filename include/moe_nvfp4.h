@@ -262,14 +262,12 @@ MOE_API moe_status_t moe_prepare_weights(const moe_nvfp4_weights_t* w, void* pre
  *                      their value; gemm2_out may be NULL
  *   workspace          moe_forward_workspace_bytes(...) bytes of device scratch
  *   step_events        optional array of `num_step_events` (0 or 5) cudaEvent_t recorded on
- *                      `stream` before permute, gemm1, gemm2, finalize and at the end; batches
- *                      of at most MOE_CHAIN_MAX_SLOTS routed slots run GEMM1 and GEMM2 as one
- *                      chained launch, whose time falls between the gemm1 and gemm2 marks
+ *                      `stream` before permute, gemm1, gemm2, finalize and at the end. GEMM1
+ *                      and GEMM2 run as one chained launch (the GEMM2 tiles of a 128-row tile
+ *                      start as soon as its GEMM1 tiles are written), whose time falls
+ *                      between the gemm1 and gemm2 marks
  * ---------------------------------------------------------------------------------------- */
-/* M * top_k at or below which GEMM1 and GEMM2 run as one chained launch (the GEMM2 tiles of
- * a 128-row tile start as soon as its GEMM1 tiles are written). */
-#define MOE_CHAIN_MAX_SLOTS 2048
-/* Chained batches of at most this many tokens run GEMM1 and GEMM2 with the operands swapped
+/* Batches of at most this many tokens run GEMM1 and GEMM2 with the operands swapped
  * (the weight tile as the MMA's 128-row operand, each expert's token rows as its 16
  * columns). A token naming one expert twice (MOE_DEV_DUPLICATE_EXPERT) can give an expert
  * more than 16 rows; rows past the 16th are then not computed. */

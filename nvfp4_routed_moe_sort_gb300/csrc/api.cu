@@ -232,13 +232,7 @@ moe_status_t forward_chain(const int32_t* padded_offsets, const int32_t* row_to_
   if ((st = mark(1)) != MOE_OK) return st;
   GemmLaunch g1 = gemm1_launch(d, L, b, pw, padded_offsets, row_to_slot, xs, top_k, dev_status);
   g1.g2 = fc2_input_scale;
-  // small batches: GEMM1 and GEMM2 in one chained launch (the GEMM2 mark then follows it)
-  const bool chained = static_cast<int64_t>(M) * top_k <= kChainMaxSlots;
-  if (!chained) {
-    st = launch_gemm(g1, s);
-    if (st != MOE_OK) return st;
-    if ((st = mark(2)) != MOE_OK) return st;
-  }
+  // GEMM1 and GEMM2 in one chained launch (the GEMM2 mark then follows it)
   GemmLaunch g2;
   g2.mode = accum ? kG2Reduce : kG2Rows;
   g2.a = b.iq;
@@ -268,19 +262,13 @@ moe_status_t forward_chain(const int32_t* padded_offsets, const int32_t* row_to_
   g2.rsf = routed_scaling_factor;
   g2.dev_status = dev_status;
   g2.tile_counter = b.sched + 1;
-  if (chained && M <= kDecodeMaxTokens) {
+  if (M <= kDecodeMaxTokens)
     st = launch_gemm_decode(g1, g2, reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + L.edone),
                             reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + L.own), hint, s);
-    if (st != MOE_OK) return st;
-    if ((st = mark(2)) != MOE_OK) return st;
-  } else if (chained) {
+  else
     st = launch_gemm_chain(g1, g2, b.mtd, s);
-    if (st != MOE_OK) return st;
-    if ((st = mark(2)) != MOE_OK) return st;
-  } else {
-    st = launch_gemm(g2, s);
-    if (st != MOE_OK) return st;
-  }
+  if (st != MOE_OK) return st;
+  if ((st = mark(2)) != MOE_OK) return st;
   if ((st = mark(3)) != MOE_OK) return st;
   if (fin) {
     st = launch_finalize(rows_out, topk_weights, topk_weights_dtype, routed_scaling_factor, token_to_row, M, top_k,

@@ -414,11 +414,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm_kernel(const __grid_c
           pre_n = 0;
         }
         if (second && ph.nkb > kStages) {
-          prefetch_l2(ph.w_raw + static_cast<int64_t>(wrow0) * (ph.K / 2), static_cast<int64_t>(256) * (ph.K / 2));
-          prefetch_l2(sfw0, 2 * kt * 512);
-          if (!wait_counter(p.e_done + e, kEpiWarps * p.ph[0].n_tiles, abort_flag, p.dev_status)) {
-            ok = false;
-            break;
+          const int target = kEpiWarps * p.ph[0].n_tiles;
+          if (ld_acquire_s32(p.e_done + e) < target) {  // only a unit that will wait prefetches
+            prefetch_l2(ph.w_raw + static_cast<int64_t>(wrow0) * (ph.K / 2), static_cast<int64_t>(256) * (ph.K / 2));
+            prefetch_l2(sfw0, 2 * kt * 512);
+            if (!wait_counter(p.e_done + e, target, abort_flag, p.dev_status)) {
+              ok = false;
+              break;
+            }
           }
           fence_proxy_async_global();  // the TMA reads below follow the observed generic writes
         } else if (second) {

@@ -1,4 +1,5 @@
-// Instantiations of the grouped GEMM kernel: GEMM1 with the SWIGLU, GEGLU activations.
+// Instantiations of the grouped GEMM kernel: the standalone GEMM1 with the plain epilogues of
+// the test hook (pre-activations, BF16 intermediate) for the SWIGLU and GEGLU activations.
 #include "gemm_kernel.cuh"
 
 namespace moe {
@@ -8,12 +9,10 @@ moe_status_t launch_gated(int mode, int act, const GemmParams& prm, int64_t unit
   if (is_chain(mode)) return launch_chain_gated(mode, act, prm, units_max, smem, s);
   switch (act) {
     case MOE_ACT_SWIGLU:
-      if (mode == kG1Fused) return launch_kernel<kG1Fused, MOE_ACT_SWIGLU>(prm, units_max, smem, s);
       if (mode == kG1Act) return launch_kernel<kG1Act, MOE_ACT_SWIGLU>(prm, units_max, smem, s);
       if (mode == kG1Preact) return launch_kernel<kG1Preact, MOE_ACT_SWIGLU>(prm, units_max, smem, s);
       break;
     case MOE_ACT_GEGLU:
-      if (mode == kG1Fused) return launch_kernel<kG1Fused, MOE_ACT_GEGLU>(prm, units_max, smem, s);
       if (mode == kG1Act) return launch_kernel<kG1Act, MOE_ACT_GEGLU>(prm, units_max, smem, s);
       if (mode == kG1Preact) return launch_kernel<kG1Preact, MOE_ACT_SWIGLU>(prm, units_max, smem, s);
       break;

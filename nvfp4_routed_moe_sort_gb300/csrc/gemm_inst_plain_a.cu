@@ -1,4 +1,5 @@
-// Instantiations of the grouped GEMM kernel: GEMM1 with the RELU2, GELU, RELU activations.
+// Instantiations of the grouped GEMM kernel: the standalone GEMM1 with the plain epilogues of
+// the test hook (pre-activations, BF16 intermediate) for the RELU2, GELU and RELU activations.
 #include "gemm_kernel.cuh"
 
 namespace moe {
@@ -8,17 +9,14 @@ moe_status_t launch_plain_a(int mode, int act, const GemmParams& prm, int64_t un
   if (is_chain(mode)) return launch_chain_plain_a(mode, act, prm, units_max, smem, s);
   switch (act) {
     case MOE_ACT_RELU2:
-      if (mode == kG1Fused) return launch_kernel<kG1Fused, MOE_ACT_RELU2>(prm, units_max, smem, s);
       if (mode == kG1Act) return launch_kernel<kG1Act, MOE_ACT_RELU2>(prm, units_max, smem, s);
       if (mode == kG1Preact) return launch_kernel<kG1Preact, MOE_ACT_RELU2>(prm, units_max, smem, s);
       break;
     case MOE_ACT_GELU:
-      if (mode == kG1Fused) return launch_kernel<kG1Fused, MOE_ACT_GELU>(prm, units_max, smem, s);
       if (mode == kG1Act) return launch_kernel<kG1Act, MOE_ACT_GELU>(prm, units_max, smem, s);
       if (mode == kG1Preact) return launch_kernel<kG1Preact, MOE_ACT_RELU2>(prm, units_max, smem, s);
       break;
     case MOE_ACT_RELU:
-      if (mode == kG1Fused) return launch_kernel<kG1Fused, MOE_ACT_RELU>(prm, units_max, smem, s);
       if (mode == kG1Act) return launch_kernel<kG1Act, MOE_ACT_RELU>(prm, units_max, smem, s);
       if (mode == kG1Preact) return launch_kernel<kG1Preact, MOE_ACT_RELU2>(prm, units_max, smem, s);
       break;

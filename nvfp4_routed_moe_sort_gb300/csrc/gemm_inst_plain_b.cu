@@ -1,4 +1,5 @@
-// Instantiations of the grouped GEMM kernel: GEMM1 with the SILU, IDENTITY activations.
+// Instantiations of the grouped GEMM kernel: the standalone GEMM1 with the plain epilogues of
+// the test hook (pre-activations, BF16 intermediate) for the SILU and IDENTITY activations.
 #include "gemm_kernel.cuh"
 
 namespace moe {
@@ -8,12 +9,10 @@ moe_status_t launch_plain_b(int mode, int act, const GemmParams& prm, int64_t un
   if (is_chain(mode)) return launch_chain_plain_b(mode, act, prm, units_max, smem, s);
   switch (act) {
     case MOE_ACT_SILU:
-      if (mode == kG1Fused) return launch_kernel<kG1Fused, MOE_ACT_SILU>(prm, units_max, smem, s);
       if (mode == kG1Act) return launch_kernel<kG1Act, MOE_ACT_SILU>(prm, units_max, smem, s);
       if (mode == kG1Preact) return launch_plain_a(mode, MOE_ACT_RELU2, prm, units_max, smem, s);
       break;
     case MOE_ACT_IDENTITY:
-      if (mode == kG1Fused) return launch_kernel<kG1Fused, MOE_ACT_IDENTITY>(prm, units_max, smem, s);
       if (mode == kG1Act) return launch_kernel<kG1Act, MOE_ACT_IDENTITY>(prm, units_max, smem, s);
       if (mode == kG1Preact) return launch_plain_a(mode, MOE_ACT_RELU2, prm, units_max, smem, s);
       break;

@@ -598,14 +598,20 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         const uint8_t* sfb0 = ph.sfb + (static_cast<int64_t>(e) * (ph.Np >> 7) + nt * 2) * kt * 512;
         const uint8_t* sfb1 = sfb0 + kt * 512;
         if (second) {
-          // the weight tile and its scales do not depend on GEMM1: start them towards L2,
-          // then wait until every GEMM1 tile of these rows has been written
-          prefetch_l2(ph.b_raw + static_cast<int64_t>(brow0) * (ph.K / 2), static_cast<int64_t>(kTileN) * (ph.K / 2));
-          prefetch_l2(sfb0, 2 * kt * 512);
-          if (!wait_counter(p.mt_done + (row0 >> 7), (kEpiThreads / 32) * p.ph[0].n_tiles, abort_flag,
-                            p.dev_status)) {
-            ok = false;
-            break;
+          // wait until every GEMM1 tile of these rows has been written; if they are not yet,
+          // the weight tile and its scales (which do not depend on GEMM1) start towards L2
+          const int32_t* done = p.mt_done + (row0 >> 7);
+          const int target = (kEpiThreads / 32) * p.ph[0].n_tiles;
+          int seen;
+          asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(seen) : "l"(done) : "memory");
+          if (seen < target) {
+            prefetch_l2(ph.b_raw + static_cast<int64_t>(brow0) * (ph.K / 2),
+                        static_cast<int64_t>(kTileN) * (ph.K / 2));
+            prefetch_l2(sfb0, 2 * kt * 512);
+            if (!wait_counter(done, target, abort_flag, p.dev_status)) {
+              ok = false;
+              break;
+            }
           }
           fence_proxy_async_global();  // the TMA reads below follow the observed generic writes
         }
@@ -734,7 +740,6 @@ moe_status_t launch_plain_a(int mode, int act, const GemmParams& prm, int64_t un
                             cudaStream_t s);
 moe_status_t launch_plain_b(int mode, int act, const GemmParams& prm, int64_t units_max, size_t smem,
                             cudaStream_t s);
-moe_status_t launch_rows(int mode, const GemmParams& prm, int64_t units_max, size_t smem, cudaStream_t s);
 moe_status_t launch_chain_gated(int mode, int act, const GemmParams& prm, int64_t units_max, size_t smem,
                                 cudaStream_t s);
 moe_status_t launch_chain_plain_a(int mode, int act, const GemmParams& prm, int64_t units_max, size_t smem,

@@ -125,12 +125,11 @@ enum GemmMode : int {
   kChainReduce = 6,  // GEMM1 (kG1Fused) then GEMM2 (kG2Reduce) in one launch
 };
 
-// Batches of at most this many routed slots run GEMM1 and GEMM2 as one chained launch: the
-// GEMM2 tiles of a row tile start once its GEMM1 tiles are written, so the second weight
-// stream overlaps the first GEMM's tail instead of waiting for a kernel boundary.
-constexpr int64_t kChainMaxSlots = MOE_CHAIN_MAX_SLOTS;
-// Chained batches of at most this many tokens (so at most 16 rows per expert) run the
-// decode-shaped GEMMs: the weight tile is the MMA's M operand, the expert's rows its N = 16.
+// GEMM1 and GEMM2 run as one chained launch: the GEMM2 tiles of a row tile start once its
+// GEMM1 tiles are written, so the second weight stream overlaps the first GEMM's tail
+// instead of waiting for a kernel boundary. Batches of at most this many tokens (so at most
+// 16 rows per expert) run the decode-shaped GEMMs: the weight tile is the MMA's M operand,
+// the expert's rows its N = 16.
 constexpr int64_t kDecodeMaxTokens = MOE_DECODE_MAX_TOKENS;
 
 struct GemmLaunch {
@@ -159,6 +158,7 @@ struct GemmLaunch {
   float rsf = 1.0f;
 };
 
+// one GEMM on its own: the plain GEMM1 epilogues of the test hook (kG1Preact, kG1Act)
 moe_status_t launch_gemm(const GemmLaunch& g, cudaStream_t s);
 // GEMM1 (g1, kG1Fused) and GEMM2 (g2, kG2Rows or kG2Reduce) in one launch; mt_done holds
 // cap / 128 zeroed counters

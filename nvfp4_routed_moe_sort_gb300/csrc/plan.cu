@@ -22,9 +22,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_single_kernel(
     int32_t* __restrict__ padded_offsets, int32_t* __restrict__ row_to_slot, int32_t* __restrict__ token_to_row,
     int32_t* dev_status) {
   __shared__ PlanSmem sm;
-  pdl_trigger();
   zero_tables(sm, El);
   pdl_wait();
+  pdl_trigger();  // after the wait: a dependent that starts early finds every earlier kernel done
   __syncthreads();
   for (int64_t s = threadIdx.x; s < n; s += blockDim.x) {
     const int l = local_of(entry_id(ids, s, id_mask), off, El);
@@ -47,9 +47,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_hist_kernel(const int32_t* 
                                                                  int64_t n, int off, int El,
                                                                  int32_t* __restrict__ hist) {
   __shared__ int cnt[kMaxLocalExperts];
-  pdl_trigger();
   for (int i = threadIdx.x; i < El; i += blockDim.x) cnt[i] = 0;
   pdl_wait();
+  pdl_trigger();  // after the wait: a dependent that starts early finds every earlier kernel done
   __syncthreads();
   const int64_t b0 = static_cast<int64_t>(blockIdx.x) * kSlotsPerBlock;
   const int64_t b1 = min(n, b0 + kSlotsPerBlock);
@@ -67,25 +67,40 @@ __global__ void __launch_bounds__(kPlanThreads) plan_scan_kernel(int32_t* __rest
                                                                  int32_t* __restrict__ padded_offsets,
                                                                  int32_t* __restrict__ row_to_slot) {
   __shared__ PlanSmem sm;
+  constexpr int kBatch = 8;  // independent histogram loads in flight per thread
   pdl_trigger();
   pdl_wait();
   for (int l = threadIdx.x; l < El; l += blockDim.x) {
     int run = 0;
-    for (int b = 0; b < nb; ++b) {
-      const int h = hist[static_cast<int64_t>(b) * El + l];
-      hist[static_cast<int64_t>(b) * El + l] = run;
-      run += h;
+    for (int b0 = 0; b0 < nb; b0 += kBatch) {
+      int h[kBatch];
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) h[i] = b0 + i < nb ? hist[static_cast<int64_t>(b0 + i) * El + l] : 0;
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) run += h[i];
     }
     sm.cnt[l] = run;
   }
   __syncthreads();
   scan_padded(sm, El);
   __syncthreads();
+  // each block's first row per expert, in place over its histogram
   for (int l = threadIdx.x; l <= El; l += blockDim.x) {
     padded_offsets[l] = sm.cursor[l];
     if (l < El) {
       counts[l] = sm.cnt[l];
-      for (int b = 0; b < nb; ++b) hist[static_cast<int64_t>(b) * El + l] += sm.cursor[l];
+      int run = sm.cursor[l];
+      for (int b0 = 0; b0 < nb; b0 += kBatch) {
+        int h[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) h[i] = b0 + i < nb ? hist[static_cast<int64_t>(b0 + i) * El + l] : 0;
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i)
+          if (b0 + i < nb) {
+            hist[static_cast<int64_t>(b0 + i) * El + l] = run;
+            run += h[i];
+          }
+      }
     }
   }
   fill_padding(sm.cursor, sm.cnt, El, sm.cursor[El], cap, row_to_slot);

@@ -82,13 +82,15 @@ __global__ void __launch_bounds__(kPrologueThreads) small_prologue_kernel(
   __shared__ PlanSmem sm;
   __shared__ unsigned s_amax[kPrologueMaxRows];      // max |x| of each own token (bits of a non-negative float)
   __shared__ int32_t s_row[kPrologueMaxSlots];       // plan row of each slot
-  pdl_trigger();
   const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
   const bool lead = c == 0;
   const int n_own = (M - c + G - 1) / G;             // own tokens c + i*G, i < n_own
   zero_tables(sm, El);
   for (int i = threadIdx.x; i < n_own; i += kPrologueThreads) s_amax[i] = 0u;
   pdl_wait();
+  // after the wait: the GEMM launched early reads the routing ids and the weights before its
+  // own wait, and finds every kernel before this one done
+  pdl_trigger();
   if (lead && threadIdx.x < 2) tile_counters[threadIdx.x] = 0;
   for (int i = c * kPrologueThreads + threadIdx.x; i < n_mt; i += G * kPrologueThreads) mt_done[i] = 0;
   const int n = M * top_k;
@@ -198,27 +200,32 @@ __global__ void __launch_bounds__(kPrologueThreads) small_prologue_kernel(
   }
 }
 
-// Larger batches, after the plan: one warp per token computes its scale (per-token max |x|
-// over the row, then the row is read again from L1/L2), quantises each 16-value block once
-// (the arithmetic of quantize_rows_kernel) and stores its codes and scale straight into
-// every plan row of the token, so the quantised activations are never written token-major
-// and read back by a permutation. Block 0 zeroes the GEMM counters; an accumulated output's
-// FP32 copy of out is made by all threads.
+// Larger batches: one warp per token computes its scale (per-token max |x| over the row,
+// then the row is read again from L1/L2) and quantises each 16-value block once (the
+// arithmetic of quantize_rows_kernel) into the warp's shared-memory buffer; after the plan it
+// stores each block's codes and scale straight into every plan row of the token, so the
+// quantised activations are never written token-major and read back by a permutation. The
+// first token of every warp is read and quantised before the dependency wait (x is an
+// input of the step, and the plan's first kernel lets its dependents start only once every
+// earlier kernel is done), so that work overlaps the plan. Block 0 zeroes the GEMM counters;
+// an accumulated output's FP32 copy of out is made by all threads.
+// Dynamic shared memory: (warps per block) x (H/16) x 9 bytes.
 __global__ void __launch_bounds__(256) quantize_scatter_kernel(
     const uint16_t* __restrict__ x, int M, int H, int64_t ld, int per_token, int top_k,
     const int32_t* __restrict__ token_to_row, float* __restrict__ xs, uint8_t* __restrict__ aq,
     uint8_t* __restrict__ asf, int32_t* __restrict__ counters, int n_counters, const uint16_t* __restrict__ acc_init,
     float* __restrict__ acc) {
+  extern __shared__ uint8_t qs_smem[];
   pdl_trigger();
-  pdl_wait();
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  if (blockIdx.x == 0)
-    for (int i = threadIdx.x; i < n_counters; i += blockDim.x) counters[i] = 0;
   const int nblk = H / kBlock;
   const int kcols_p = static_cast<int>(roundup64(H, kTileK) / 16);
-  for (int64_t t = warp0; t < M; t += nwarps) {
+  uint2* s_codes = reinterpret_cast<uint2*>(qs_smem) + static_cast<int64_t>(wib) * nblk;
+  uint8_t* s_q = qs_smem + static_cast<int64_t>(blockDim.x >> 5) * nblk * 8 + static_cast<int64_t>(wib) * nblk;
+  // the token's scale and quantised blocks into the warp's buffers; returns the decode scale
+  auto stage = [&](int64_t t) -> float {
     const uint16_t* row = x + t * ld;
     float g = 1.0f, dec = 1.0f;
     if (per_token) {
@@ -235,18 +242,31 @@ __global__ void __launch_bounds__(256) quantize_scatter_kernel(
         dec = __fdiv_rn(amax, kGlobalNumerator);
       }
     }
-    // the token's plan rows (lane j holds slot j's row)
-    const int my_row = lane < top_k ? token_to_row[t * top_k + lane] : -1;
     for (int b = lane; b < nblk; b += 32) {
       float v[16];
       load_block16(row + b * kBlock, v);
       uint32_t codes[2];
-      const uint32_t q = quantize_block16(v, g, codes);
+      s_q[b] = static_cast<uint8_t>(quantize_block16(v, g, codes));
+      s_codes[b] = make_uint2(codes[0], codes[1]);
+    }
+    return dec;
+  };
+  float dec = warp0 < M ? stage(warp0) : 0.0f;
+  pdl_wait();
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < n_counters; i += blockDim.x) counters[i] = 0;
+  for (int64_t t = warp0; t < M; t += nwarps) {
+    if (t != warp0) dec = stage(t);
+    // the token's plan rows (lane j holds slot j's row); each lane stores the blocks it staged
+    const int my_row = lane < top_k ? token_to_row[t * top_k + lane] : -1;
+    for (int b = lane; b < nblk; b += 32) {
+      const uint2 c = s_codes[b];
+      const uint8_t q = s_q[b];
       for (int j = 0; j < top_k; ++j) {
         const int prow = j < 32 ? __shfl_sync(0xffffffffu, my_row, j) : token_to_row[t * top_k + j];
         if (prow < 0) continue;
-        *reinterpret_cast<uint2*>(aq + static_cast<int64_t>(prow) * (H / 2) + b * 8) = make_uint2(codes[0], codes[1]);
-        asf[sf_tile_offset(prow, b, kcols_p)] = static_cast<uint8_t>(q);
+        *reinterpret_cast<uint2*>(aq + static_cast<int64_t>(prow) * (H / 2) + b * 8) = c;
+        asf[sf_tile_offset(prow, b, kcols_p)] = q;
       }
     }
     // scale columns of the K padding (H not a multiple of 256) are zero
@@ -390,10 +410,19 @@ extern "C" moe_status_t moe_routed_forward(const uint16_t* x, int32_t M, int64_t
     const WorkspaceLayout L = workspace_layout(d, M, top_k, do_finalize);
     uint8_t* fb = static_cast<uint8_t*>(fwd);
     const bool accum = do_finalize == MOE_OUTPUT_ACCUMULATE;
-    const int64_t blocks = (static_cast<int64_t>(M) + 7) / 8;  // 8 warps (tokens) per block
+    // warps (tokens) per block: 8, fewer when a warp's H/16 x 9 staging bytes are large
+    const int64_t stage_bytes = d.H / 16 * 9;
+    int64_t wpb = (200 << 10) / stage_bytes;
+    wpb = wpb > 8 ? 8 : wpb;
+    MOE_CHECK(wpb >= 1, MOE_ERR_UNSUPPORTED_SHAPE);
+    const size_t qs_smem = static_cast<size_t>(wpb * stage_bytes);
+    if (qs_smem > (48 << 10))
+      MOE_CUDA(cudaFuncSetAttribute(quantize_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(qs_smem)));
+    const int64_t blocks = (static_cast<int64_t>(M) + wpb - 1) / wpb;
     const int64_t max_blocks = static_cast<int64_t>(num_sms()) * 16;
     st = launch_pdl(quantize_scatter_kernel, dim3(static_cast<unsigned>(blocks < max_blocks ? blocks : max_blocks)),
-                    dim3(256), 0, s, x, static_cast<int>(M), static_cast<int>(d.H), ld_x,
+                    dim3(static_cast<unsigned>(wpb * 32)), qs_smem, s, x, static_cast<int>(M), static_cast<int>(d.H), ld_x,
                     act_scale_mode == MOE_SCALE_PER_TOKEN ? 1 : 0, static_cast<int>(top_k),
                     static_cast<const int32_t*>(token_to_row), xs, fb + L.aq, fb + L.asf,
                     reinterpret_cast<int32_t*>(fb + L.sched),
