@@ -257,24 +257,23 @@ __global__ void __launch_bounds__(256) quantize_scatter_kernel(
     for (int i = threadIdx.x; i < n_counters; i += blockDim.x) counters[i] = 0;
   for (int64_t t = warp0; t < M; t += nwarps) {
     if (t != warp0) dec = stage(t);
-    // the token's plan rows (lane j holds slot j's row); each lane stores the blocks it staged
+    __syncwarp();  // the staged blocks are read by other lanes below
+    // the token's plan rows (lane j holds slot j's row): per row, 16-byte code vectors (two
+    // blocks) and 4-byte scale groups (the four scales of a 128x4 tile row are contiguous);
+    // H is a multiple of 128, so the blocks split evenly into both
     const int my_row = lane < top_k ? token_to_row[t * top_k + lane] : -1;
-    for (int b = lane; b < nblk; b += 32) {
-      const uint2 c = s_codes[b];
-      const uint8_t q = s_q[b];
-      for (int j = 0; j < top_k; ++j) {
-        const int prow = j < 32 ? __shfl_sync(0xffffffffu, my_row, j) : token_to_row[t * top_k + j];
-        if (prow < 0) continue;
-        *reinterpret_cast<uint2*>(aq + static_cast<int64_t>(prow) * (H / 2) + b * 8) = c;
-        asf[sf_tile_offset(prow, b, kcols_p)] = q;
-      }
+    const uint4* c16 = reinterpret_cast<const uint4*>(s_codes);
+    const uint32_t* q4 = reinterpret_cast<const uint32_t*>(s_q);
+    for (int j = 0; j < top_k; ++j) {
+      const int prow = j < 32 ? __shfl_sync(0xffffffffu, my_row, j) : token_to_row[t * top_k + j];
+      if (prow < 0) continue;
+      uint4* dst = reinterpret_cast<uint4*>(aq + static_cast<int64_t>(prow) * (H / 2));
+      for (int v = lane; v < nblk / 2; v += 32) dst[v] = c16[v];
+      // scale groups, then zero groups on the K padding (H not a multiple of 256)
+      for (int g = lane; g < kcols_p / 4; g += 32)
+        *reinterpret_cast<uint32_t*>(asf + sf_tile_offset(prow, 4 * g, kcols_p)) = g < nblk / 4 ? q4[g] : 0u;
     }
-    // scale columns of the K padding (H not a multiple of 256) are zero
-    for (int c = nblk + lane; c < kcols_p; c += 32)
-      for (int j = 0; j < top_k; ++j) {
-        const int prow = token_to_row[t * top_k + j];
-        if (prow >= 0) asf[sf_tile_offset(prow, c, kcols_p)] = 0;
-      }
+    __syncwarp();  // every lane's reads of the buffers precede the next token's staging
     if (lane == 0) xs[t] = dec;
   }
   if (acc != nullptr) {
