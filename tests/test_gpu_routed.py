@@ -20,6 +20,10 @@ CASES = {
                                 weight_seed=33),
     # separate kernels (too large for the prologue)
     "swiglu_ragged": mi.MoEConfig("swiglu_ragged", M=300, H=512, I=256, E=8, top_k=2, seed=11, weight_seed=11),
+    # the plan's three kernels and the quantiser storing into the plan rows, with K tails in
+    # both GEMMs (H and I = 128 mod 256: zero scale groups on the K padding)
+    "ktail_large": mi.MoEConfig("ktail_large", M=400, H=384, I=384, E=12, top_k=6, seed=34, weight_seed=34,
+                                local_offset=2, num_local=8),
 }
 
 
@@ -35,7 +39,7 @@ def _unrouted(cfg):
 @pytest.mark.parametrize("do_finalize", [True, False])
 def test_routed_equals_separate_calls(name, do_finalize):
     cfg = CASES[name]
-    ids, tw = _unrouted(cfg) if name in ("decode_ep", "relu2_small") else (None, None)
+    ids, tw = _unrouted(cfg) if name in ("decode_ep", "relu2_small", "ktail_large") else (None, None)
     p = Problem(cfg, ids, tw)
     if do_finalize:
         a = bf16_np(p.run_routed(True)).copy()
