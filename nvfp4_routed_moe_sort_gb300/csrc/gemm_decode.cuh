@@ -283,6 +283,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm_kernel(const __grid_c
     }
   }
   pdl_wait();  // the plan, the token rows and the counters come from earlier kernels
+  // the producer's claim of its offered unit goes out now; its round trip overlaps the
+  // plan load below (whether the unit is offered at all is known only after it)
+  int cas_old = 1;
+  if (threadIdx.x == 0 && static_cast<int>(blockIdx.x) < p.n_static &&
+      !((p.dbg_hooks & 2) && (blockIdx.x & 1)))
+    cas_old = atomicCAS(p.own + blockIdx.x, 0, 1);
   for (int i = threadIdx.x; i <= p.El; i += blockDim.x) s_off[i] = p.padded_offsets[i];
   __syncthreads();
   if (warp == 0) {
@@ -333,8 +339,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm_kernel(const __grid_c
         int u = -1;
         if (first) {
           first = false;
-          const bool skip = (p.dbg_hooks & 2) && (blockIdx.x & 1);
-          if (u_static >= 0 && !skip && atomicCAS(p.own + u_static, 0, 1) == 0) {
+          // the claim issued after the wait (flags past the offered range are never read)
+          if (u_static >= 0 && cas_old == 0) {
             u = u_static;
             atomicAdd(p.owned, 1);
           }

@@ -58,6 +58,7 @@ bool small_batch(int64_t M, int64_t k, int64_t H) {
 
 constexpr int kPrologueMaxRows = static_cast<int>(kPrologueMaxValues / 128);  // H >= 128
 constexpr int kPrologueMaxCtas = 32;
+constexpr int kPrologueStageBlocks = 1024;  // own 16-value blocks quantised during the plan scan
 
 // A grid of G <= 32 CTAs, CTA c taking tokens c, c + G, ... Every CTA builds the whole plan
 // in shared memory (at most 2048 slots: the one-block plan of plan_single_kernel, from the
@@ -71,7 +72,9 @@ constexpr int kPrologueMaxCtas = 32;
 //  (2) NVFP4 quantisation of its tokens' 16-value blocks (the arithmetic of
 //      quantize_rows_kernel), each block's 8 code bytes and scale byte stored straight into
 //      every plan row of the token (the permuted operand of GEMM1 and its 128x4 scale
-//      tiles): the quantised activations never make a round trip through memory.
+//      tiles): the quantised activations never make a round trip through memory. When the
+//      own blocks fit in shared memory they are quantised while warp 0 scans the plan, and
+//      only stored once the rows are placed.
 // Also its tokens' scales and, for an accumulated output, the FP32 copy of their rows of out.
 __global__ void __launch_bounds__(kPrologueThreads) small_prologue_kernel(
     const uint16_t* __restrict__ x, int M, int H, int64_t ld, int per_token, const int32_t* __restrict__ ids,
@@ -82,6 +85,8 @@ __global__ void __launch_bounds__(kPrologueThreads) small_prologue_kernel(
   __shared__ PlanSmem sm;
   __shared__ unsigned s_amax[kPrologueMaxRows];      // max |x| of each own token (bits of a non-negative float)
   __shared__ int32_t s_row[kPrologueMaxSlots];       // plan row of each slot
+  __shared__ uint2 s_code[kPrologueStageBlocks];     // own blocks' codes (when they fit)
+  __shared__ uint8_t s_qsc[kPrologueStageBlocks];    // and scale bytes
   const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
   const bool lead = c == 0;
   const int n_own = (M - c + G - 1) / G;             // own tokens c + i*G, i < n_own
@@ -114,8 +119,25 @@ __global__ void __launch_bounds__(kPrologueThreads) small_prologue_kernel(
     }
   }
   __syncthreads();
-  // (1) plan
-  scan_padded(sm, El);
+  // (1) plan: warp 0 scans the expert counts while the other warps quantise the own blocks
+  const bool staged = nb_own <= kPrologueStageBlocks;
+  if (threadIdx.x < 32) {
+    scan_padded(sm, El);
+  } else if (staged) {
+    for (int bi = threadIdx.x - 32; bi < nb_own; bi += kPrologueThreads - 32) {
+      const int i = bi / nblk, b = bi - i * nblk;
+      float g = 1.0f;
+      if (per_token) {
+        const float amax = __uint_as_float(s_amax[i]);
+        if (amax > 0.0f) g = __fdiv_rn(kGlobalNumerator, amax);
+      }
+      float v[16];
+      load_block16(x + static_cast<int64_t>(c + i * G) * ld + b * kBlock, v);
+      uint32_t codes[2];
+      s_qsc[bi] = static_cast<uint8_t>(quantize_block16(v, g, codes));
+      s_code[bi] = make_uint2(codes[0], codes[1]);
+    }
+  }
   __syncthreads();
   if (lead)
     for (int l = threadIdx.x; l <= El; l += kPrologueThreads) {
@@ -169,11 +191,19 @@ __global__ void __launch_bounds__(kPrologueThreads) small_prologue_kernel(
     }
     if (j == 0 && b == 0) xs[r] = dec;
     if (row < 0) continue;
-    float v[16];
-    load_block16(x + static_cast<int64_t>(r) * ld + b * kBlock, v);
-    uint32_t codes[2];
-    const uint32_t q = quantize_block16(v, g, codes);
-    *reinterpret_cast<uint2*>(aq + static_cast<int64_t>(row) * (H / 2) + b * 8) = make_uint2(codes[0], codes[1]);
+    uint2 code;
+    uint32_t q;
+    if (staged) {
+      code = s_code[i * nblk + b];
+      q = s_qsc[i * nblk + b];
+    } else {
+      float v[16];
+      load_block16(x + static_cast<int64_t>(r) * ld + b * kBlock, v);
+      uint32_t codes[2];
+      q = quantize_block16(v, g, codes);
+      code = make_uint2(codes[0], codes[1]);
+    }
+    *reinterpret_cast<uint2*>(aq + static_cast<int64_t>(row) * (H / 2) + b * 8) = code;
     asf[sf_tile_offset(row, b, kcols_p)] = static_cast<uint8_t>(q);
   }
   // zero scales on the K padding columns of the own tokens' routed rows (H not a multiple of 256)
