@@ -29,6 +29,9 @@ SMALL = {
     "decode_dense": mi.MoEConfig("decode_dense", M=16, H=384, I=256, E=4, top_k=3, seed=14, weight_seed=14),
     "relu2_decode": mi.MoEConfig("relu2_decode", M=13, H=512, I=384, E=10, top_k=4, act="relu2", seed=15,
                                  weight_seed=15, local_offset=2, num_local=6),
+    # decode-shaped, GEMM2 with more K chunks (I = 1536: six) than pipeline stages, so its
+    # tiles wait for the expert's GEMM1 tiles before loading; GEMM1 one K chunk (H = 256)
+    "decode_long_k2": mi.MoEConfig("decode_long_k2", M=6, H=256, I=1536, E=6, top_k=2, seed=16, weight_seed=16),
 }
 
 
@@ -118,7 +121,7 @@ def test_forward_matches_oracle(name, do_finalize):
         assert_close_output(bf16_np(g2)[real], ref["rows"][real], name + " rows")
 
 
-@pytest.mark.parametrize("name", ["swiglu_ragged", "relu2_ep_small", "decode_t8", "decode_dense", "relu2_decode"])
+@pytest.mark.parametrize("name", ["swiglu_ragged", "relu2_ep_small", "decode_t8", "decode_dense", "relu2_decode", "decode_long_k2"])
 def test_finalize_of_unfinalized_equals_finalized(name):
     # decode-sized batches combine inside the GEMM launch; the standalone combine of their
     # unfinalized rows must give the same bytes
