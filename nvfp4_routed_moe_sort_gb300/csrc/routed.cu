@@ -85,8 +85,9 @@ __global__ void __launch_bounds__(kPrologueThreads) small_prologue_kernel(
   __shared__ PlanSmem sm;
   __shared__ unsigned s_amax[kPrologueMaxRows];      // max |x| of each own token (bits of a non-negative float)
   __shared__ int32_t s_row[kPrologueMaxSlots];       // plan row of each slot
-  __shared__ uint2 s_code[kPrologueStageBlocks];     // own blocks' codes (when they fit)
-  __shared__ uint8_t s_qsc[kPrologueStageBlocks];    // and scale bytes
+  __shared__ __align__(16) uint2 s_code[kPrologueStageBlocks];    // own blocks' codes (when they fit)
+  __shared__ __align__(16) uint8_t s_qsc[kPrologueStageBlocks];   // and scale bytes
+  __shared__ int16_t s_loc[kPrologueMaxSlots];       // local expert of each slot, or -1
   const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
   const bool lead = c == 0;
   const int n_own = (M - c + G - 1) / G;             // own tokens c + i*G, i < n_own
@@ -105,6 +106,7 @@ __global__ void __launch_bounds__(kPrologueThreads) small_prologue_kernel(
   // (0) histogram of the routed slots per local expert; own tokens' maxima
   for (int s = threadIdx.x; s < n; s += kPrologueThreads) {
     const int l = local_of(entry_id(ids, s, id_mask), off, El);
+    s_loc[s] = static_cast<int16_t>(l);
     if (l >= 0) atomicAdd(&sm.cnt[l], 1);
   }
   if (per_token) {
@@ -158,7 +160,9 @@ __global__ void __launch_bounds__(kPrologueThreads) small_prologue_kernel(
   __syncthreads();
   place_range(ids, id_mask, 0, n, top_k, off, El, sm, nullptr, s_row, nullptr);
   __syncthreads();
-  // own tokens' slots: token_to_row, row_to_slot and the duplicate-expert check (as moe_plan)
+  // own tokens' slots: token_to_row, row_to_slot and the duplicate-expert check (as moe_plan:
+  // a routed slot naming the same expert as an earlier slot of its token; for local slots
+  // equal ids are equal local indices, kept in shared memory since the histogram)
   for (int it = threadIdx.x; it < n_own * top_k; it += kPrologueThreads) {
     const int i = it / top_k, j = it - i * top_k;
     const int sl = (c + i * G) * top_k + j;
@@ -166,53 +170,75 @@ __global__ void __launch_bounds__(kPrologueThreads) small_prologue_kernel(
     token_to_row[sl] = row;
     if (row >= 0) {
       row_to_slot[row] = sl;
-      const int id = entry_id(ids, sl, id_mask);
+      const int l = s_loc[sl];
       for (int q = sl - j; q < sl; ++q)
-        if (entry_id(ids, q, id_mask) == id) atomicOr(dev_status, MOE_DEV_DUPLICATE_EXPERT);
+        if (s_loc[q] == l) atomicOr(dev_status, MOE_DEV_DUPLICATE_EXPERT);
     }
   }
-  // (2) own tokens: one thread per (token, slot, block), consecutive threads on consecutive
-  // blocks of one plan row; each block is quantised by the same arithmetic for every slot
   const int kcols_p = static_cast<int>(roundup64(H, kTileK) / 16);  // scale columns incl. K padding
-  const int per_tok = top_k * nblk;
-  for (int it = threadIdx.x; it < n_own * per_tok; it += kPrologueThreads) {
-    const int i = it / per_tok, rem = it - i * per_tok;
-    const int j = rem / nblk, b = rem - j * nblk;
-    const int r = c + i * G;
-    const int row = s_row[r * top_k + j];
-    if (row < 0 && !(j == 0 && b == 0)) continue;
-    float g = 1.0f, dec = 1.0f;
-    if (per_token) {
-      const float amax = __uint_as_float(s_amax[i]);
-      if (amax > 0.0f) {
-        g = __fdiv_rn(kGlobalNumerator, amax);
-        dec = __fdiv_rn(amax, kGlobalNumerator);
+  if (staged) {
+    // (2) the staged blocks into every plan row of their token: per row 16-byte code vectors
+    // (two blocks) and 4-byte scale groups (the four scales of a 128x4 tile row are
+    // contiguous), zero groups on the K padding; H is a multiple of 128, so the blocks split
+    // evenly into both
+    const int nv = nblk / 2, ng = kcols_p / 4, per_row = nv + ng;
+    const uint4* c16 = reinterpret_cast<const uint4*>(s_code);
+    const uint32_t* q4 = reinterpret_cast<const uint32_t*>(s_qsc);
+    for (int it = threadIdx.x; it < n_own * top_k * per_row; it += kPrologueThreads) {
+      const int sl = it / per_row, w = it - sl * per_row;  // own slot: token i, slot j
+      const int i = sl / top_k, j = sl - i * top_k;
+      const int row = s_row[(c + i * G) * top_k + j];
+      if (row < 0) continue;
+      if (w < nv) {
+        reinterpret_cast<uint4*>(aq + static_cast<int64_t>(row) * (H / 2))[w] = c16[i * nv + w];
+      } else {
+        const int g = w - nv;
+        *reinterpret_cast<uint32_t*>(asf + sf_tile_offset(row, 4 * g, kcols_p)) = g < nblk / 4 ? q4[i * (nblk / 4) + g] : 0u;
       }
     }
-    if (j == 0 && b == 0) xs[r] = dec;
-    if (row < 0) continue;
-    uint2 code;
-    uint32_t q;
-    if (staged) {
-      code = s_code[i * nblk + b];
-      q = s_qsc[i * nblk + b];
-    } else {
+    for (int i = threadIdx.x; i < n_own; i += kPrologueThreads) {
+      float dec = 1.0f;
+      if (per_token) {
+        const float amax = __uint_as_float(s_amax[i]);
+        if (amax > 0.0f) dec = __fdiv_rn(amax, kGlobalNumerator);
+      }
+      xs[c + i * G] = dec;
+    }
+  } else {
+    // (2) own tokens: one thread per (token, slot, block), consecutive threads on consecutive
+    // blocks of one plan row; each block is quantised by the same arithmetic for every slot
+    const int per_tok = top_k * nblk;
+    for (int it = threadIdx.x; it < n_own * per_tok; it += kPrologueThreads) {
+      const int i = it / per_tok, rem = it - i * per_tok;
+      const int j = rem / nblk, b = rem - j * nblk;
+      const int r = c + i * G;
+      const int row = s_row[r * top_k + j];
+      if (row < 0 && !(j == 0 && b == 0)) continue;
+      float g = 1.0f, dec = 1.0f;
+      if (per_token) {
+        const float amax = __uint_as_float(s_amax[i]);
+        if (amax > 0.0f) {
+          g = __fdiv_rn(kGlobalNumerator, amax);
+          dec = __fdiv_rn(amax, kGlobalNumerator);
+        }
+      }
+      if (j == 0 && b == 0) xs[r] = dec;
+      if (row < 0) continue;
       float v[16];
       load_block16(x + static_cast<int64_t>(r) * ld + b * kBlock, v);
       uint32_t codes[2];
-      q = quantize_block16(v, g, codes);
-      code = make_uint2(codes[0], codes[1]);
+      const uint32_t q = quantize_block16(v, g, codes);
+      *reinterpret_cast<uint2*>(aq + static_cast<int64_t>(row) * (H / 2) + b * 8) = make_uint2(codes[0], codes[1]);
+      asf[sf_tile_offset(row, b, kcols_p)] = static_cast<uint8_t>(q);
     }
-    *reinterpret_cast<uint2*>(aq + static_cast<int64_t>(row) * (H / 2) + b * 8) = code;
-    asf[sf_tile_offset(row, b, kcols_p)] = static_cast<uint8_t>(q);
-  }
-  // zero scales on the K padding columns of the own tokens' routed rows (H not a multiple of 256)
-  const int npad = kcols_p - nblk;
-  for (int it = threadIdx.x; it < n_own * top_k * npad; it += kPrologueThreads) {
-    const int sl = it / npad;                           // own slot index: token i, slot j
-    const int i = sl / top_k, j = sl - i * top_k;
-    const int row = s_row[(c + i * G) * top_k + j];
-    if (row >= 0) asf[sf_tile_offset(row, nblk + (it - sl * npad), kcols_p)] = 0;
+    // zero scales on the K padding columns of the own tokens' routed rows (H not a multiple of 256)
+    const int npad = kcols_p - nblk;
+    for (int it = threadIdx.x; it < n_own * top_k * npad; it += kPrologueThreads) {
+      const int sl = it / npad;                         // own slot index: token i, slot j
+      const int i = sl / top_k, j = sl - i * top_k;
+      const int row = s_row[(c + i * G) * top_k + j];
+      if (row >= 0) asf[sf_tile_offset(row, nblk + (it - sl * npad), kcols_p)] = 0;
+    }
   }
   // accumulated output: acc = fp32(out) on the own tokens' rows
   if (acc != nullptr) {
