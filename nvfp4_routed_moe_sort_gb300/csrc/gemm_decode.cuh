@@ -286,9 +286,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm_kernel(const __grid_c
   // the producer's claim of its offered unit goes out now; its round trip overlaps the
   // plan load below (whether the unit is offered at all is known only after it)
   int cas_old = 1;
-  if (threadIdx.x == 0 && static_cast<int>(blockIdx.x) < p.n_static &&
-      !((p.dbg_hooks & 2) && (blockIdx.x & 1)))
-    cas_old = atomicCAS(p.own + blockIdx.x, 0, 1);
+  int next_claim = 0;  // the producer's counter claim for its next unit, issued one unit early
+  if (threadIdx.x == 0) {
+    if (static_cast<int>(blockIdx.x) < p.n_static && !((p.dbg_hooks & 2) && (blockIdx.x & 1)))
+      cas_old = atomicCAS(p.own + blockIdx.x, 0, 1);
+    next_claim = atomicAdd(p.tile_counter, 1);
+  }
   for (int i = threadIdx.x; i <= p.El; i += blockDim.x) s_off[i] = p.padded_offsets[i];
   __syncthreads();
   if (warp == 0) {
@@ -347,7 +350,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm_kernel(const __grid_c
         }
         while (u < 0) {
           if (u_held < 0) {
-            u_held = n_first + atomicAdd(p.tile_counter, 1);
+            // the claim issued one unit ago; the next one goes out now, so its round trip
+            // overlaps this unit's loads
+            u_held = n_first + next_claim;
+            next_claim = atomicAdd(p.tile_counter, 1);
             if (u_held < units0) {  // GEMM1 units need no sweep
               u = u_held;
               u_held = -1;
