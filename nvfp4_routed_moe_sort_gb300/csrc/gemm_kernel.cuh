@@ -551,6 +551,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       sparse_compute<kEpi1, MOE_ACT_IDENTITY>(p, p.ph[1], threadIdx.x - 64, 0, 0, 0, 1, s_stage, s_slot, s_scal, true);
   }
   pdl_wait();  // the plan, activations and tile counter come from earlier kernels
+  // the producer's first claim goes out now (its round trip overlaps the plan load); each
+  // later claim is issued one unit early, while the current unit's loads go out
+  int next_claim = 0;
+  if (threadIdx.x == 0) next_claim = atomicAdd(p.tile_counter, 1);
   for (int i = threadIdx.x; i <= p.El; i += blockDim.x) s_off[i] = p.padded_offsets[i];
   tc_fence_before();
   __syncthreads();
@@ -581,7 +585,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       while (ok) {
         // claim the next unit (in order, from the global counter) and publish its id
         if (!mbar_wait(&unit_empty[rslot], rphase ^ 1, abort_flag, p.dev_status)) { ok = false; break; }
-        int u = atomicAdd(p.tile_counter, 1);
+        // claims increase per CTA, so a GEMM2 tile never waits behind a GEMM1 tile that its
+        // own CTA has claimed but not started
+        int u = next_claim;
+        next_claim = atomicAdd(p.tile_counter, 1);
         if (u >= total_units) u = -1;
         unit_ring[rslot] = u;
         mbar_arrive(&unit_full[rslot]);
