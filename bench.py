@@ -59,6 +59,32 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+# --------------------------------------------------------------------------- replicas
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest of every rank's x, returned on every rank (x itself for one process). The
+    whole job is timed by its slowest replica; `device` is where the reduction tensor lives
+    (the GPU for NCCL, None for gloo)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(tokens_per_rank: int, ms_slowest: float, world: int) -> float:
+    """Whole-job tokens/s: `world` independent replicas, each taking tokens_per_rank tokens
+    per step, timed by the slowest one."""
+    return world * tokens_per_rank / (ms_slowest * 1e-3)
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
 # --------------------------------------------------------------------------- algorithmic work
 def kernel_work(cfg, ids):
     """Per-launch algorithmic bytes and FLOPs of each kernel of one step (no padding rows)."""
@@ -234,8 +260,7 @@ def run_gpu(args, cfg, rank, world):
         flush()
         graph.replay()
     torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
+    barrier(world)
     s_ev, e_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(dev.index)
     clocks.start()
@@ -250,6 +275,7 @@ def run_gpu(args, cfg, rank, world):
         e_ev.synchronize()
         step_times.append(s_ev.elapsed_time(e_ev))
     torch.cuda.synchronize()
+    barrier(world)
     wall = time.perf_counter() - t0
     clk = clocks.stop()
     # kernel boundaries: the same calls launched eagerly with an event between kernels. A
@@ -276,11 +302,7 @@ def run_gpu(args, cfg, rank, world):
     names = ["prologue", "gemm1", "gemm2", "combine"]
     per = {n: [t[c] for t in kern_times] for c, n in enumerate(names)}
     steps_ms = step_times
-    ms = float(np.mean(steps_ms))
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(float(np.mean(steps_ms)), world, dev)
     work, stepw, R, active = kernel_work(cfg, ids)
     kern_ms = {n: float(np.mean(v)) for n, v in per.items()}
     # GEMM1 and GEMM2 run as one launch (its time is the gemm1 interval): the decode kernel
@@ -307,6 +329,9 @@ def run_gpu(args, cfg, rank, world):
     step_roof_s = max(stepw["bytes"] / (peaks["hbm_gbs"] * 1e9), stepw["flops"] / (fp4_peak * 1e12))
     # end to end through the public API with host buffers
     e2e = None if args.no_e2e else run_e2e(layer, x, ids, tw, dev, max(3, min(K, 50)), flush)
+    if e2e is not None:  # the whole job end to end: every replica's copies and step, the slowest
+        e2e["ms_per_step"] = max_over_ranks(e2e["ms_per_step"], world, dev)
+        e2e["value"] = replica_throughput(M, e2e["ms_per_step"], world)
     # the same graph with a write-only flush (its dirty lines are written back during the step)
     wo = L2Flush(dev, clean=False)
     wo_times = []
@@ -326,7 +351,7 @@ def run_gpu(args, cfg, rank, world):
     else:
         launches_per_step = (1 if M * k <= 2048 else 3) + 3
     res = {
-        "metric": METRIC, "value": world * M / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "metric": METRIC, "value": replica_throughput(M, ms, world), "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "nvfp4 (e2m1 x e2m1, e4m3 block scales, fp32 accumulate)", "data": "synthetic",
         "config": {"workload": workload_name(cfg), "tokens": M, "hidden": cfg.H, "inter": cfg.I,
