@@ -24,6 +24,14 @@ CASES = {
     # both GEMMs (H and I = 128 mod 256: zero scale groups on the K padding)
     "ktail_large": mi.MoEConfig("ktail_large", M=400, H=384, I=384, E=12, top_k=6, seed=34, weight_seed=34,
                                 local_offset=2, num_local=8),
+    # size limits: exactly 2048 slots and M*H = 2^17 (the largest fused-prologue batch); 2051
+    # slots (the separate kernels, a two-block plan); 17 tokens (just past the decode-shaped
+    # GEMMs); the largest local expert count (512) with expert-parallel masking
+    "slots_2048": mi.MoEConfig("slots_2048", M=256, H=512, I=256, E=16, top_k=8, seed=35, weight_seed=35),
+    "slots_2051": mi.MoEConfig("slots_2051", M=293, H=256, I=256, E=16, top_k=7, seed=36, weight_seed=36),
+    "decode_m17": mi.MoEConfig("decode_m17", M=17, H=512, I=256, E=8, top_k=4, seed=37, weight_seed=37),
+    "experts_512": mi.MoEConfig("experts_512", M=40, H=256, I=128, E=600, top_k=3, seed=38, weight_seed=38,
+                                local_offset=50, num_local=512),
 }
 
 
