@@ -32,6 +32,9 @@ CASES = {
     "decode_m17": mi.MoEConfig("decode_m17", M=17, H=512, I=256, E=8, top_k=4, seed=37, weight_seed=37),
     "experts_512": mi.MoEConfig("experts_512", M=40, H=256, I=128, E=600, top_k=3, seed=38, weight_seed=38,
                                 local_offset=50, num_local=512),
+    # a very wide row: 2048 blocks per token, more than the prologue stages in shared memory
+    # (it quantises after placing the rows instead); GEMM1 with 128 K chunks
+    "wide_h": mi.MoEConfig("wide_h", M=3, H=32768, I=128, E=4, top_k=2, seed=39, weight_seed=39),
 }
 
 
