@@ -417,7 +417,7 @@ def run_e2e(layer, x, ids, tw, dev, steps, flush):
     ms = float(np.mean(times))
     return {"value": M / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
             "h2d_bytes_per_step": int(nb_x + nb_id + nb_tw), "d2h_bytes_per_step": int(hout.numel() * 2),
-            "h2d_copies_per_step": 1}
+            "h2d_copies_per_step": 1, "output": "finalized"}
 
 
 # --------------------------------------------------------------------------- oracle arm
