@@ -196,9 +196,11 @@ def setup_gpu(cfg, dev):
 def kernel_source_hash() -> str:
     """sha256 prefix of the GEMM kernel sources (gemm_kernel.cuh, gemm_decode.cuh, common.cuh)."""
     csrc = os.path.join(ROOT, "nvfp4_routed_moe_sort_gb300", "csrc")
-    data = b"".join(open(os.path.join(csrc, f), "rb").read()
-                    for f in ("gemm_kernel.cuh", "gemm_decode.cuh", "common.cuh"))
-    return hashlib.sha256(data).hexdigest()[:16]
+    h = hashlib.sha256()
+    for name in ("gemm_kernel.cuh", "gemm_decode.cuh", "common.cuh"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def traffic_from_profiles(kernel: str, workload: str):

@@ -22,7 +22,8 @@ def lib():
 
 
 def _declared():
-    src = open(HEADER).read()
+    with open(HEADER) as f:
+        src = f.read()
     return sorted(set(re.findall(r"^MOE_API [^(]*?\b(moe_\w+)\(", src, flags=re.M)))
 
 

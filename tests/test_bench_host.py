@@ -33,7 +33,8 @@ def test_kernel_work_hand_example():
 
 def test_traffic_lookup_follows_the_kernel_hash(monkeypatch):
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
-    rows = [ln.split() for ln in open(path) if ln.strip() and not ln.startswith("#")]
+    with open(path) as f:
+        rows = [ln.split() for ln in f if ln.strip() and not ln.startswith("#")]
     assert rows, "no traffic rows"
     h = bench.kernel_source_hash()
     for workload, kernel, nbytes, _, row_hash in rows:

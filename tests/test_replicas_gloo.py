@@ -35,7 +35,7 @@ def _replica(rank: int, world: int, port: int, local_ms, results):
 
 def test_replicas_are_timed_by_the_slowest_rank():
     world, local_ms = 2, [0.05, 0.08]
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         results = m.dict()
         mp.spawn(_replica, args=(world, _free_port(), local_ms, results), nprocs=world, join=True)
         got = dict(results)
