@@ -87,24 +87,52 @@ def barrier(world: int):
 
 # --------------------------------------------------------------------------- algorithmic work
 def kernel_work(cfg, ids):
-    """Per-launch algorithmic bytes and FLOPs of each kernel of one step (no padding rows)."""
+    """Per-launch work of each kernel of one step (no padding rows, no unused experts).
+
+    `bytes` is the scope table's algorithmic count: the weights of the active local experts
+    and their alphas, and the layer's own inputs and outputs (BF16 hidden states in, BF16
+    output out, routing ids and weights), each charged to the kernel that reads or writes
+    it; intermediates and permuted copies are excluded, since an implementation may avoid
+    them, so the kernels' `bytes` sum to the whole step's. `bytes_incl_intermediates` adds
+    what this implementation writes and reads back between its kernels (the NVFP4 activation
+    pack and its permuted rows, the NVFP4 intermediate, the BF16 expert rows)."""
     l = ids.astype(np.int64) - cfg.local_offset
     valid = (l >= 0) & (l < cfg.El)
     R = int(valid.sum())
     active = int(np.unique(l[valid]).size)
     M, H, I, N1, k = cfg.M, cfg.H, cfg.I, cfg.N1, cfg.top_k
     w = {
-        "quantize": {"bytes": M * H * 2 + M * H * NV + M * 4, "flops": 0.0},
-        "plan": {"bytes": M * k * 4 * 2 + cfg.El * 8, "flops": 0.0},
-        "permute": {"bytes": 2 * R * H * NV, "flops": 0.0},
-        "gemm1": {"bytes": active * N1 * H * NV + R * H * NV + R * I * NV + cfg.El * 4,
+        "quantize": {"bytes": M * H * 2, "bytes_incl_intermediates": M * H * 2 + M * H * NV + M * 4,
+                     "flops": 0.0},
+        "plan": {"bytes": M * k * 4, "bytes_incl_intermediates": M * k * 4 * 2 + cfg.El * 8, "flops": 0.0},
+        "permute": {"bytes": 0, "bytes_incl_intermediates": 2 * R * H * NV, "flops": 0.0},
+        "gemm1": {"bytes": active * N1 * H * NV + cfg.El * 4,
+                  "bytes_incl_intermediates": active * N1 * H * NV + R * H * NV + R * I * NV + cfg.El * 4,
                   "flops": 2.0 * R * H * N1},
-        "gemm2": {"bytes": active * H * I * NV + R * I * NV + R * H * 2 + cfg.El * 4,
+        "gemm2": {"bytes": active * H * I * NV + cfg.El * 4,
+                  "bytes_incl_intermediates": active * H * I * NV + R * I * NV + R * H * 2 + cfg.El * 4,
                   "flops": 2.0 * R * I * H},
-        "finalize": {"bytes": R * H * 2 + M * k * 8 + M * H * 2, "flops": 0.0},
+        "finalize": {"bytes": M * H * 2 + M * k * 4,
+                     "bytes_incl_intermediates": R * H * 2 + M * k * 8 + M * H * 2, "flops": 0.0},
     }
     step = mi.algorithmic_work(cfg, ids, finalize=True)
     return w, step, R, active
+
+
+def roofline(bytes_, flops, t_s, peaks):
+    """Roofline of one launch: the bound is the larger of bytes at the HBM peak and FLOPs at
+    the FP4 tensor peak; frac = that time / the measured time t_s."""
+    fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
+    hbm_time = bytes_ / (peaks["hbm_gbs"] * 1e9)
+    tc_time = flops / (fp4_peak * 1e12)
+    if hbm_time >= tc_time:
+        r = {"bound": "hbm", "achieved": bytes_ / t_s / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    else:
+        r = {"bound": "tensor", "achieved": flops / t_s / 1e12, "peak": fp4_peak, "unit": "TFLOP/s"}
+    r["frac"] = r["achieved"] / r["peak"]
+    r["peak_source"] = (f"{peaks['source']} HBM copy" if r["bound"] == "hbm"
+                        else f"{peaks['source']} bf16 burst x {FP4_OVER_BF16:g} (nominal FP4/BF16)")
+    return r
 
 
 # --------------------------------------------------------------------------- clocks
@@ -160,13 +188,16 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------- GPU arm
-def setup_gpu(cfg, dev):
+def weight_key(cfg) -> tuple:
+    """What the prepared layer of a workload depends on: workloads with equal keys share it."""
+    return (cfg.H, cfg.I, cfg.E, cfg.act, cfg.weight_seed, cfg.local_offset, cfg.El, cfg.fc2_input_scale,
+            cfg.scale_mode)
+
+
+def setup_layer(cfg, dev):
     import torch
 
     import nvfp4_routed_moe_sort_gb300 as pkg
-    x = mi.hidden_bf16(cfg, dev)
-    ids, tw = mi.routing(cfg)
-    q1, q2 = [], []
     # draw and quantise one expert at a time (the BF16 stacks of the large configs are 22 GB)
     El = cfg.El
     d1 = torch.empty(El, cfg.N1, cfg.H // 2, dtype=torch.uint8, device=dev)
@@ -190,7 +221,13 @@ def setup_gpu(cfg, dev):
                                local_expert_offset=cfg.local_offset, fc2_input_scale=cfg.fc2_input_scale,
                                scale_mode=cfg.scale_mode)
     torch.cuda.synchronize()
-    return layer, x, ids, tw
+    return layer
+
+
+def setup_inputs(cfg, dev):
+    x = mi.hidden_bf16(cfg, dev)
+    ids, tw = mi.routing(cfg)
+    return x, ids, tw
 
 
 def kernel_source_hash() -> str:
@@ -237,14 +274,11 @@ class L2Flush:
             self.sink = self.r.sum()
 
 
-def run_gpu(args, cfg, rank, world):
+def measure(args, cfg, layer, x, ids, tw, dev, world, with_e2e: bool):
+    """One workload: K timed CUDA-graph replays of the whole step (L2 flushed between them),
+    the per-kernel split from eager calls, the rooflines, and optionally the end-to-end run."""
     import torch
 
-    dev = torch.device(f"cuda:{int(os.environ.get('LOCAL_RANK', 0))}")
-    torch.cuda.set_device(dev)
-    from nvfp4_routed_moe_sort_gb300.build import build
-    build()
-    layer, x, ids, tw = setup_gpu(cfg, dev)
     ids_t = torch.from_numpy(ids).to(dev)
     tw_t = torch.from_numpy(tw).to(dev)
     M, k = ids.shape
@@ -303,34 +337,29 @@ def run_gpu(args, cfg, rank, world):
     # prologue = quantise + plan + permute (one kernel for small batches)
     names = ["prologue", "gemm1", "gemm2", "combine"]
     per = {n: [t[c] for t in kern_times] for c, n in enumerate(names)}
-    steps_ms = step_times
-    ms = max_over_ranks(float(np.mean(steps_ms)), world, dev)
+    ms = max_over_ranks(float(np.mean(step_times)), world, dev)
     work, stepw, R, active = kernel_work(cfg, ids)
     kern_ms = {n: float(np.mean(v)) for n, v in per.items()}
     # GEMM1 and GEMM2 run as one launch (its time is the gemm1 interval): the decode kernel
     # (weights as the 128-row MMA operand) up to 16 tokens, else the chained one
     dom = "gemm1+gemm2 (decode)" if M <= 16 else "gemm1+gemm2 (chained)"
     kern_ms[dom] = kern_ms.pop("gemm1") + kern_ms.pop("gemm2")
-    work[dom] = {key: work["gemm1"][key] + work["gemm2"][key] for key in ("bytes", "flops")}
+    work[dom] = {key: work["gemm1"][key] + work["gemm2"][key]
+                 for key in ("bytes", "bytes_incl_intermediates", "flops")}
     peaks = load_peaks()
-    fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
     t_dom = kern_ms[dom] * 1e-3
-    bytes_dom = work[dom]["bytes"]
-    flops_dom = work[dom]["flops"]
-    hbm_time = bytes_dom / (peaks["hbm_gbs"] * 1e9)
-    tc_time = flops_dom / (fp4_peak * 1e12)
-    if hbm_time >= tc_time:
-        roof = {"bound": "hbm", "achieved": bytes_dom / t_dom / 1e9, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
-    else:
-        roof = {"bound": "tensor", "achieved": flops_dom / t_dom / 1e12, "peak": fp4_peak, "unit": "TFLOP/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof = roofline(work[dom]["bytes"], work[dom]["flops"], t_dom, peaks)
     roof["kernel"] = dom
-    roof["peak_source"] = (f"{peaks['source']} HBM copy" if roof["bound"] == "hbm"
-                           else f"{peaks['source']} bf16 burst x {FP4_OVER_BF16:g} (nominal FP4/BF16)")
+    roof["bytes"] = work[dom]["bytes"]
+    roof["flops"] = work[dom]["flops"]
     roof["traffic"] = traffic_from_profiles(dom, cfg.name)
+    incl = roofline(work[dom]["bytes_incl_intermediates"], work[dom]["flops"], t_dom, peaks)
+    roof["frac_incl_intermediates"] = incl["frac"]
+    roof["bytes_incl_intermediates"] = work[dom]["bytes_incl_intermediates"]
+    fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
     step_roof_s = max(stepw["bytes"] / (peaks["hbm_gbs"] * 1e9), stepw["flops"] / (fp4_peak * 1e12))
     # end to end through the public API with host buffers
-    e2e = None if args.no_e2e else run_e2e(layer, x, ids, tw, dev, max(3, min(K, 50)), flush)
+    e2e = run_e2e(layer, x, ids, tw, dev, max(3, min(K, 50)), flush) if with_e2e else None
     if e2e is not None:  # the whole job end to end: every replica's copies and step, the slowest
         e2e["ms_per_step"] = max_over_ranks(e2e["ms_per_step"], world, dev)
         e2e["value"] = replica_throughput(M, e2e["ms_per_step"], world)
@@ -344,7 +373,7 @@ def run_gpu(args, cfg, rank, world):
         e_ev.record()
         e_ev.synchronize()
         wo_times.append(s_ev.elapsed_time(e_ev))
-    del wo
+    del wo, flush, graph
     small = M * k <= 2048 and M * cfg.H <= (1 << 17)
     # small: prologue, GEMMs (one launch), combine; otherwise the plan (one kernel up to 2048
     # slots, else three), the quantiser storing into the plan rows, GEMMs, combine
@@ -352,14 +381,15 @@ def run_gpu(args, cfg, rank, world):
         launches_per_step = 3
     else:
         launches_per_step = (1 if M * k <= 2048 else 3) + 3
-    res = {
+    return {
         "metric": METRIC, "value": replica_throughput(M, ms, world), "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "nvfp4 (e2m1 x e2m1, e4m3 block scales, fp32 accumulate)", "data": "synthetic",
         "config": {"workload": workload_name(cfg), "tokens": M, "hidden": cfg.H, "inter": cfg.I,
                    "experts": cfg.E, "top_k": k, "routed_rows": R, "active_experts": active,
                    "l2": ("flushed between steps outside the timed events: 256 MB write"
-                          + (", then 256 MB read of a second buffer (clean lines)" if flush.r is not None else "")),
+                          + (", then 256 MB read of a second buffer (clean lines)"
+                             if args.l2_flush == "write+read" else "")),
                    "output": args.output,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roof,
@@ -377,6 +407,55 @@ def run_gpu(args, cfg, rank, world):
         "clocks": clk,
         "wall_s_timed_region": wall,
     }
+
+
+# the metric's other configurations, measured in the same run after the headline one
+EXTRA_WORKLOADS = ["decode_t4", "wide_decode", "prefill_uniform", "prefill_skewed", "relu2_ep"]
+
+
+def workload_summary(r: dict) -> dict:
+    """The fields of one extra workload's measurement kept in the `workloads` object."""
+    c = r["config"]
+    return {"workload": c["workload"], "tokens": c["tokens"], "routed_rows": c["routed_rows"],
+            "active_experts": c["active_experts"], "ms_per_step": r["ms_per_step"], "tokens_per_s": r["value"],
+            "step_roofline": r["step_roofline"], "roofline": r["roofline"], "kernels_ms": r["kernels_ms"],
+            "eager_ms_per_step": r["eager_ms_per_step"], "gpu_launches": r["gpu_launches"], "clocks": r["clocks"]}
+
+
+def run_gpu(args, cfg, rank, world):
+    import torch
+
+    dev = torch.device(f"cuda:{int(os.environ.get('LOCAL_RANK', 0))}")
+    torch.cuda.set_device(dev)
+    from nvfp4_routed_moe_sort_gb300.build import build
+    build()
+    layers = {}
+
+    def layer_for(c):
+        key = weight_key(c)
+        if key not in layers:
+            layers.clear()            # one weight set resident at a time
+            torch.cuda.empty_cache()
+            layers[key] = setup_layer(c, dev)
+        return layers[key]
+
+    x, ids, tw = setup_inputs(cfg, dev)
+    res = measure(args, cfg, layer_for(cfg), x, ids, tw, dev, world, with_e2e=not args.no_e2e)
+    extra = [] if args.workloads == "none" else (
+        EXTRA_WORKLOADS if args.workloads == "all" else [w for w in args.workloads.split(",") if w])
+    extra = [w for w in extra if w != args.workload and not args.set]
+    if extra:
+        # group workloads that share a weight set, so each set is prepared once
+        order = sorted(extra, key=lambda w: (weight_key(mi.CONFIGS[w]) != weight_key(cfg),
+                                             str(weight_key(mi.CONFIGS[w]))))
+        res["workloads"] = {}
+        for w in order:
+            c = mi.CONFIGS[w]
+            xw, idw, tww = setup_inputs(c, dev)
+            r = measure(args, c, layer_for(c), xw, idw, tww, dev, world, with_e2e=False)
+            res["workloads"][w] = workload_summary(r)
+            del xw
+        res["workloads"] = {w: res["workloads"][w] for w in extra}
     return res
 
 
@@ -543,9 +622,12 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer run (profiling)")
     ap.add_argument("--set", action="append", default=[], metavar="FIELD=VALUE",
                     help="override a workload field (e.g. E=64 M=1024) for smaller profiling cases")
+    ap.add_argument("--workloads", default="all",
+                    help="the other configurations measured in the same run and reported in the `workloads` "
+                         "object: all (default), none, or a comma-separated list")
     args = ap.parse_args()
     if args.warmup < 3:
-        args.warmup = 3
+        ap.error("--warmup must be at least 3 (untimed warm-up steps before the timed region)")
     cfg = mi.CONFIGS[args.workload]
     for kv in args.set:
         k_, v_ = kv.split("=", 1)

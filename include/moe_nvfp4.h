@@ -15,8 +15,10 @@
  * Conventions shared by every entry point:
  *  - Every pointer argument is a DEVICE pointer unless stated otherwise, owned by
  *    the caller, and must be 16-byte aligned. The library never allocates device
- *    memory, never synchronises the stream and keeps no state between calls, so
- *    every call can be captured in a CUDA graph with fixed, capacity-sized buffers.
+ *    memory, never synchronises the stream and keeps no state between calls (one
+ *    exception: the fixed scratch array of moe_plan_noalloc, below), so every call
+ *    can be captured in a CUDA graph with fixed, capacity-sized buffers. Test hooks
+ *    live in a separate test build (moe_nvfp4_test.h), not in this library.
  *  - All work is enqueued on `stream` (a cudaStream_t; NULL = legacy default stream).
  *  - Arguments are validated on the host before anything is launched; a bad
  *    argument returns a status and launches nothing. A launch failure returns
@@ -45,7 +47,7 @@
 extern "C" {
 #endif
 
-#define MOE_NVFP4_ABI_VERSION 2
+#define MOE_NVFP4_ABI_VERSION 3
 
 #if defined(__GNUC__)
 #define MOE_API __attribute__((visibility("default")))
@@ -67,7 +69,8 @@ typedef enum {
 
 /* Bits OR-ed into *dev_status by the kernels. */
 #define MOE_DEV_DUPLICATE_EXPERT 1 /* a token names the same local expert twice ([CUDNN] "distinct experts") */
-#define MOE_DEV_TIMEOUT 2          /* a pipeline wait in a GEMM kernel gave up (bounded spin) */
+#define MOE_DEV_TIMEOUT 2          /* a bounded wait in a GEMM kernel gave up after 2 s; the kernel
+                                      abandoned its remaining tiles and returned (outputs undefined) */
 
 /* Expert activations. [MCORE] flashinfer_routed_nvfp4_moe(activation_type): squared-ReLU or
  * SwiGLU experts; [CUDNN] Activation functions: SwiGLU with default scalars, GeGLU, GELU, ReLU,
@@ -200,8 +203,10 @@ MOE_API moe_status_t moe_plan(const int32_t* topk_ids, int32_t topk_ids_format, 
  *  - Size limit: ceil(M * top_k / 2048) * num_local_experts * 4 bytes must not exceed
  *    MOE_PLAN_NOALLOC_SCRATCH_BYTES (inputs of at most 2048 slots need no scratch at all);
  *    larger inputs are rejected with MOE_ERR_UNSUPPORTED_SHAPE before anything runs.
- *  - The first call on each device looks up the array's device address on that device
- *    (cudaGetSymbolAddress) and caches it; make that first call before any stream capture.
+ *  - The first call in each CUDA context looks up the array's device address in that
+ *    context (cudaGetSymbolAddress) and caches it under the context's unique id, so a
+ *    context torn down and re-created (cudaDeviceReset) is looked up afresh; make the first
+ *    call in a context before any stream capture.
  *  - Every call on a device shares the one array and leaves its contents behind; nothing in
  *    it must start at zero, but calls that overlap on the GPU (other streams, other host
  *    threads) race on it and must be serialised by the caller.
@@ -339,31 +344,6 @@ MOE_API moe_status_t moe_routed_forward(const uint16_t* x, int32_t M, int64_t ld
                                         int32_t* token_to_row, void* workspace, size_t workspace_bytes,
                                         int32_t* dev_status, void* const* step_events, int32_t num_step_events,
                                         moe_stream_t stream);
-
-/* ----------------------------------------------------------------------------------------
- * Test hook: runs the forward's permute and GEMM1 with a plain epilogue instead of the
- * fused requantiser. mode 0: FP32 pre-activations y = acc * xs[t] * alpha1[e] into
- * `dbg_out` [capacity, N1] (canonical [gate; up] column order); mode 1: the BF16
- * intermediate (after SwiGLU / squared-ReLU) into `dbg_out` [capacity, I]. Real rows only.
- * Same arguments and workspace as the forward.
- * ---------------------------------------------------------------------------------------- */
-MOE_API moe_status_t moe_debug_gemm1(const int32_t* padded_offsets, const int32_t* row_to_slot, int32_t M,
-                             int32_t top_k, const uint8_t* xq, const uint8_t* xsf, const float* xs,
-                             const moe_nvfp4_weights_t* w, const void* prepared,
-                             size_t prepared_bytes, int32_t mode, void* dbg_out, void* workspace,
-                             size_t workspace_bytes, int32_t* dev_status, moe_stream_t stream);
-
-/* ----------------------------------------------------------------------------------------
- * Test hook of the decode GEMM's scheduling (the one-call path, at most 16 tokens): each CTA
- * loads its first unit's weight stages before waiting for the prologue, guessing the expert
- * from the routing ids, and takes that unit through an ownership flag; the results never
- * depend on either. flags = 0 (the default) leaves the scheduling alone; bit 0 makes every
- * guess wrong (the next routed expert), so the stages are reloaded; bit 1 makes the odd CTAs
- * leave their first unit untaken, so other CTAs take it before any GEMM2 unit. Applies to
- * launches made after the call (a captured graph keeps the flags it was captured with).
- * Process-wide; not thread-safe. Returns the previous flags.
- * ---------------------------------------------------------------------------------------- */
-MOE_API int32_t moe_debug_set_decode_hooks(int32_t flags);
 
 #ifdef __cplusplus
 }

@@ -1,4 +1,5 @@
-"""ctypes binding of libmoe_nvfp4.so (the C ABI in include/moe_nvfp4.h).
+"""ctypes binding of libmoe_nvfp4.so (the C ABI in include/moe_nvfp4.h) and of the test
+build libmoe_nvfp4_test.so (include/moe_nvfp4_test.h, loaded only by test_lib()).
 
 Argument marshalling only: every function here turns torch tensors into device
 pointers, passes torch's current CUDA stream and raises on a non-OK status. All of
@@ -11,8 +12,10 @@ import os
 from ctypes import c_float, c_int32, c_int64, c_size_t, c_void_p
 
 from .build import LIB as LIB_PATH
+from .build import TEST_LIB as TEST_LIB_PATH
 
 _lib = None
+_test_lib = None
 
 MOE_OK = 0
 MOE_ACT_SWIGLU, MOE_ACT_RELU2, MOE_ACT_GEGLU, MOE_ACT_GELU, MOE_ACT_RELU, MOE_ACT_SILU, MOE_ACT_IDENTITY = range(7)
@@ -28,9 +31,11 @@ EXPORTED = [
     "moe_status_string", "moe_abi_version", "moe_quantize_input", "moe_plan_capacity",
     "moe_plan_workspace_bytes", "moe_plan", "moe_quantize_weights", "moe_prepared_weights_bytes",
     "moe_prepare_weights", "moe_forward_workspace_bytes", "moe_forward_workspace_layout",
-    "moe_grouped_fp4_forward", "moe_finalize", "moe_debug_gemm1", "moe_plan_noalloc",
-    "moe_routed_forward_workspace_bytes", "moe_routed_forward", "moe_debug_set_decode_hooks",
+    "moe_grouped_fp4_forward", "moe_finalize", "moe_plan_noalloc",
+    "moe_routed_forward_workspace_bytes", "moe_routed_forward",
 ]
+# the test build's extra entry points (include/moe_nvfp4_test.h)
+TEST_EXPORTED = ["moe_test_default_options", "moe_test_routed_forward", "moe_test_gemm1"]
 MOE_PLAN_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 
@@ -48,8 +53,20 @@ class WeightsT(ctypes.Structure):
     ]
 
 
-def _declare(lib):
+class TestOptionsT(ctypes.Structure):
+    """moe_test_options_t"""
+    _fields_ = [("decode_hooks", c_int32), ("withhold_release", c_int32), ("wait_limit_ns", ctypes.c_uint64)]
+
+
+# moe_routed_forward's arguments up to (not including) the stream
+_ROUTED_ARGS = [c_void_p, c_int32, c_int64, c_int32, c_void_p, c_int32, c_int32, c_int32, c_int32, c_void_p,
+                c_int32, c_float, ctypes.POINTER(WeightsT), c_void_p, c_size_t, c_float, c_int32, c_void_p, c_void_p,
+                c_void_p, c_void_p, c_size_t, c_void_p, ctypes.POINTER(c_void_p), c_int32]
+
+
+def _declare(lib, test=False):
     P = c_void_p
+    routed = list(_ROUTED_ARGS)
     sig = {
         "moe_status_string": (ctypes.c_char_p, [c_int32]),
         "moe_abi_version": (c_int32, []),
@@ -71,13 +88,15 @@ def _declare(lib):
                                               c_size_t, P, ctypes.POINTER(c_void_p), c_int32, P]),
         "moe_finalize": (c_int32, [P, P, c_int32, c_float, P, c_int32, c_int32, c_int32, P, P]),
         "moe_routed_forward_workspace_bytes": (c_size_t, [c_int32, c_int32, ctypes.POINTER(WeightsT), c_int32]),
-        "moe_routed_forward": (c_int32, [P, c_int32, c_int64, c_int32, P, c_int32, c_int32, c_int32, c_int32, P,
-                                         c_int32, c_float, ctypes.POINTER(WeightsT), P, c_size_t, c_float, c_int32,
-                                         P, P, P, P, c_size_t, P, ctypes.POINTER(c_void_p), c_int32, P]),
-        "moe_debug_gemm1": (c_int32, [P, P, c_int32, c_int32, P, P, P, ctypes.POINTER(WeightsT), P,
-                                      c_size_t, c_int32, P, P, c_size_t, P, P]),
-        "moe_debug_set_decode_hooks": (c_int32, [c_int32]),
+        "moe_routed_forward": (c_int32, routed + [P]),
     }
+    if test:
+        sig.update({
+            "moe_test_default_options": (TestOptionsT, []),
+            "moe_test_routed_forward": (c_int32, routed + [ctypes.POINTER(TestOptionsT), P]),
+            "moe_test_gemm1": (c_int32, [P, P, c_int32, c_int32, P, P, P, ctypes.POINTER(WeightsT), P,
+                                         c_size_t, c_int32, P, P, c_size_t, P, P]),
+        })
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
         f.restype = res
@@ -94,6 +113,28 @@ def lib():
         _lib = ctypes.CDLL(LIB_PATH)
         _declare(_lib)
     return _lib
+
+
+def test_lib():
+    """The test build (libmoe_nvfp4_test.so): every product entry point plus those of
+    include/moe_nvfp4_test.h. Only tests load it."""
+    global _test_lib
+    if _test_lib is None:
+        if not os.path.exists(TEST_LIB_PATH):
+            raise MoEError(f"{TEST_LIB_PATH} is missing: build it first (nvfp4_routed_moe_sort_gb300.build)")
+        _test_lib = ctypes.CDLL(TEST_LIB_PATH)
+        _declare(_test_lib, test=True)
+    return _test_lib
+
+
+def test_options(decode_hooks: int = 0, withhold_release: bool = False, wait_limit_ns: int | None = None):
+    """moe_test_options_t from the test build's defaults, with the given fields changed."""
+    o = test_lib().moe_test_default_options()
+    o.decode_hooks = int(decode_hooks)
+    o.withhold_release = int(bool(withhold_release))
+    if wait_limit_ns is not None:
+        o.wait_limit_ns = int(wait_limit_ns)
+    return o
 
 
 def status_string(code: int) -> str:
@@ -221,18 +262,22 @@ def moe_routed_forward_workspace_bytes(M, top_k, w: WeightsT, do_finalize) -> in
 
 def moe_routed_forward(x, act_scale_mode, topk_ids, num_experts, local_expert_offset, topk_weights, w: WeightsT,
                        prepared, fc2_input_scale, do_finalize, out, gemm2_out, token_to_row, workspace, dev_status,
-                       step_events=None, stream=None, routed_scaling_factor=1.0, packed=False):
+                       step_events=None, stream=None, routed_scaling_factor=1.0, packed=False, test_options=None):
     """The whole layer from BF16 hidden states x [M, H] (one C call). packed=True: topk_ids holds
-    packed slots (and topk_weights may be the same tensor)."""
+    packed slots (and topk_weights may be the same tensor). test_options (a TestOptionsT from
+    test_options()): call the test build's moe_test_routed_forward instead."""
     M, k = topk_ids.shape
     ev, nev = _events(step_events)
-    _check(lib().moe_routed_forward(
-        _ptr(x), M, x.stride(0), act_scale_mode, _ptr(topk_ids), MOE_IDS_PACKED if packed else MOE_IDS_INT32, k,
-        num_experts, local_expert_offset, _ptr(topk_weights), _weights_dtype(topk_weights),
-        float(routed_scaling_factor), ctypes.byref(w), _ptr(prepared), prepared.numel() * prepared.element_size(),
-        float(fc2_input_scale), int(do_finalize), _ptr(out), _ptr(gemm2_out), _ptr(token_to_row), _ptr(workspace),
-        workspace.numel() * workspace.element_size(), _ptr(dev_status), ev, nev, _stream(stream)),
-        "moe_routed_forward")
+    args = (_ptr(x), M, x.stride(0), act_scale_mode, _ptr(topk_ids), MOE_IDS_PACKED if packed else MOE_IDS_INT32, k,
+            num_experts, local_expert_offset, _ptr(topk_weights), _weights_dtype(topk_weights),
+            float(routed_scaling_factor), ctypes.byref(w), _ptr(prepared), prepared.numel() * prepared.element_size(),
+            float(fc2_input_scale), int(do_finalize), _ptr(out), _ptr(gemm2_out), _ptr(token_to_row),
+            _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(dev_status), ev, nev)
+    if test_options is None:
+        _check(lib().moe_routed_forward(*args, _stream(stream)), "moe_routed_forward")
+    else:
+        _check(test_lib().moe_test_routed_forward(*args, ctypes.byref(test_options), _stream(stream)),
+               "moe_test_routed_forward")
 
 
 def moe_grouped_fp4_forward(padded_offsets, row_to_slot, token_to_row, xq, xsf, xs, w: WeightsT, prepared,
@@ -258,15 +303,11 @@ def moe_finalize(gemm2_out, topk_weights, token_to_row, out, stream=None, routed
                               _stream(stream)), "moe_finalize")
 
 
-def moe_debug_set_decode_hooks(flags: int) -> int:
-    """Test hook of the decode GEMM's scheduling (bit 0: wrong expert guesses, bit 1: odd CTAs
-    leave their first unit to others); returns the previous flags."""
-    return int(lib().moe_debug_set_decode_hooks(int(flags)))
-
-
-def moe_debug_gemm1(padded_offsets, row_to_slot, M, top_k, xq, xsf, xs, w: WeightsT, prepared, mode,
-                    dbg_out, workspace, dev_status, stream=None):
-    _check(lib().moe_debug_gemm1(
+def moe_test_gemm1(padded_offsets, row_to_slot, M, top_k, xq, xsf, xs, w: WeightsT, prepared, mode,
+                   dbg_out, workspace, dev_status, stream=None):
+    """Test build: the forward's GEMM1 with a plain epilogue (mode 0 FP32 pre-activations,
+    1 the BF16 intermediate) into dbg_out."""
+    _check(test_lib().moe_test_gemm1(
         _ptr(padded_offsets), _ptr(row_to_slot), M, top_k, _ptr(xq), _ptr(xsf), _ptr(xs), ctypes.byref(w),
         _ptr(prepared), prepared.numel() * prepared.element_size(), mode, _ptr(dbg_out), _ptr(workspace),
-        workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream)), "moe_debug_gemm1")
+        workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream)), "moe_test_gemm1")

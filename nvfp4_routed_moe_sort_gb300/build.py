@@ -1,8 +1,10 @@
-"""Builds libmoe_nvfp4.so in-tree with nvcc for sm_103a.
+"""Builds libmoe_nvfp4.so (the product library) and libmoe_nvfp4_test.so (the test build)
+in-tree with nvcc for sm_103a.
 
-Each .cu file compiles to an object in parallel; the objects link into one shared
-library (CUDA runtime linked statically) next to this file. The build is skipped when
-the library is newer than every source.
+Each .cu file compiles to an object in parallel. The product library links the objects of
+csrc/*.cu (CUDA runtime linked statically); the test library links the same objects plus
+those of csrc/testbuild/*.cu, the entry points of include/moe_nvfp4_test.h, which only
+tests load. The build is skipped when both libraries are newer than every source.
 """
 from __future__ import annotations
 
@@ -15,7 +17,9 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
+TESTBUILD = os.path.join(CSRC, "testbuild")
 LIB = os.path.join(PKG, "libmoe_nvfp4.so")
+TEST_LIB = os.path.join(PKG, "libmoe_nvfp4_test.so")
 INCLUDE = os.path.join(ROOT, "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -31,19 +35,26 @@ def _nvcc() -> str:
 
 
 def sources() -> list[str]:
+    """The product library's translation units."""
     return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
+def test_sources() -> list[str]:
+    """The test build's extra translation units."""
+    return sorted(os.path.join(TESTBUILD, f) for f in os.listdir(TESTBUILD) if f.endswith(".cu"))
+
+
 def _deps() -> list[str]:
-    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
-    files.append(os.path.join(INCLUDE, "moe_nvfp4.h"))
+    files = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if os.path.isfile(os.path.join(CSRC, f))]
+    files += [os.path.join(TESTBUILD, f) for f in os.listdir(TESTBUILD)]
+    files += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE)]
     return files
 
 
 def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+    if not (os.path.exists(LIB) and os.path.exists(TEST_LIB)):
         return False
-    t = os.path.getmtime(LIB)
+    t = min(os.path.getmtime(LIB), os.path.getmtime(TEST_LIB))
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
@@ -54,7 +65,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(BUILD, exist_ok=True)
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        prefix = "test_" if os.path.dirname(src) == TESTBUILD else ""
+        obj = os.path.join(BUILD, prefix + os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc, *ARCH, *FLAGS, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -63,14 +75,21 @@ def build(force: bool = False, verbose: bool = False) -> str:
             print(r.stdout, r.stderr)
         return obj
 
+    product, extra = sources(), test_sources()
     with concurrent.futures.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 4)) as ex:
-        objs = list(ex.map(compile_one, sources()))
-    tmp = LIB + ".tmp"
-    cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+        objs = list(ex.map(compile_one, product + extra))
+    prod_objs, test_objs = objs[:len(product)], objs[len(product):]
+
+    def link(out: str, objects: list[str]):
+        tmp = out + ".tmp"
+        cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objects]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link of {out} failed:\n{r.stdout}\n{r.stderr}")
+        os.replace(tmp, out)
+
+    link(LIB, prod_objs)
+    link(TEST_LIB, prod_objs + test_objs)
     return LIB
 
 

@@ -29,14 +29,7 @@ moe_status_t moe::check_weights(const moe_nvfp4_weights_t* w) {
   return MOE_OK;
 }
 
-namespace {
-
-struct Bufs {
-  int32_t* sched;
-  int32_t* mtd;  // followed by the expert counters (edone)
-  uint8_t *aq, *asf, *iq, *isf;
-  uint16_t* g;
-};
+namespace moe {
 
 Bufs carve(void* ws, const WorkspaceLayout& L) {
   uint8_t* b = static_cast<uint8_t*>(ws);
@@ -50,11 +43,6 @@ Bufs carve(void* ws, const WorkspaceLayout& L) {
   r.g = L.g ? reinterpret_cast<uint16_t*>(b + L.g) : nullptr;
   return r;
 }
-
-struct Prepared {
-  const uint8_t *w1, *w1sf, *w2, *w2sf;
-  const float *a1, *a2, *a1g;
-};
 
 Prepared prepared_ptrs(const void* prepared, const PreparedLayout& L) {
   const uint8_t* b = static_cast<const uint8_t*>(prepared);
@@ -115,7 +103,7 @@ GemmLaunch gemm1_launch(const Dims& d, const WorkspaceLayout& L, const Bufs& b, 
   return g;
 }
 
-}  // namespace
+}  // namespace moe
 
 extern "C" const char* moe_status_string(int32_t status) {
   switch (status) {
@@ -200,7 +188,7 @@ moe_status_t forward_chain(const int32_t* padded_offsets, const int32_t* row_to_
                            int32_t topk_weights_dtype, float routed_scaling_factor, float fc2_input_scale,
                            int32_t do_finalize, uint16_t* out, uint16_t* gemm2_out, void* workspace,
                            int32_t* dev_status, void* const* step_events, int32_t num_step_events, bool run_permute,
-                           const RoutingHint& hint, cudaStream_t s) {
+                           const RoutingHint& hint, const TestOptions& topt, cudaStream_t s) {
   const Dims d = make_dims(w);
   const bool fin = do_finalize == MOE_OUTPUT_FINALIZED;
   const bool accum = do_finalize == MOE_OUTPUT_ACCUMULATE;
@@ -264,9 +252,9 @@ moe_status_t forward_chain(const int32_t* padded_offsets, const int32_t* row_to_
   g2.tile_counter = b.sched + 1;
   if (M <= kDecodeMaxTokens)
     st = launch_gemm_decode(g1, g2, reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + L.edone),
-                            reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + L.own), hint, s);
+                            reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + L.own), hint, topt, s);
   else
-    st = launch_gemm_chain(g1, g2, b.mtd, s);
+    st = launch_gemm_chain(g1, g2, b.mtd, topt, s);
   if (st != MOE_OK) return st;
   if ((st = mark(2)) != MOE_OK) return st;
   if ((st = mark(3)) != MOE_OK) return st;
@@ -333,36 +321,6 @@ extern "C" moe_status_t moe_grouped_fp4_forward(const int32_t* padded_offsets, c
   }
   return forward_chain(padded_offsets, row_to_slot, token_to_row, M, top_k, xq, xsf, xs, w, prepared, topk_weights,
                        topk_weights_dtype, routed_scaling_factor, fc2_input_scale, do_finalize, out, gemm2_out,
-                       workspace, dev_status, step_events, num_step_events, true, RoutingHint(),
+                       workspace, dev_status, step_events, num_step_events, true, RoutingHint(), TestOptions(),
                        as_stream(stream));
-}
-
-extern "C" moe_status_t moe_debug_gemm1(const int32_t* padded_offsets, const int32_t* row_to_slot, int32_t M,
-                                        int32_t top_k, const uint8_t* xq, const uint8_t* xsf, const float* xs,
-                                        const moe_nvfp4_weights_t* w, const void* prepared, size_t prepared_bytes,
-                                        int32_t mode, void* dbg_out, void* workspace, size_t workspace_bytes,
-                                        int32_t* dev_status, moe_stream_t stream) {
-  moe_status_t st = check_weights(w);
-  if (st != MOE_OK) return st;
-  MOE_CHECK(M >= 0 && top_k >= 1 && (mode == 0 || mode == 1), MOE_ERR_INVALID_ARGUMENT);
-  const Dims d = make_dims(w);
-  const WorkspaceLayout L = workspace_layout(d, M, top_k, MOE_OUTPUT_UNFINALIZED);
-  st = check_forward_common(padded_offsets, row_to_slot, M, top_k, xq, xsf, xs, w, prepared, prepared_bytes,
-                            workspace, workspace_bytes, dev_status, L.total);
-  if (st != MOE_OK) return st;
-  if (M == 0) return MOE_OK;
-  MOE_CHECK(dbg_out != nullptr, MOE_ERR_INVALID_ARGUMENT);
-  MOE_CHECK(aligned16(dbg_out), MOE_ERR_MISALIGNED);
-  cudaStream_t s = as_stream(stream);
-  const Bufs b = carve(workspace, L);
-  const Prepared pw = prepared_ptrs(prepared, prepared_layout(d));
-  st = launch_permute(padded_offsets, static_cast<int>(d.El), row_to_slot, top_k, L.cap, xq, xsf,
-                      static_cast<int>(d.H), b.aq, b.asf, b.sched, b.mtd, counter_ints(L, L.mtd), nullptr, nullptr, 0,
-                      s);
-  if (st != MOE_OK) return st;
-  GemmLaunch g1 = gemm1_launch(d, L, b, pw, padded_offsets, row_to_slot, xs, top_k, dev_status);
-  g1.mode = mode == 0 ? kG1Preact : kG1Act;
-  g1.out = dbg_out;
-  g1.out_sf = nullptr;
-  return launch_gemm(g1, s);
 }

@@ -182,17 +182,18 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 
 // A wait that gives up: after `limit_ns` it raises the CTA's abort flag, ORs
 // MOE_DEV_TIMEOUT into the status word and returns false. It also returns false as soon as
-// another role of the CTA has aborted.
+// another role of the CTA has aborted. The kernels take the limit as a launch parameter:
+// kWaitLimitNs from every product entry point.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int32_t* dev_status) {
+                                          int32_t* dev_status, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       *abort_flag = 1;
       if (dev_status) atomicOr(dev_status, MOE_DEV_TIMEOUT);
       return false;

@@ -70,7 +70,7 @@ bool encode_rows(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t 
 
 }  // namespace
 
-namespace {
+namespace gemm {
 
 bool fill_phase(Phase& ph, const GemmLaunch& g) {
   if (!encode_rows(&ph.tmap_a, g.a, g.K / 2, g.cap, kTileM)) return false;
@@ -114,33 +114,28 @@ size_t smem_bytes(int64_t El, bool sparse) {
          (sparse ? kSparseStageBytes : 0);
 }
 
-moe_status_t dispatch(int mode, int act, const GemmParams& prm, int64_t units_max, size_t smem, cudaStream_t s) {
+}  // namespace gemm
+
+namespace {
+
+moe_status_t dispatch_chain(int mode, int act, const GemmParams& prm, int64_t units_max, size_t smem,
+                            cudaStream_t s) {
   switch (act) {
     case MOE_ACT_SWIGLU:
-    case MOE_ACT_GEGLU: return gemm::launch_gated(mode, act, prm, units_max, smem, s);
+    case MOE_ACT_GEGLU: return gemm::launch_chain_gated(mode, act, prm, units_max, smem, s);
     case MOE_ACT_RELU2:
     case MOE_ACT_GELU:
-    case MOE_ACT_RELU: return gemm::launch_plain_a(mode, act, prm, units_max, smem, s);
+    case MOE_ACT_RELU: return gemm::launch_chain_plain_a(mode, act, prm, units_max, smem, s);
     case MOE_ACT_SILU:
-    case MOE_ACT_IDENTITY: return gemm::launch_plain_b(mode, act, prm, units_max, smem, s);
+    case MOE_ACT_IDENTITY: return gemm::launch_chain_plain_b(mode, act, prm, units_max, smem, s);
     default: return MOE_ERR_INVALID_ARGUMENT;
   }
 }
 
 }  // namespace
 
-moe_status_t launch_gemm(const GemmLaunch& g, cudaStream_t s) {
-  if (g.cap == 0) return MOE_OK;
-  GemmParams prm;
-  memset(&prm, 0, sizeof(prm));
-  if (!fill_phase(prm.ph[0], g)) return MOE_ERR_CUDA;
-  fill_common(prm, g);
-  prm.sparse = 0;  // the plain GEMM1 epilogues of the test hook
-  const int64_t units_max = (g.cap / kTileM) * prm.ph[0].n_tiles;
-  return dispatch(g.mode, g.act, prm, units_max, smem_bytes(g.El, prm.sparse), s);
-}
-
-moe_status_t launch_gemm_chain(const GemmLaunch& g1, const GemmLaunch& g2, int32_t* mt_done, cudaStream_t s) {
+moe_status_t launch_gemm_chain(const GemmLaunch& g1, const GemmLaunch& g2, int32_t* mt_done, const TestOptions& topt,
+                               cudaStream_t s) {
   if (g1.cap == 0) return MOE_OK;
   GemmParams prm;
   memset(&prm, 0, sizeof(prm));
@@ -151,17 +146,15 @@ moe_status_t launch_gemm_chain(const GemmLaunch& g1, const GemmLaunch& g2, int32
   prm.rsf = g2.rsf;
   prm.mt_done = mt_done;
   prm.sparse = g1.El <= kSparseMaxExperts;
+  prm.wait_ns = topt.wait_limit_ns;
+  prm.withhold = topt.withhold_release;
   const int mode = g2.mode == kG2Reduce ? kChainReduce : kChainRows;
   const int64_t units_max = (g1.cap / kTileM) * (prm.ph[0].n_tiles + prm.ph[1].n_tiles);
-  return dispatch(mode, g1.act, prm, units_max, smem_bytes(g1.El, prm.sparse), s);
+  return dispatch_chain(mode, g1.act, prm, units_max, smem_bytes(g1.El, prm.sparse), s);
 }
 
-namespace {
-int32_t g_decode_hooks = 0;  // moe_debug_set_decode_hooks
-}  // namespace
-
 moe_status_t launch_gemm_decode(const GemmLaunch& g1, const GemmLaunch& g2, int32_t* e_done, int32_t* own,
-                                const RoutingHint& hint, cudaStream_t s) {
+                                const RoutingHint& hint, const TestOptions& topt, cudaStream_t s) {
   if (g1.cap == 0) return MOE_OK;
   dgemm::Params prm;
   memset(&prm, 0, sizeof(prm));
@@ -193,7 +186,9 @@ moe_status_t launch_gemm_decode(const GemmLaunch& g1, const GemmLaunch& g2, int3
   prm.e_done = e_done;
   prm.own = own;
   prm.owned = g2.tile_counter;  // the second tile counter: unused by this kernel otherwise
-  prm.dbg_hooks = g_decode_hooks;
+  prm.dbg_hooks = topt.decode_hooks & 3;
+  prm.wait_ns = topt.wait_limit_ns;
+  prm.withhold = topt.withhold_release;
   prm.hint_ids = hint.ids;
   prm.hint_mask = hint.id_mask;
   prm.hint_off = hint.off;
@@ -214,9 +209,3 @@ moe_status_t launch_gemm_decode(const GemmLaunch& g1, const GemmLaunch& g2, int3
 }
 
 }  // namespace moe
-
-extern "C" int32_t moe_debug_set_decode_hooks(int32_t flags) {
-  const int32_t prev = moe::g_decode_hooks;
-  moe::g_decode_hooks = flags & 3;
-  return prev;
-}

@@ -91,7 +91,7 @@ struct Params {
   int32_t* e_done;        // per local expert: GEMM1 epilogue warps done (zeroed before the launch)
   int32_t* own;           // ownership flags of units [0, n_static) (zeroed before the launch)
   int32_t* owned;         // count of the flags set (zeroed before the launch)
-  int32_t dbg_hooks;      // test hook: bit 0 wrong guesses, bit 1 odd CTAs skip their offered unit
+  int32_t dbg_hooks;      // test build only: bit 0 wrong guesses, bit 1 odd CTAs skip their offered unit
   int32_t n_static;       // statically offered first units (0: every unit from the counter)
   const int32_t* hint_ids;  // routing ids of the step [hint_slots] (read before the wait)
   int32_t hint_mask, hint_off, hint_slots;
@@ -100,6 +100,8 @@ struct Params {
   const void* route_w;
   int32_t route_w_dtype;
   float rsf;
+  uint64_t wait_ns;       // limit of every bounded wait (kWaitLimitNs unless a test build shortens it)
+  int32_t withhold;       // test build only: the first active expert's GEMM1 units never publish
 };
 
 __device__ __forceinline__ void red_add_f32(float* out, float v) {
@@ -120,7 +122,7 @@ __device__ __forceinline__ int ld_acquire_s32(const int32_t* p) {
 }
 
 __device__ __forceinline__ bool wait_counter(const int32_t* counter, int target, volatile int* abort_flag,
-                                             int32_t* dev_status) {
+                                             int32_t* dev_status, uint64_t limit_ns) {
   uint64_t t0 = 0;
   while (true) {
     int v;
@@ -130,7 +132,7 @@ __device__ __forceinline__ bool wait_counter(const int32_t* counter, int target,
     const uint64_t now = globaltimer_ns();
     if (t0 == 0) {
       t0 = now;
-    } else if (now - t0 > kWaitLimitNs) {
+    } else if (now - t0 > limit_ns) {
       *abort_flag = 1;
       if (dev_status) atomicOr(dev_status, MOE_DEV_TIMEOUT);
       return false;
@@ -314,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm_kernel(const __grid_c
   const int units0 = n_active * p.ph[0].n_tiles;
   const int total_units = units0 + n_active * p.ph[1].n_tiles;
   auto take_unit = [&](uint32_t& rslot, uint32_t& rphase, bool one_lane) -> int {
-    bool got = mbar_wait(&unit_full[rslot], rphase, abort_flag, p.dev_status);
+    bool got = mbar_wait(&unit_full[rslot], rphase, abort_flag, p.dev_status, p.wait_ns);
     if (!one_lane) got = __all_sync(0xffffffffu, got);
     if (!got) return -2;
     const int u = unit_ring[rslot];
@@ -338,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm_kernel(const __grid_c
       int sweep = 0;    // next offered unit to check before the first GEMM2 unit
       bool first = true;
       while (ok) {
-        if (!mbar_wait(&unit_empty[rslot], rphase ^ 1, abort_flag, p.dev_status)) { ok = false; break; }
+        if (!mbar_wait(&unit_empty[rslot], rphase ^ 1, abort_flag, p.dev_status, p.wait_ns)) { ok = false; break; }
         int u = -1;
         if (first) {
           first = false;
@@ -386,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm_kernel(const __grid_c
         if (pre_n > 0) {
           // the stages loaded before the wait land before their buffers are reused
           for (int kb = 0; kb < pre_n; ++kb)
-            if (!mbar_wait(&pre_bar[kb], 0, abort_flag, p.dev_status)) ok = false;
+            if (!mbar_wait(&pre_bar[kb], 0, abort_flag, p.dev_status, p.wait_ns)) ok = false;
           if (!ok) break;
         }
         if (u < 0) break;
@@ -411,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm_kernel(const __grid_c
           // confirms their expert, else reload them in full below
           if (u == u_static && !second && e == pre_e) {
             for (int kb = 0; kb < pre_n; ++kb) {
-              if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.dev_status)) { ok = false; break; }
+              if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.dev_status, p.wait_ns)) { ok = false; break; }
               uint8_t* st = smem + stage * kStageBytes;
               mbar_arrive_expect_tx(&full[stage], kXBytes + kSfxBytes);
               tma_load_2d(st + kOffX, &ph.tmap_x, kb * 128, seg, &full[stage]);
@@ -430,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm_kernel(const __grid_c
           if (ld_acquire_s32(p.e_done + e) < target) {  // only a unit that will wait prefetches
             prefetch_l2(ph.w_raw + static_cast<int64_t>(wrow0) * (ph.K / 2), static_cast<int64_t>(256) * (ph.K / 2));
             prefetch_l2(sfw0, 2 * kt * 512);
-            if (!wait_counter(p.e_done + e, target, abort_flag, p.dev_status)) {
+            if (!wait_counter(p.e_done + e, target, abort_flag, p.dev_status, p.wait_ns)) {
               ok = false;
               break;
             }
@@ -439,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm_kernel(const __grid_c
         } else if (second) {
           pre = ph.nkb;
           for (int kb = 0; kb < pre; ++kb) {
-            if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.dev_status)) { ok = false; break; }
+            if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.dev_status, p.wait_ns)) { ok = false; break; }
             uint8_t* st = smem + stage * kStageBytes;
             mbar_arrive_expect_tx(&full[stage], kStageBytes);
             tma_load_2d(st, &ph.tmap_w, kb * 128, wrow0, &full[stage]);
@@ -450,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm_kernel(const __grid_c
             if (++stage == kStages) { stage = 0; phase ^= 1; }
           }
           if (!ok) break;
-          if (!wait_counter(p.e_done + e, kEpiWarps * p.ph[0].n_tiles, abort_flag, p.dev_status)) {
+          if (!wait_counter(p.e_done + e, kEpiWarps * p.ph[0].n_tiles, abort_flag, p.dev_status, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -463,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm_kernel(const __grid_c
           }
         }
         for (int kb = pre; kb < ph.nkb; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.dev_status)) { ok = false; break; }
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.dev_status, p.wait_ns)) { ok = false; break; }
           uint8_t* st = smem + stage * kStageBytes;
           mbar_arrive_expect_tx(&full[stage], kStageBytes);
           tma_load_2d(st, &ph.tmap_w, kb * 128, wrow0, &full[stage]);
@@ -476,11 +478,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm_kernel(const __grid_c
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
       }
-      if (!ok) {
-        for (int s = 0; s < kStages; ++s)
-          if (issued_mask & (1u << s)) mbar_drain(&full[s], (issued_phase >> s) & 1);
-        for (int kb = 0; kb < pre_n; ++kb) mbar_drain(&pre_bar[kb], 0);
-      }
+      // every issued copy lands before the CTA exits (after an abort, or when another role
+      // gave up before consuming it)
+      for (int s = 0; s < kStages; ++s)
+        if (issued_mask & (1u << s)) mbar_drain(&full[s], (issued_phase >> s) & 1);
+      for (int kb = 0; kb < pre_n; ++kb) mbar_drain(&pre_bar[kb], 0);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -492,12 +494,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm_kernel(const __grid_c
       while (ok) {
         const int u = take_unit(rslot, rphase, true);
         if (u < 0) break;
-        if (!mbar_wait(&acc_empty[buf], acc_phase[buf] ^ 1, abort_flag, p.dev_status)) { ok = false; break; }
+        if (!mbar_wait(&acc_empty[buf], acc_phase[buf] ^ 1, abort_flag, p.dev_status, p.wait_ns)) { ok = false; break; }
         tc_fence_after();
         const int nkb = p.ph[u >= units0 ? 1 : 0].nkb;
         const uint32_t acc = tmem + buf * kAccCols;
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(&full[stage], phase, abort_flag, p.dev_status)) { ok = false; break; }
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.dev_status, p.wait_ns)) { ok = false; break; }
           tc_fence_after();
           const uint32_t st = smem_u32(smem + stage * kStageBytes);
           const uint32_t sft = tmem + kSfCol0 + stage * kSfColsPerStage;
@@ -565,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm_kernel(const __grid_c
       }
       const float a = ph.alpha[e];
       const float ag = (!second && kGated) ? ph.alpha_gate[e] : a;
-      bool ok = mbar_wait(&acc_full[buf], acc_phase[buf], abort_flag, p.dev_status);
+      bool ok = mbar_wait(&acc_full[buf], acc_phase[buf], abort_flag, p.dev_status, p.wait_ns);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
@@ -606,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm_kernel(const __grid_c
           for (int t = 0; t < n_e && t < kTokens; ++t) ph.out_sf[sf_tile_offset(seg + t, I / 16 + r, ip16)] = 0;
         // publish this warp's share of the GEMM1 tile to the GEMM2 units of the expert
         __syncwarp();
-        if (lane == 0) red_release_add(p.e_done + e, 1);
+        if (lane == 0 && !(p.withhold && e == s_act[0])) red_release_add(p.e_done + e, 1);
       } else {
         const float d2 = __fmul_rn(a, __fdiv_rn(1.0f, p.g2));
 #pragma unroll

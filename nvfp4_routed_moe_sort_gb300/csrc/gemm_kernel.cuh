@@ -70,6 +70,8 @@ struct GemmParams {
   int32_t route_w_dtype;
   float rsf;
   int32_t sparse;       // the sparse epilogue is enabled (shared memory holds its stage)
+  uint64_t wait_ns;     // limit of every bounded wait (kWaitLimitNs unless a test build shortens it)
+  int32_t withhold;     // test build only: GEMM1 tiles of row tile 0 never publish their completion
 };
 
 __host__ __device__ constexpr bool is_g2(int mode) { return mode == kG2Rows || mode == kG2Reduce; }
@@ -372,7 +374,7 @@ __device__ __noinline__ bool sparse_epilogue(const GemmParams& p, const Phase& p
                                                 uint64_t* stage_full, uint64_t* stage_empty, uint32_t& sphase,
                                                 volatile int* abort_flag) {
   if (q == 0) {
-    bool ok = mbar_wait(stage_empty, sphase ^ 1, abort_flag, p.dev_status);
+    bool ok = mbar_wait(stage_empty, sphase ^ 1, abort_flag, p.dev_status, p.wait_ns);
     if (!__all_sync(0xffffffffu, ok)) return false;
     // 32 columns at a time (few registers: this path runs inside the dense epilogue's loop)
     float4* dst = reinterpret_cast<float4*>(s_stage + (lane & (kSparseRows - 1)) * kTileN + half * 128);
@@ -402,7 +404,7 @@ __device__ __noinline__ bool sparse_epilogue(const GemmParams& p, const Phase& p
     tc_fence_before();
     mbar_arrive(acc_empty);
   }
-  bool ok = mbar_wait(stage_full, sphase, abort_flag, p.dev_status);
+  bool ok = mbar_wait(stage_full, sphase, abort_flag, p.dev_status, p.wait_ns);
   if (!__all_sync(0xffffffffu, ok)) return false;
   sphase ^= 1;
   int nrows = 0;  // real rows lead the tile
@@ -417,7 +419,7 @@ __device__ __noinline__ bool sparse_epilogue(const GemmParams& p, const Phase& p
 // Bounded wait until *counter >= target (acquire): the GEMM2 half of a chained launch waits
 // here for the GEMM1 tiles it reads. Gives up like mbar_wait.
 __device__ __forceinline__ bool wait_counter(const int32_t* counter, int target, volatile int* abort_flag,
-                                             int32_t* dev_status) {
+                                             int32_t* dev_status, uint64_t limit_ns) {
   uint64_t t0 = 0;
   while (true) {
     int v;
@@ -427,7 +429,7 @@ __device__ __forceinline__ bool wait_counter(const int32_t* counter, int target,
     const uint64_t now = globaltimer_ns();
     if (t0 == 0) {
       t0 = now;
-    } else if (now - t0 > kWaitLimitNs) {
+    } else if (now - t0 > limit_ns) {
       *abort_flag = 1;
       if (dev_status) atomicOr(dev_status, MOE_DEV_TIMEOUT);
       return false;
@@ -473,7 +475,7 @@ __device__ __forceinline__ bool epilogue_unit(const GemmParams& p, const Phase& 
   const bool sparse = (EK == kG1Fused || is_g2(EK)) && p.sparse && p.row_to_slot[row0 + kSparseRows] < 0;
   float scal = xs_t;
   if constexpr (EK == kG2Reduce) scal = slot >= 0 ? route_weight(p.route_w, p.route_w_dtype, slot, p.rsf) : 0.0f;
-  bool ok = mbar_wait(acc_full, acc_phase, abort_flag, p.dev_status);
+  bool ok = mbar_wait(acc_full, acc_phase, abort_flag, p.dev_status, p.wait_ns);
   ok = __all_sync(0xffffffffu, ok);
   if (!ok) return false;
   tc_fence_after();
@@ -566,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
   const int total_units = units0 + (kChain ? mtiles * p.ph[1].n_tiles : 0);
   // the producer claims work units and hands their ids to the MMA and epilogue warps
   auto take_unit = [&](uint32_t& rslot, uint32_t& rphase, bool one_lane) -> int {
-    bool got = mbar_wait(&unit_full[rslot], rphase, abort_flag, p.dev_status);
+    bool got = mbar_wait(&unit_full[rslot], rphase, abort_flag, p.dev_status, p.wait_ns);
     if (!one_lane) got = __all_sync(0xffffffffu, got);
     if (!got) return -2;
     const int u = unit_ring[rslot];
@@ -584,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       bool ok = true;
       while (ok) {
         // claim the next unit (in order, from the global counter) and publish its id
-        if (!mbar_wait(&unit_empty[rslot], rphase ^ 1, abort_flag, p.dev_status)) { ok = false; break; }
+        if (!mbar_wait(&unit_empty[rslot], rphase ^ 1, abort_flag, p.dev_status, p.wait_ns)) { ok = false; break; }
         // claims increase per CTA, so a GEMM2 tile never waits behind a GEMM1 tile that its
         // own CTA has claimed but not started
         int u = next_claim;
@@ -615,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             prefetch_l2(ph.b_raw + static_cast<int64_t>(brow0) * (ph.K / 2),
                         static_cast<int64_t>(kTileN) * (ph.K / 2));
             prefetch_l2(sfb0, 2 * kt * 512);
-            if (!wait_counter(done, target, abort_flag, p.dev_status)) {
+            if (!wait_counter(done, target, abort_flag, p.dev_status, p.wait_ns)) {
               ok = false;
               break;
             }
@@ -628,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         const bool short_tile = p.row_to_slot[row0 + 32] < 0;
         const uint32_t tx = short_tile ? kStageTx - (kABytes - 32 * 128) : kStageTx;
         for (int kb = 0; kb < ph.nkb; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.dev_status)) { ok = false; break; }
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.dev_status, p.wait_ns)) { ok = false; break; }
           uint8_t* st = smem + stage * kStageBytes;
           mbar_arrive_expect_tx(&full[stage], tx);
           tma_load_2d(st, short_tile ? &ph.tmap_a32 : &ph.tmap_a, kb * 128, row0, &full[stage]);
@@ -641,11 +643,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
       }
-      if (!ok) {
-        // copies may still be landing in shared memory: let them finish before exit
-        for (int s = 0; s < kStages; ++s)
-          if (issued_mask & (1u << s)) mbar_drain(&full[s], (issued_phase >> s) & 1);
-      }
+      // copies may still be landing in shared memory (after an abort, or when another role
+      // gave up before consuming them): let every issued stage land before the CTA exits
+      for (int s = 0; s < kStages; ++s)
+        if (issued_mask & (1u << s)) mbar_drain(&full[s], (issued_phase >> s) & 1);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -656,11 +657,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       while (ok) {
         const int u = take_unit(rslot, rphase, true);
         if (u < 0) break;
-        if (!mbar_wait(acc_empty, acc_phase ^ 1, abort_flag, p.dev_status)) { ok = false; break; }
+        if (!mbar_wait(acc_empty, acc_phase ^ 1, abort_flag, p.dev_status, p.wait_ns)) { ok = false; break; }
         tc_fence_after();
         const int nkb = p.ph[kChain && u >= units0 ? 1 : 0].nkb;
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(&full[stage], phase, abort_flag, p.dev_status)) { ok = false; break; }
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.dev_status, p.wait_ns)) { ok = false; break; }
           tc_fence_after();
           const uint32_t st = smem_u32(smem + stage * kStageBytes);
           const uint32_t sft = tmem + kSfCol0 + stage * kSfColsPerStage;
@@ -714,7 +715,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         if (kChain) {
           // this warp's share of a GEMM1 tile is written: publish it to the GEMM2 tiles
           __syncwarp();
-          if (lane == 0) red_release_add(p.mt_done + (row0 >> 7), 1);
+          if (lane == 0 && !(p.withhold && row0 < kTileM)) red_release_add(p.mt_done + (row0 >> 7), 1);
         }
       } else if constexpr (kChain) {
         if (!epilogue_unit<kEpi1, MOE_ACT_IDENTITY>(p, p.ph[1], u - units0, s_off, tmem_row, q, half, lane, r, etid,
@@ -741,12 +742,12 @@ moe_status_t launch_kernel(const GemmParams& prm, int64_t units_max, size_t smem
   return launch_pdl(kern, dim3(grid), dim3(kThreads), smem, s, prm);
 }
 
-// instantiated in the gemm_inst_*.cu files
-moe_status_t launch_gated(int mode, int act, const GemmParams& prm, int64_t units_max, size_t smem, cudaStream_t s);
-moe_status_t launch_plain_a(int mode, int act, const GemmParams& prm, int64_t units_max, size_t smem,
-                            cudaStream_t s);
-moe_status_t launch_plain_b(int mode, int act, const GemmParams& prm, int64_t units_max, size_t smem,
-                            cudaStream_t s);
+// launch set-up shared by the chained launcher (gemm.cu) and the test build's standalone GEMM1
+bool fill_phase(Phase& ph, const GemmLaunch& g);
+void fill_common(GemmParams& prm, const GemmLaunch& g);
+size_t smem_bytes(int64_t El, bool sparse);
+
+// instantiated in the gemm_inst_chain_*.cu files
 moe_status_t launch_chain_gated(int mode, int act, const GemmParams& prm, int64_t units_max, size_t smem,
                                 cudaStream_t s);
 moe_status_t launch_chain_plain_a(int mode, int act, const GemmParams& prm, int64_t units_max, size_t smem,

@@ -132,6 +132,18 @@ enum GemmMode : int {
 // the expert's rows its N = 16.
 constexpr int64_t kDecodeMaxTokens = MOE_DECODE_MAX_TOKENS;
 
+// Options that only the test build's entry points change; every product entry point passes
+// the defaults. decode_hooks: the decode GEMM's scheduling fallbacks forced (bit 0: every
+// first-unit guess wrong, bit 1: odd CTAs leave their offered unit to others);
+// wait_limit_ns: the limit of every bounded wait in the GEMM kernels; withhold_release: the
+// GEMM1 tiles of the first row tile (chained GEMMs) or of the first active expert (decode
+// GEMMs) never publish their completion, so a GEMM2 wait runs out.
+struct TestOptions {
+  int32_t decode_hooks = 0;
+  uint64_t wait_limit_ns = kWaitLimitNs;
+  int32_t withhold_release = 0;
+};
+
 struct GemmLaunch {
   int mode;
   const uint8_t* a;      // [cap, K/2] packed rows in plan order
@@ -158,15 +170,14 @@ struct GemmLaunch {
   float rsf = 1.0f;
 };
 
-// one GEMM on its own: the plain GEMM1 epilogues of the test hook (kG1Preact, kG1Act)
-moe_status_t launch_gemm(const GemmLaunch& g, cudaStream_t s);
 // GEMM1 (g1, kG1Fused) and GEMM2 (g2, kG2Rows or kG2Reduce) in one launch; mt_done holds
 // cap / 128 zeroed counters
-moe_status_t launch_gemm_chain(const GemmLaunch& g1, const GemmLaunch& g2, int32_t* mt_done, cudaStream_t s);
+moe_status_t launch_gemm_chain(const GemmLaunch& g1, const GemmLaunch& g2, int32_t* mt_done, const TestOptions& topt,
+                               cudaStream_t s);
 // the same with the decode-shaped kernel (at most 16 rows per expert); e_done holds E_local
 // zeroed counters
 moe_status_t launch_gemm_decode(const GemmLaunch& g1, const GemmLaunch& g2, int32_t* e_done, int32_t* own,
-                                const RoutingHint& hint, cudaStream_t s);
+                                const RoutingHint& hint, const TestOptions& topt, cudaStream_t s);
 moe_status_t launch_permute(const int32_t* padded_offsets, int El, const int32_t* row_to_slot, int top_k,
                             int64_t cap, const uint8_t* xq, const uint8_t* xsf, int H, uint8_t* aq, uint8_t* asf,
                             int32_t* tile_counters, int32_t* mt_done, int64_t n_mt, const uint16_t* acc_init,
@@ -184,7 +195,38 @@ moe_status_t forward_chain(const int32_t* padded_offsets, const int32_t* row_to_
                            int32_t topk_weights_dtype, float routed_scaling_factor, float fc2_input_scale,
                            int32_t do_finalize, uint16_t* out, uint16_t* gemm2_out, void* workspace,
                            int32_t* dev_status, void* const* step_events, int32_t num_step_events, bool run_permute,
-                           const RoutingHint& hint, cudaStream_t s);
+                           const RoutingHint& hint, const TestOptions& topt, cudaStream_t s);
+// The forward workspace carved into its buffers, and the prepared weights' parts (api.cu).
+struct Bufs {
+  int32_t* sched;
+  int32_t* mtd;  // followed by the expert counters (edone)
+  uint8_t *aq, *asf, *iq, *isf;
+  uint16_t* g;
+};
+Bufs carve(void* ws, const WorkspaceLayout& L);
+struct Prepared {
+  const uint8_t *w1, *w1sf, *w2, *w2sf;
+  const float *a1, *a2, *a1g;
+};
+Prepared prepared_ptrs(const void* prepared, const PreparedLayout& L);
+// GEMM1 of a forward: the permuted activations times W1 into the intermediate (kG1Fused)
+GemmLaunch gemm1_launch(const Dims& d, const WorkspaceLayout& L, const Bufs& b, const Prepared& pw,
+                        const int32_t* padded_offsets, const int32_t* row_to_slot, const float* xs, int top_k,
+                        int32_t* dev_status);
+// moe_routed_forward with the test build's options (routed.cu)
+moe_status_t routed_forward(const uint16_t* x, int32_t M, int64_t ld_x, int32_t act_scale_mode,
+                            const int32_t* topk_ids, int32_t topk_ids_format, int32_t top_k, int32_t num_experts,
+                            int32_t local_expert_offset, const void* topk_weights, int32_t topk_weights_dtype,
+                            float routed_scaling_factor, const moe_nvfp4_weights_t* w, const void* prepared,
+                            size_t prepared_bytes, float fc2_input_scale, int32_t do_finalize, uint16_t* out,
+                            uint16_t* gemm2_out, int32_t* token_to_row, void* workspace, size_t workspace_bytes,
+                            int32_t* dev_status, void* const* step_events, int32_t num_step_events,
+                            const TestOptions& topt, moe_stream_t stream);
+// the forward's argument checks shared with the test build's standalone GEMM1 (api.cu)
+moe_status_t check_forward_common(const int32_t* padded_offsets, const int32_t* row_to_slot, int32_t M,
+                                  int32_t top_k, const uint8_t* xq, const uint8_t* xsf, const float* xs,
+                                  const moe_nvfp4_weights_t* w, const void* prepared, size_t prepared_bytes,
+                                  void* workspace, size_t workspace_bytes, int32_t* dev_status, size_t ws_need);
 moe_status_t launch_prepare_matrix(const uint8_t* src, const uint8_t* src_sf, int E, int rows, int rows_p, int K,
                                    int gated_inter, uint8_t* dst, uint8_t* dst_sf, cudaStream_t s);
 

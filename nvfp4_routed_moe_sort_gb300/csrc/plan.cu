@@ -204,8 +204,10 @@ extern "C" moe_status_t moe_plan(const int32_t* topk_ids, int32_t topk_ids_forma
 // The array is file-scope device memory, so every GPU that loads the library holds it
 // (MOE_PLAN_NOALLOC_SCRATCH_BYTES) until the process exits. In host code its name is only
 // a host-side stand-in: the kernels are given the device address that
-// cudaGetSymbolAddress returns, looked up once per device on that device's first call and
-// cached. All calls on a device share the array and it keeps the last call's contents;
+// cudaGetSymbolAddress returns in the current context. That address is cached per CUDA
+// context, keyed by the context's unique id (cuCtxGetId, never reused within a process), so
+// a context torn down and re-created (cudaDeviceReset) gets a fresh lookup, never a stale
+// address. All calls in a context share the array and it keeps the last call's contents;
 // nothing in it has to start at zero (each call writes every histogram entry it later
 // reads), but calls that overlap on the GPU (two streams, or two threads) race on it.
 // ---------------------------------------------------------------------------------------
@@ -217,22 +219,56 @@ namespace {
 constexpr int64_t kNoAllocScratchInts = MOE_PLAN_NOALLOC_SCRATCH_BYTES / 4;
 static __device__ __align__(256) int32_t g_plan_noalloc_scratch[kNoAllocScratchInts];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_noalloc_mu;
-int32_t* g_noalloc_ptr[kMaxDevices] = {};
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
 
-// device address of the scratch array on the current device (looked up on first use)
+template <typename Fn>
+Fn driver_fn(const char* name) {
+  void* ptr = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &ptr, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return nullptr;
+  return reinterpret_cast<Fn>(ptr);
+}
+
+// unique id of the calling thread's current context, or 0 when it cannot be read
+unsigned long long current_context_id() {
+  static const CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+  static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+constexpr int kCacheSlots = 64;
+std::mutex g_noalloc_mu;
+unsigned long long g_noalloc_ctx[kCacheSlots] = {};  // context ids (0 = empty slot)
+int32_t* g_noalloc_ptr[kCacheSlots] = {};
+
+// device address of the scratch array in the current context (looked up on the first call
+// in each context; every call when the context id cannot be read or the cache is full)
 moe_status_t noalloc_scratch(int32_t** out) {
-  int dev = -1;
-  MOE_CUDA(cudaGetDevice(&dev));
-  if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  const unsigned long long id = current_context_id();
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (g_noalloc_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_plan_noalloc_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
-    g_noalloc_ptr[dev] = static_cast<int32_t*>(p);
+  int free_slot = -1;
+  for (int i = 0; id != 0 && i < kCacheSlots; ++i) {
+    if (g_noalloc_ctx[i] == id) {
+      *out = g_noalloc_ptr[i];
+      return MOE_OK;
+    }
+    if (g_noalloc_ctx[i] == 0 && free_slot < 0) free_slot = i;
   }
-  *out = g_noalloc_ptr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_plan_noalloc_scratch) != cudaSuccess || p == nullptr) return MOE_ERR_CUDA;
+  if (id != 0 && free_slot >= 0) {
+    g_noalloc_ctx[free_slot] = id;
+    g_noalloc_ptr[free_slot] = static_cast<int32_t*>(p);
+  }
+  *out = static_cast<int32_t*>(p);
   return MOE_OK;
 }
 

@@ -368,15 +368,14 @@ extern "C" size_t moe_routed_forward_workspace_bytes(int32_t M, int32_t top_k, c
   return routed_layout(make_dims(w), M, top_k, do_finalize).total;
 }
 
-extern "C" moe_status_t moe_routed_forward(const uint16_t* x, int32_t M, int64_t ld_x, int32_t act_scale_mode,
-                                           const int32_t* topk_ids, int32_t topk_ids_format, int32_t top_k,
-                                           int32_t num_experts, int32_t local_expert_offset, const void* topk_weights,
-                                           int32_t topk_weights_dtype, float routed_scaling_factor,
-                                           const moe_nvfp4_weights_t* w, const void* prepared, size_t prepared_bytes,
-                                           float fc2_input_scale, int32_t do_finalize, uint16_t* out,
-                                           uint16_t* gemm2_out, int32_t* token_to_row, void* workspace,
-                                           size_t workspace_bytes, int32_t* dev_status, void* const* step_events,
-                                           int32_t num_step_events, moe_stream_t stream) {
+moe_status_t moe::routed_forward(const uint16_t* x, int32_t M, int64_t ld_x, int32_t act_scale_mode,
+                                 const int32_t* topk_ids, int32_t topk_ids_format, int32_t top_k, int32_t num_experts,
+                                 int32_t local_expert_offset, const void* topk_weights, int32_t topk_weights_dtype,
+                                 float routed_scaling_factor, const moe_nvfp4_weights_t* w, const void* prepared,
+                                 size_t prepared_bytes, float fc2_input_scale, int32_t do_finalize, uint16_t* out,
+                                 uint16_t* gemm2_out, int32_t* token_to_row, void* workspace, size_t workspace_bytes,
+                                 int32_t* dev_status, void* const* step_events, int32_t num_step_events,
+                                 const TestOptions& topt, moe_stream_t stream) {
   moe_status_t st = check_weights(w);
   if (st != MOE_OK) return st;
   MOE_CHECK(M >= 0 && top_k >= 1, MOE_ERR_INVALID_ARGUMENT);
@@ -492,5 +491,20 @@ extern "C" moe_status_t moe_routed_forward(const uint16_t* x, int32_t M, int64_t
   hint.slots = M * top_k;
   return forward_chain(padded, r2s, token_to_row, M, top_k, xq, xsf, xs, w, prepared, topk_weights,
                        topk_weights_dtype, routed_scaling_factor, fc2_input_scale, do_finalize, out, gemm2_out, fwd,
-                       dev_status, num_step_events == 5 ? fwd_events : nullptr, num_step_events, false, hint, s);
+                       dev_status, num_step_events == 5 ? fwd_events : nullptr, num_step_events, false, hint, topt, s);
+}
+
+extern "C" moe_status_t moe_routed_forward(const uint16_t* x, int32_t M, int64_t ld_x, int32_t act_scale_mode,
+                                           const int32_t* topk_ids, int32_t topk_ids_format, int32_t top_k,
+                                           int32_t num_experts, int32_t local_expert_offset, const void* topk_weights,
+                                           int32_t topk_weights_dtype, float routed_scaling_factor,
+                                           const moe_nvfp4_weights_t* w, const void* prepared, size_t prepared_bytes,
+                                           float fc2_input_scale, int32_t do_finalize, uint16_t* out,
+                                           uint16_t* gemm2_out, int32_t* token_to_row, void* workspace,
+                                           size_t workspace_bytes, int32_t* dev_status, void* const* step_events,
+                                           int32_t num_step_events, moe_stream_t stream) {
+  return routed_forward(x, M, ld_x, act_scale_mode, topk_ids, topk_ids_format, top_k, num_experts,
+                        local_expert_offset, topk_weights, topk_weights_dtype, routed_scaling_factor, w, prepared,
+                        prepared_bytes, fc2_input_scale, do_finalize, out, gemm2_out, token_to_row, workspace,
+                        workspace_bytes, dev_status, step_events, num_step_events, TestOptions(), stream);
 }

@@ -129,13 +129,15 @@ class NVFP4RoutedMoE:
                                   routed_scaling_factor=self.routed_scaling_factor)
 
     def routed(self, x: torch.Tensor, topk_ids: torch.Tensor, topk_weights: torch.Tensor, b: dict, do_finalize,
-               packed: bool = False, step_events=None, out=None):
-        """One moe_routed_forward call into the buffers ``b`` of routed_buffers()."""
+               packed: bool = False, step_events=None, out=None, test_options=None):
+        """One moe_routed_forward call into the buffers ``b`` of routed_buffers() (with
+        ``test_options``, the test build's moe_test_routed_forward)."""
         L.moe_routed_forward(x.view(torch.int16), self.scale_mode, topk_ids, self.num_experts,
                              self.local_expert_offset, topk_weights, self.w, self.prepared, self.fc2_input_scale,
                              int(do_finalize), out if out is not None else b["out"], b["gemm2_out"],
                              b["token_to_row"], b["ws"], b["dev_status"], step_events=step_events,
-                             routed_scaling_factor=self.routed_scaling_factor, packed=packed)
+                             routed_scaling_factor=self.routed_scaling_factor, packed=packed,
+                             test_options=test_options)
 
     @staticmethod
     def _prefix(x, topk_ids, topk_weights, out, token_capacity):

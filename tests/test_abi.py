@@ -3,6 +3,7 @@ validates arguments on the host (no GPU is touched by these calls)."""
 import ctypes
 import os
 import re
+import subprocess
 
 import pytest
 import torch
@@ -21,20 +22,43 @@ def lib():
     return pkg.lib()
 
 
-def _declared():
-    with open(HEADER) as f:
+TEST_HEADER = os.path.join(ROOT, "include", "moe_nvfp4_test.h")
+
+
+def _declared(header=HEADER):
+    with open(header) as f:
         src = f.read()
     return sorted(set(re.findall(r"^MOE_API [^(]*?\b(moe_\w+)\(", src, flags=re.M)))
 
 
 def test_header_declares_binding_names():
     assert _declared() == sorted(L.EXPORTED)
+    assert _declared(TEST_HEADER) == sorted(L.TEST_EXPORTED)
 
 
 def test_exports_every_declared_symbol(lib):
     for name in _declared():
         assert hasattr(lib, name), name
-    assert pkg.moe_abi_version() == 2
+    assert pkg.moe_abi_version() == 3
+
+
+def test_test_build_exports_product_and_test_symbols(lib):
+    tl = pkg.test_lib()
+    for name in _declared() + _declared(TEST_HEADER):
+        assert hasattr(tl, name), name
+    o = pkg.test_options()
+    assert (o.decode_hooks, o.withhold_release, o.wait_limit_ns) == (0, 0, 2_000_000_000)
+
+
+def test_product_library_exports_no_test_hooks(lib):
+    """The test hooks (standalone GEMM1, decode scheduling fallbacks, shortened waits) live in
+    the test build only: the product library exports no moe_test_* or moe_debug_* symbol."""
+    for name in _declared(TEST_HEADER) + ["moe_debug_gemm1", "moe_debug_set_decode_hooks"]:
+        assert not hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", pkg.LIB_PATH], capture_output=True, text=True)
+    if out.returncode == 0:
+        exported = {ln.split()[-1] for ln in out.stdout.splitlines() if " T " in ln}
+        assert sorted(n for n in exported if n.startswith("moe_")) == sorted(L.EXPORTED)
 
 
 def test_status_strings(lib):

@@ -21,14 +21,36 @@ def test_kernel_work_hand_example():
     ids = np.array([[1, 0], [2, 1], [3, 0]], dtype=np.int32)
     w, step, R, active = bench.kernel_work(cfg, ids)
     assert R == 3 and active == 2
-    H, I, N1 = 256, 128, 256  # SwiGLU: N1 = 2 I
-    assert w["gemm1"]["bytes"] == active * N1 * H * NV + R * H * NV + R * I * NV + 2 * 4
-    assert w["gemm2"]["bytes"] == active * H * I * NV + R * I * NV + R * H * 2 + 2 * 4
+    H, I, N1, M, k = 256, 128, 256, 3, 2  # SwiGLU: N1 = 2 I
+    # the scope table's count: active experts' weights and alphas (no intermediates)
+    assert w["gemm1"]["bytes"] == active * N1 * H * NV + 2 * 4
+    assert w["gemm2"]["bytes"] == active * H * I * NV + 2 * 4
+    # this implementation's own round trips on top: permuted rows, intermediate, expert rows
+    assert w["gemm1"]["bytes_incl_intermediates"] == active * N1 * H * NV + R * H * NV + R * I * NV + 2 * 4
+    assert w["gemm2"]["bytes_incl_intermediates"] == active * H * I * NV + R * I * NV + R * H * 2 + 2 * 4
     assert w["gemm1"]["flops"] == 2.0 * R * H * N1
     assert w["gemm2"]["flops"] == 2.0 * R * I * H
-    # the whole step moves at least the active experts' weights and computes both GEMMs
-    assert step["bytes"] >= active * (N1 * H + H * I) * NV
-    assert step["flops"] >= w["gemm1"]["flops"] + w["gemm2"]["flops"]
+    # the kernels' algorithmic bytes add up to the whole step's: weights, alphas, BF16 in and
+    # out, routing ids and weights
+    assert sum(v["bytes"] for v in w.values()) == step["bytes"]
+    assert step["bytes"] == active * (N1 * H + H * I) * NV + 8 * 2 + 2 * M * H * 2 + M * k * 8
+    assert step["flops"] == w["gemm1"]["flops"] + w["gemm2"]["flops"]
+
+
+def test_roofline_bound_and_fraction():
+    peaks = {"hbm_gbs": 8000.0, "bf16_tflops": 2000.0, "source": "test"}
+    # 8 GB in 2 ms at 8 TB/s peak: HBM-bound, achieved 4 TB/s = half the peak
+    r = bench.roofline(8e9, 1e12, 2e-3, peaks)
+    assert r["bound"] == "hbm" and abs(r["frac"] - 0.5) < 1e-12 and r["unit"] == "GB/s"
+    # 1 GB and 12 PFLOP in 2 ms: tensor-bound at 2000 x 6 = 12 PF/s, so frac = (1 ms) / (2 ms)
+    r = bench.roofline(1e9, 12e12, 2e-3, peaks)
+    assert r["bound"] == "tensor" and abs(r["frac"] - 0.5) < 1e-12 and r["unit"] == "TFLOP/s"
+
+
+def test_warmup_below_three_is_rejected():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", "tiny",
+                          "--steps", "1", "--warmup", "2"], capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert out.returncode != 0 and "--warmup" in out.stderr
 
 
 def test_traffic_lookup_follows_the_kernel_hash(monkeypatch):

@@ -17,7 +17,7 @@ PROGRAM = r"""
 #include <stdio.h>
 
 int main(void) {
-  if (moe_abi_version() != 2) return 1;
+  if (moe_abi_version() != MOE_NVFP4_ABI_VERSION) return 1;
   const char* ok = moe_status_string(MOE_OK);
   if (ok == NULL || ok[0] == '\0') return 2;
   /* 300 tokens, top-2, 8 local experts: 600 slots + 127 padding rows per expert, to 128 */
@@ -44,3 +44,31 @@ def test_header_compiles_as_c_and_links(tmp_path):
     run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
     assert run.returncode == 0, (run.returncode, run.stdout, run.stderr)
     assert run.stdout.strip()  # the status string of the rejected call
+
+
+TEST_PROGRAM = r"""
+#include "moe_nvfp4_test.h"
+#include <stdio.h>
+
+int main(void) {
+  moe_test_options_t o = moe_test_default_options();
+  if (o.decode_hooks != 0 || o.withhold_release != 0 || o.wait_limit_ns != 2000000000ull) return 1;
+  if (moe_abi_version() != MOE_NVFP4_ABI_VERSION) return 2;
+  printf("ok\n");
+  return 0;
+}
+"""
+
+
+@pytest.mark.skipif(shutil.which("gcc") is None, reason="no C compiler")
+def test_test_header_compiles_as_c_and_links_against_the_test_build(tmp_path):
+    build()
+    src = tmp_path / "use_test_header.c"
+    src.write_text(TEST_PROGRAM)
+    exe = tmp_path / "use_test_header"
+    cc = subprocess.run(["gcc", "-std=c11", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.join(ROOT, "include"),
+                         str(src), "-L", PKG, "-lmoe_nvfp4_test", f"-Wl,-rpath,{PKG}", "-o", str(exe)],
+                        capture_output=True, text=True)
+    assert cc.returncode == 0, cc.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert run.returncode == 0, (run.returncode, run.stdout, run.stderr)

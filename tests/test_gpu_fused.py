@@ -88,7 +88,7 @@ def test_separate_gate_scalars(act):
     b = p.bufs(True)
     cap = b["capacity"]
     dbg = torch.full((cap, cfg.N1), float("nan"), dtype=torch.float32, device=DEV)
-    pkg.moe_debug_gemm1(b["padded_offsets"], b["row_to_slot"], cfg.M, cfg.top_k, b["xq"], b["xsf"], b["xs"],
+    pkg.moe_test_gemm1(b["padded_offsets"], b["row_to_slot"], cfg.M, cfg.top_k, b["xq"], b["xsf"], b["xs"],
                         p.layer.w, p.layer.prepared, 0, dbg, b["ws"], b["dev_status"])
     torch.cuda.synchronize()
     real = ref["plan"]["row_to_slot"] >= 0

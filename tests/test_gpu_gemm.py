@@ -43,7 +43,7 @@ def _gpu_debug(p: Problem, mode: int):
     ncols = cfg.N1 if mode == 0 else cfg.I
     dbg = torch.full((cap, ncols), float("nan"), dtype=torch.float32 if mode == 0 else torch.bfloat16,
                      device=DEV)
-    pkg.moe_debug_gemm1(b["padded_offsets"], b["row_to_slot"], cfg.M, cfg.top_k, b["xq"], b["xsf"], b["xs"],
+    pkg.moe_test_gemm1(b["padded_offsets"], b["row_to_slot"], cfg.M, cfg.top_k, b["xq"], b["xsf"], b["xs"],
                         p.layer.w, p.layer.prepared, mode, dbg, b["ws"], b["dev_status"])
     torch.cuda.synchronize()
     return dbg

@@ -1,0 +1,105 @@
+"""Guard bands around every buffer the library writes (a stand-in for a memory checker).
+
+Each output and scratch buffer of the one-call path (moe_routed_forward: workspace,
+token_to_row, out or gemm2_out, dev_status) and of the separate calls (activation pack, plan
+arrays, plan scratch, forward workspace, outputs) is carved out of a larger allocation with
+4 KB of patterned bytes before and after it. The layer runs through those buffers on shapes
+that reach every kernel (fused prologue, the plan's multi-block kernels, the quantiser that
+stores into the plan rows, decode and chained GEMMs, K and column tails, expert-parallel
+masking, unrouted slots); afterwards every band must be intact and the results must equal
+those of normally allocated buffers.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gpu_harness import DEV, Problem, bf16_np, mi, pkg
+
+pytestmark = pytest.mark.gpu
+
+BAND = 4096
+
+CASES = {
+    "tiny": mi.CONFIGS["tiny"],
+    "decode_t8": mi.CONFIGS["decode_t8"],
+    "decode_ep": mi.MoEConfig("decode_ep", M=12, H=1024, I=256, E=32, top_k=6, seed=31, weight_seed=31,
+                              local_offset=8, num_local=16),
+    "swiglu_ragged": mi.MoEConfig("swiglu_ragged", M=300, H=512, I=256, E=8, top_k=2, seed=11, weight_seed=11),
+    "ktail_large": mi.MoEConfig("ktail_large", M=400, H=384, I=384, E=12, top_k=6, seed=34, weight_seed=34,
+                                local_offset=2, num_local=8),
+}
+
+
+class Guarded:
+    """Buffers carved from allocations with patterned bands before and after each."""
+
+    def __init__(self):
+        self.allocs = []
+
+    def __call__(self, shape, dtype, fill=None):
+        n = int(np.prod(shape)) * torch.empty(0, dtype=dtype).element_size()
+        raw = torch.empty(n + 2 * BAND, dtype=torch.uint8, device=DEV)
+        pattern = (torch.arange(BAND, device=DEV, dtype=torch.int32) * 7 + 0xA5).to(torch.uint8)
+        raw[:BAND] = pattern
+        raw[BAND + n:] = pattern
+        view = raw[BAND:BAND + n].view(dtype).view(*shape)
+        if fill is not None:
+            view.fill_(fill)
+        self.allocs.append((raw, n, pattern))
+        return view
+
+    def intact(self) -> bool:
+        torch.cuda.synchronize()
+        return all(torch.equal(raw[:BAND], pat) and torch.equal(raw[BAND + n:], pat) for raw, n, pat in self.allocs)
+
+
+def _routing(cfg):
+    ids, tw = mi.routing(cfg)
+    if cfg.num_local is not None or cfg.name == "ktail_large":
+        ids = mi.with_unrouted(ids, 0.15, 7, cfg.E)
+    return ids, tw
+
+
+@pytest.mark.parametrize("mode", [1, 0])
+@pytest.mark.parametrize("name", list(CASES))
+def test_guard_bands_intact(name, mode):
+    cfg = CASES[name]
+    ids, tw = _routing(cfg)
+    p = Problem(cfg, ids, tw)
+    lay, M, k, El, H = p.layer, cfg.M, cfg.top_k, cfg.El, cfg.H
+    # reference results from the layer's own (normally allocated) buffers
+    ref = p.run_routed(mode)
+    ref = bf16_np(ref if mode else ref[0]).copy()
+    ref_t2r = lay.routed_buffers(M, k, mode)["token_to_row"].cpu().numpy().copy()
+    g = Guarded()
+    cap = pkg.moe_plan_capacity(M, k, El)
+    routed = {
+        "ws": g((max(pkg.moe_routed_forward_workspace_bytes(M, k, lay.w, mode), 16),), torch.uint8),
+        "token_to_row": g((M, k), torch.int32),
+        "dev_status": g((4,), torch.int32, 0),
+        "out": g((M, H), torch.bfloat16) if mode == 1 else None,
+        "gemm2_out": g((max(cap, 1), H), torch.bfloat16) if mode == 0 else None,
+        "capacity": cap,
+    }
+    separate = {
+        "xq": g((M, H // 2), torch.uint8), "xsf": g((M, H // 16), torch.uint8), "xs": g((M,), torch.float32),
+        "counts": g((El,), torch.int32), "padded_offsets": g((El + 1,), torch.int32),
+        "row_to_slot": g((max(cap, 1),), torch.int32), "token_to_row": g((M, k), torch.int32),
+        "plan_ws": g((max(pkg.moe_plan_workspace_bytes(M, k, El), 16),), torch.uint8),
+        "ws": g((max(pkg.moe_forward_workspace_bytes(M, k, lay.w, mode), 16),), torch.uint8),
+        "dev_status": g((4,), torch.int32, 0),
+        "out": g((M, H), torch.bfloat16) if mode == 1 else None,
+        "gemm2_out": g((max(cap, 1), H), torch.bfloat16) if mode == 0 else None,
+        "capacity": cap,
+    }
+    lay._bufs[("routed", M, k, mode)] = routed
+    lay._bufs[(M, k, mode)] = separate
+    for which, run, bufs in (("one-call", p.run_routed, routed), ("separate", p.run, separate)):
+        res = run(mode)
+        got = bf16_np(res if mode else res[0])
+        t2r = bufs["token_to_row"].cpu().numpy()
+        assert np.array_equal(t2r, ref_t2r), which
+        rows = slice(None) if mode else ref_t2r[ref_t2r >= 0]
+        assert np.array_equal(got[rows], ref[rows]), which
+        assert g.intact(), f"{name}: a guard band was overwritten ({which} path)"
+    assert int(routed["dev_status"][0].item()) == 0 and int(separate["dev_status"][0].item()) == 0

@@ -75,22 +75,25 @@ def test_decode_scheduling_fallbacks(name, hooks):
     """The decode GEMM loads each CTA's first unit's weights before the plan exists, guessing
     the expert from the routing ids, and offers that unit to the CTA through an ownership
     flag. Wrong guesses (bit 0: the stages are reloaded) and first units left to other CTAs
-    (bit 1: taken by the sweep before any GEMM2 unit) give the same bytes as the normal
-    schedule, finalized and unfinalized."""
+    (bit 1: taken by the sweep before any GEMM2 unit), forced through the test build's
+    options, give the same bytes as the normal schedule, finalized and unfinalized."""
     cfg = CASES[name]
     ids, tw = _unrouted(cfg) if name == "decode_ep" else (None, None)
     p = Problem(cfg, ids, tw)
     ref = bf16_np(p.run_routed(True)).copy()
     g2r, _, t2r = p.run_routed(False)
     g2r, t2r = bf16_np(g2r).copy(), to_np(t2r).copy()
-    prev = pkg._lib.moe_debug_set_decode_hooks(hooks)
-    try:
-        got = bf16_np(p.run_routed(True)).copy()
-        g2, _, t2 = p.run_routed(False)
-        g2, t2 = bf16_np(g2).copy(), to_np(t2).copy()
-    finally:
-        pkg._lib.moe_debug_set_decode_hooks(prev)
-    assert prev == 0
+    opts = pkg.test_options(decode_hooks=hooks)
+
+    def hooked(mode):
+        b = p.layer.routed_buffers(cfg.M, cfg.top_k, mode)
+        p.layer.routed(p.x, p.ids_t, p.tw_t, b, mode, test_options=opts)
+        torch.cuda.synchronize()
+        return b
+
+    got = bf16_np(hooked(True)["out"]).copy()
+    b = hooked(False)
+    g2, t2 = bf16_np(b["gemm2_out"]).copy(), to_np(b["token_to_row"]).copy()
     assert np.array_equal(got, ref)
     assert np.array_equal(t2, t2r)
     real = t2r[t2r >= 0]
@@ -146,3 +149,35 @@ def test_routed_graph_replay_new_routing_small_batch():
     assert all(evs[i].elapsed_time(evs[i + 1]) >= 0 for i in range(4))
     p2 = Problem(cfg2)
     assert np.array_equal(got, bf16_np(p2.run(True)))
+
+
+@pytest.mark.parametrize("name", ["decode_t8", "swiglu_ragged"])
+def test_refresh_in_place_under_captured_graph(name):
+    """In-place weight refresh at stable addresses (Megatron-Core prepare_routed_nvfp4_weights
+    with out=...): a graph captured before the refresh computes with the new weights after it.
+    The layer's linear NVFP4 weights are overwritten with a second seeded set, refresh()
+    re-prepares them into the same buffer, and one replay of the old graph must equal the
+    oracle on the new weights (and the new weights' own layer, bit for bit)."""
+    cfg = CASES[name]
+    p = Problem(cfg)
+    x, ids, tw = p.x.clone(), p.ids_t.clone(), p.tw_t.clone()
+    g = p.layer.capture(x, ids, tw, True)
+    g.replay()
+    torch.cuda.synchronize()
+    out_buf = p.layer.routed_buffers(cfg.M, cfg.top_k, True)["out"]
+    before = bf16_np(out_buf).copy()
+    assert np.array_equal(before, bf16_np(p.run_routed(True)))
+    prepared_ptr = p.layer.prepared.data_ptr()
+    cfg2 = cfg.with_(weight_seed=cfg.weight_seed + 1000)
+    p2 = Problem(cfg2)                       # same tokens and routing, new weights
+    for dst, src in zip(p.q1 + p.q2, p2.q1 + p2.q2):
+        dst.copy_(src)
+    p.layer.refresh()
+    g.replay()
+    torch.cuda.synchronize()
+    got = bf16_np(out_buf).copy()
+    assert p.layer.prepared.data_ptr() == prepared_ptr
+    assert not np.array_equal(got, before)
+    assert np.array_equal(got, bf16_np(p2.run_routed(True)))
+    assert_close_output(got, p2.oracle_forward()["out"], f"{name} after refresh")
+    assert p.layer.device_status(cfg.M, cfg.top_k, True) == 0
