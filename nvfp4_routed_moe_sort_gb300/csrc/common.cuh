@@ -21,7 +21,7 @@ namespace moe {
 constexpr int kSegAlign = 128;     // expert segments padded to 128 rows
 constexpr int kBlock = 16;         // NVFP4 block size
 constexpr int kTileM = 128;        // GEMM rows per tile (one MMA M)
-constexpr int kTileN = 256;        // GEMM columns per tile (two N=128 MMAs)
+constexpr int kTileN = 256;        // GEMM columns per tile (one N=256 MMA per K step)
 constexpr int kTileK = 256;        // K elements per pipeline stage (128 bytes per row)
 constexpr int kMaxLocalExperts = 512;
 

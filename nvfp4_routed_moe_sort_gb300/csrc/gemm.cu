@@ -13,7 +13,7 @@
 //                rows x 128 B, 128-byte swizzle) and three 2 KB bulk copies of 128x4 scale
 //                tiles, all completing on the stage's full barrier;
 //   warp 1       TMEM owner and MMA issuer: per stage, 12 tcgen05.cp of scale tiles into
-//                TMEM and 8 tcgen05.mma.kind::mxf4nvf4 (M=128, N=128, K=64, E2M1 x E2M1
+//                TMEM and 4 tcgen05.mma.kind::mxf4nvf4 (M=128, N=256, K=64, E2M1 x E2M1
 //                with UE4M3 scales per 16 values, FP32 accumulation in TMEM);
 //   warps 2..9   epilogue: two warps per TMEM lane quarter, one per column half; each pulls
 //                its 128 accumulator columns into registers (tcgen05.ld) and releases the
@@ -26,8 +26,9 @@
 // same weight tile at the same time and share it in L2. The producer hands each claimed id
 // to the MMA and epilogue warps through a 4-entry shared-memory ring. The unit count comes
 // from padded_offsets on the device.
-// TMEM: columns [0, 256) accumulator (two N=128 halves), [256, 448) scale tiles of the four
-// stages (16 columns of A scales + 32 of B scales each). Every wait is bounded.
+// TMEM: columns [0, 256) accumulator, [256, 448) scale tiles of the four stages (16 columns
+// of A scales + 32 of B scales each, the B scales of one K step in 8 adjacent columns: the
+// 128-row halves side by side, as the N=256 MMA reads them). Every wait is bounded.
 #include "gemm_kernel.cuh"
 #include "gemm_decode.cuh"
 

@@ -650,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_mxf4nvf4(kTileM, 128);
+      constexpr uint32_t idesc = idesc_mxf4nvf4(kTileM, kTileN);
       uint32_t stage = 0, phase = 0, acc_phase = 0;
       uint32_t rslot = 0, rphase = 0;
       bool ok = true;
@@ -665,23 +665,22 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
           tc_fence_after();
           const uint32_t st = smem_u32(smem + stage * kStageBytes);
           const uint32_t sft = tmem + kSfCol0 + stage * kSfColsPerStage;
+          // scales into TMEM: A's 4 atoms (one per K=64 step) in columns [0, 16); B's in
+          // [16, 48), the two 128-row halves of a K step side by side (8 columns per step), the
+          // layout an N=256 MMA reads its B scales from
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) tmem_cp_sf_tile(sft + kk * 4, sdesc_sf_tile(st + kOffSfa + kk * 512));
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
+          for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              tmem_cp_sf_tile(sft + 16 + h * 16 + kk * 4, sdesc_sf_tile(st + kOffSfb + h * 2048 + kk * 512));
+            for (int h = 0; h < 2; ++h)
+              tmem_cp_sf_tile(sft + 16 + kk * 8 + h * 4, sdesc_sf_tile(st + kOffSfb + h * 2048 + kk * 512));
+          // one M=128, N=256, K=64 MMA per K step: the 256-row B tile is one operand (8-row
+          // groups 1024 bytes apart, so its second half follows the first)
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t adesc = sdesc_kmajor_sw128(st + kk * 32);
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const uint64_t bdesc = sdesc_kmajor_sw128(st + kOffB + h * (128 * 128) + kk * 32);
-              mma_mxf4nvf4(tmem + h * 128, adesc, bdesc, idesc, sft + kk * 4, sft + 16 + h * 16 + kk * 4,
-                           (kb | kk) != 0);
-            }
-          }
+          for (int kk = 0; kk < 4; ++kk)
+            mma_mxf4nvf4(tmem, sdesc_kmajor_sw128(st + kk * 32), sdesc_kmajor_sw128(st + kOffB + kk * 32), idesc,
+                         sft + kk * 4, sft + 16 + kk * 8, (kb | kk) != 0);
           tc_commit(&empty[stage]);
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
