@@ -26,8 +26,23 @@ constexpr uint32_t kStageTx = kStageBytes;
 constexpr int kTmemCols = 512;
 constexpr int kSfCol0 = 256;
 constexpr int kSfColsPerStage = 48;
-constexpr int kThreads = 320;  // producer, MMA, 8 epilogue warps
+// 16 warps in four warpgroups: warpgroup 0 = producer (warp 0), MMA issuer (warp 1) and two
+// scale writers (warps 2, 3); warpgroups 1-2 = the eight epilogue warps (4-11); warpgroup 3
+// = two scale writers (warps 12, 13) and two idle warps. A warp reaches only the TMEM lane
+// quarter warp % 4, so the four writers (quarters 2, 3, 0, 1) cover all 128 lanes.
+constexpr int kThreads = 512;
 constexpr int kEpiThreads = 256;
+constexpr int kEpiWarp0 = 4;
+__host__ __device__ constexpr bool is_sf_writer(int warp) { return warp == 2 || warp == 3 || warp == 12 || warp == 13; }
+constexpr int kSfWriters = 4;
+// Register split (setmaxnreg): the epilogue warpgroups hold a tile's 128 accumulator columns
+// per thread; the other two need few (72 keeps the producer's loop free of spills, which on
+// its own slowed the launch by several percent). The launch gives 512 x 128 = 65536
+// registers, and the split must not exceed that, or the raising warps would wait forever.
+constexpr int kRegsAtLaunch = 128;
+constexpr int kRegsEpi = 184;
+constexpr int kRegsOther = 72;
+static_assert(2 * 128 * kRegsEpi + 2 * 128 * kRegsOther <= kThreads * kRegsAtLaunch, "register split");
 constexpr int kSmemExtra = 1024 /*align*/ + 256 /*barriers*/;
 constexpr int kUnitRing = 4;      // work-unit ids handed from the producer to the other roles
 // Tiles whose real rows all lie in the first kSparseRows rows (decode: a few tokens per
@@ -36,9 +51,12 @@ constexpr int kUnitRing = 4;      // work-unit ids handed from the producer to t
 constexpr int kSparseRows = 8;
 constexpr int kSparseStageBytes = kSparseRows * kTileN * 4 + kSparseRows * 8;  // FP32 rows, slot + scalar
 constexpr int kSparseMaxExperts = 384;  // above this the expert offsets leave no room for the stage
-constexpr int kRingConsumers = 1 + kEpiThreads / 32;  // MMA thread + one lane per epilogue warp
+constexpr int kRingConsumers = 1 + kEpiThreads / 32 + kSfWriters;  // MMA thread, one lane per epilogue and writer warp
 
 static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
+// barriers (full, empty, sf_full per stage; acc_full, acc_empty, final; the unit ring's two
+// sets; stage_full, stage_empty), then the unit ring, the TMEM address and the abort flag
+static_assert((3 * kStages + 3 + 2 * kUnitRing + 2) * 8 + kUnitRing * 4 + 8 <= 256, "barrier area");
 static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
 
 // One GEMM of the launch: operands, scales, per-expert scalars and output.
@@ -505,8 +523,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
   uint64_t* unit_empty = unit_full + kUnitRing;
   uint64_t* stage_full = unit_empty + kUnitRing;
   uint64_t* stage_empty = stage_full + 1;
-  volatile int32_t* unit_ring = reinterpret_cast<volatile int32_t*>(stage_empty + 1);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stage_empty + 1) + kUnitRing;
+  uint64_t* sf_full = stage_empty + 1;  // per stage: its scales are in TMEM (one arrival per writer warp)
+  volatile int32_t* unit_ring = reinterpret_cast<volatile int32_t*>(sf_full + kStages);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_full + kStages) + kUnitRing;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int32_t* s_off = reinterpret_cast<int32_t*>(smem + kStages * kStageBytes + 256);
   // sparse-epilogue stage: [kSparseRows][kTileN] FP32, then per-row slot and scalar
@@ -515,11 +534,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
   float* s_scal = reinterpret_cast<float*>(s_slot + kSparseRows);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool epi_warp = warp >= kEpiWarp0 && warp < kEpiWarp0 + kEpiThreads / 32;
   pdl_trigger();
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+      mbar_init(&sf_full[s], kSfWriters);
     }
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, kEpiThreads);
@@ -544,13 +565,15 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
-  if (warp >= 2 && p.sparse) {
+  if (epi_warp && p.sparse) {
     // while the previous kernel finishes: one dry pass of the sparse epilogue (expert 0),
     // which brings its code and the scalar tables into the caches
     if constexpr (kEpi0 == kG1Fused || is_g2(kEpi0))
-      sparse_compute<kEpi0, ACT>(p, p.ph[0], threadIdx.x - 64, 0, 0, 0, 1, s_stage, s_slot, s_scal, true);
+      sparse_compute<kEpi0, ACT>(p, p.ph[0], threadIdx.x - kEpiWarp0 * 32, 0, 0, 0, 1, s_stage, s_slot, s_scal,
+                                 true);
     if constexpr (kChain)
-      sparse_compute<kEpi1, MOE_ACT_IDENTITY>(p, p.ph[1], threadIdx.x - 64, 0, 0, 0, 1, s_stage, s_slot, s_scal, true);
+      sparse_compute<kEpi1, MOE_ACT_IDENTITY>(p, p.ph[1], threadIdx.x - kEpiWarp0 * 32, 0, 0, 0, 1, s_stage, s_slot,
+                                              s_scal, true);
   }
   pdl_wait();  // the plan, activations and tile counter come from earlier kernels
   // the producer's first claim goes out now (its round trip overlaps the plan load); each
@@ -578,128 +601,167 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     return u;
   };
 
-  if (warp == 0) {
-    if (lane == 0) {
-      uint32_t stage = 0, phase = 0;
-      uint32_t issued_mask = 0, issued_phase = 0;
-      uint32_t rslot = 0, rphase = 0;
-      bool ok = true;
-      while (ok) {
-        // claim the next unit (in order, from the global counter) and publish its id
-        if (!mbar_wait(&unit_empty[rslot], rphase ^ 1, abort_flag, p.dev_status, p.wait_ns)) { ok = false; break; }
-        // claims increase per CTA, so a GEMM2 tile never waits behind a GEMM1 tile that its
-        // own CTA has claimed but not started
-        int u = next_claim;
-        next_claim = atomicAdd(p.tile_counter, 1);
-        if (u >= total_units) u = -1;
-        unit_ring[rslot] = u;
-        mbar_arrive(&unit_full[rslot]);
-        if (++rslot == kUnitRing) { rslot = 0; rphase ^= 1; }
-        if (u < 0) break;
-        const bool second = kChain && u >= units0;
-        const Phase& ph = p.ph[second ? 1 : 0];
-        int e, nt, mi;
-        decode_unit(second ? u - units0 : u, s_off, p.El, ph.n_tiles, e, nt, mi);
-        const int row0 = s_off[e] + mi * kTileM;
-        const int brow0 = e * ph.Np + nt * kTileN;
-        const int64_t kt = ph.Kp >> 6;  // 512-byte scale tiles per 128 rows
-        const uint8_t* sfa = ph.sfa + static_cast<int64_t>(row0 >> 7) * kt * 512;
-        const uint8_t* sfb0 = ph.sfb + (static_cast<int64_t>(e) * (ph.Np >> 7) + nt * 2) * kt * 512;
-        const uint8_t* sfb1 = sfb0 + kt * 512;
-        if (second) {
-          // wait until every GEMM1 tile of these rows has been written; if they are not yet,
-          // the weight tile and its scales (which do not depend on GEMM1) start towards L2
-          const int32_t* done = p.mt_done + (row0 >> 7);
-          const int target = (kEpiThreads / 32) * p.ph[0].n_tiles;
-          int seen;
-          asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(seen) : "l"(done) : "memory");
-          if (seen < target) {
-            prefetch_l2(ph.b_raw + static_cast<int64_t>(brow0) * (ph.K / 2),
-                        static_cast<int64_t>(kTileN) * (ph.K / 2));
-            prefetch_l2(sfb0, 2 * kt * 512);
-            if (!wait_counter(done, target, abort_flag, p.dev_status, p.wait_ns)) {
-              ok = false;
-              break;
+  if (!epi_warp) {
+    // warpgroups 0 and 3 give up registers first; the epilogue's raise draws on them
+    setmaxnreg_dec<kRegsOther>();
+    if (warp == 0) {
+      if (lane == 0) {
+        uint32_t stage = 0, phase = 0;
+        uint32_t issued_mask = 0, issued_phase = 0;
+        uint32_t rslot = 0, rphase = 0;
+        bool ok = true;
+        while (ok) {
+          // claim the next unit (in order, from the global counter) and publish its id
+          if (!mbar_wait(&unit_empty[rslot], rphase ^ 1, abort_flag, p.dev_status, p.wait_ns)) { ok = false; break; }
+          // claims increase per CTA, so a GEMM2 tile never waits behind a GEMM1 tile that its
+          // own CTA has claimed but not started
+          int u = next_claim;
+          next_claim = atomicAdd(p.tile_counter, 1);
+          if (u >= total_units) u = -1;
+          unit_ring[rslot] = u;
+          mbar_arrive(&unit_full[rslot]);
+          if (++rslot == kUnitRing) { rslot = 0; rphase ^= 1; }
+          if (u < 0) break;
+          const bool second = kChain && u >= units0;
+          const Phase& ph = p.ph[second ? 1 : 0];
+          int e, nt, mi;
+          decode_unit(second ? u - units0 : u, s_off, p.El, ph.n_tiles, e, nt, mi);
+          const int row0 = s_off[e] + mi * kTileM;
+          const int brow0 = e * ph.Np + nt * kTileN;
+          const int64_t kt = ph.Kp >> 6;  // 512-byte scale tiles per 128 rows
+          const uint8_t* sfa = ph.sfa + static_cast<int64_t>(row0 >> 7) * kt * 512;
+          const uint8_t* sfb0 = ph.sfb + (static_cast<int64_t>(e) * (ph.Np >> 7) + nt * 2) * kt * 512;
+          const uint8_t* sfb1 = sfb0 + kt * 512;
+          if (second) {
+            // wait until every GEMM1 tile of these rows has been written; if they are not yet,
+            // the weight tile and its scales (which do not depend on GEMM1) start towards L2
+            const int32_t* done = p.mt_done + (row0 >> 7);
+            const int target = (kEpiThreads / 32) * p.ph[0].n_tiles;
+            int seen;
+            asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(seen) : "l"(done) : "memory");
+            if (seen < target) {
+              prefetch_l2(ph.b_raw + static_cast<int64_t>(brow0) * (ph.K / 2),
+                          static_cast<int64_t>(kTileN) * (ph.K / 2));
+              prefetch_l2(sfb0, 2 * kt * 512);
+              if (!wait_counter(done, target, abort_flag, p.dev_status, p.wait_ns)) {
+                ok = false;
+                break;
+              }
             }
+            fence_proxy_async_global();  // the TMA reads below follow the observed generic writes
           }
-          fence_proxy_async_global();  // the TMA reads below follow the observed generic writes
+          // a tile whose row 32 is padding has all its real rows in the first 32 (padding rows
+          // end a segment): load only those; the MMA rows fed by stale shared memory are
+          // padding rows, whose results are never stored
+          const bool short_tile = p.row_to_slot[row0 + 32] < 0;
+          const uint32_t tx = short_tile ? kStageTx - (kABytes - 32 * 128) : kStageTx;
+          for (int kb = 0; kb < ph.nkb; ++kb) {
+            if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.dev_status, p.wait_ns)) { ok = false; break; }
+            uint8_t* st = smem + stage * kStageBytes;
+            mbar_arrive_expect_tx(&full[stage], tx);
+            tma_load_2d(st, short_tile ? &ph.tmap_a32 : &ph.tmap_a, kb * 128, row0, &full[stage]);
+            tma_load_2d(st + kOffB, &ph.tmap_b, kb * 128, brow0, &full[stage]);
+            bulk_load(st + kOffSfa, sfa + kb * 2048, 2048, &full[stage]);
+            bulk_load(st + kOffSfb, sfb0 + kb * 2048, 2048, &full[stage]);
+            bulk_load(st + kOffSfb + 2048, sfb1 + kb * 2048, 2048, &full[stage]);
+            issued_mask |= 1u << stage;
+            issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+            if (++stage == kStages) { stage = 0; phase ^= 1; }
+          }
         }
-        // a tile whose row 32 is padding has all its real rows in the first 32 (padding rows
-        // end a segment): load only those; the MMA rows fed by stale shared memory are
-        // padding rows, whose results are never stored
-        const bool short_tile = p.row_to_slot[row0 + 32] < 0;
-        const uint32_t tx = short_tile ? kStageTx - (kABytes - 32 * 128) : kStageTx;
-        for (int kb = 0; kb < ph.nkb; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.dev_status, p.wait_ns)) { ok = false; break; }
-          uint8_t* st = smem + stage * kStageBytes;
-          mbar_arrive_expect_tx(&full[stage], tx);
-          tma_load_2d(st, short_tile ? &ph.tmap_a32 : &ph.tmap_a, kb * 128, row0, &full[stage]);
-          tma_load_2d(st + kOffB, &ph.tmap_b, kb * 128, brow0, &full[stage]);
-          bulk_load(st + kOffSfa, sfa + kb * 2048, 2048, &full[stage]);
-          bulk_load(st + kOffSfb, sfb0 + kb * 2048, 2048, &full[stage]);
-          bulk_load(st + kOffSfb + 2048, sfb1 + kb * 2048, 2048, &full[stage]);
-          issued_mask |= 1u << stage;
-          issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
-          if (++stage == kStages) { stage = 0; phase ^= 1; }
-        }
+        // copies may still be landing in shared memory (after an abort, or when another role
+        // gave up before consuming them): let every issued stage land before the CTA exits
+        for (int s = 0; s < kStages; ++s)
+          if (issued_mask & (1u << s)) mbar_drain(&full[s], (issued_phase >> s) & 1);
       }
-      // copies may still be landing in shared memory (after an abort, or when another role
-      // gave up before consuming them): let every issued stage land before the CTA exits
-      for (int s = 0; s < kStages; ++s)
-        if (issued_mask & (1u << s)) mbar_drain(&full[s], (issued_phase >> s) & 1);
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_mxf4nvf4(kTileM, kTileN);
-      uint32_t stage = 0, phase = 0, acc_phase = 0;
+    } else if (warp == 1) {
+      if (lane == 0) {
+        constexpr uint32_t idesc = idesc_mxf4nvf4(kTileM, kTileN);
+        uint32_t stage = 0, phase = 0, acc_phase = 0;
+        uint32_t rslot = 0, rphase = 0;
+        bool ok = true;
+        while (ok) {
+          const int u = take_unit(rslot, rphase, true);
+          if (u < 0) break;
+          if (!mbar_wait(acc_empty, acc_phase ^ 1, abort_flag, p.dev_status, p.wait_ns)) { ok = false; break; }
+          tc_fence_after();
+          const int nkb = p.ph[kChain && u >= units0 ? 1 : 0].nkb;
+          for (int kb = 0; kb < nkb; ++kb) {
+            // the stage's operands have landed and the writer warps have put its scales in TMEM
+            if (!mbar_wait(&sf_full[stage], phase, abort_flag, p.dev_status, p.wait_ns)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t st = smem_u32(smem + stage * kStageBytes);
+            const uint32_t sft = tmem + kSfCol0 + stage * kSfColsPerStage;
+            // one M=128, N=256, K=64 MMA per K step: the 256-row B tile is one operand (8-row
+            // groups 1024 bytes apart, so its second half follows the first)
+  #pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_mxf4nvf4(tmem, sdesc_kmajor_sw128(st + kk * 32), sdesc_kmajor_sw128(st + kOffB + kk * 32), idesc,
+                           sft + kk * 4, sft + 16 + kk * 8, (kb | kk) != 0);
+            tc_commit(&empty[stage]);
+            if (++stage == kStages) { stage = 0; phase ^= 1; }
+          }
+          if (!ok) break;
+          tc_commit(acc_full);
+          acc_phase ^= 1;
+        }
+        // every MMA issued by this thread has finished before TMEM is released
+        tc_commit(final_bar);
+        mbar_drain(final_bar, 0);
+      }
+    } else if (is_sf_writer(warp)) {
+      // Scale writers: per stage, once its copies have landed, each writer warp stores the
+      // stage's scale atoms into its own TMEM lane quarter (tcgen05.st), the layout the
+      // MMAs read: A's 4 atoms (one per K=64 step) in columns [0, 16); B's in [16, 48), the
+      // two 128-row halves of a K step side by side (8 columns per step). Line l of a 512-byte
+      // atom (16 bytes: the scales of rows l, l+32, l+64, l+96) goes to lane l of every
+      // quarter, as a replicating copy of the atom would put it. This keeps the MMA thread's
+      // instruction stream to the MMAs alone. A stage's scale columns are free once its
+      // operands have landed: the producer reloads a stage only after the MMAs that read it
+      // (and its scale columns) have completed.
+      const uint32_t sf_lane = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + kSfCol0;
+      uint32_t stage = 0, phase = 0;
       uint32_t rslot = 0, rphase = 0;
       bool ok = true;
       while (ok) {
-        const int u = take_unit(rslot, rphase, true);
+        const int u = take_unit(rslot, rphase, false);
         if (u < 0) break;
-        if (!mbar_wait(acc_empty, acc_phase ^ 1, abort_flag, p.dev_status, p.wait_ns)) { ok = false; break; }
-        tc_fence_after();
         const int nkb = p.ph[kChain && u >= units0 ? 1 : 0].nkb;
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(&full[stage], phase, abort_flag, p.dev_status, p.wait_ns)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t st = smem_u32(smem + stage * kStageBytes);
-          const uint32_t sft = tmem + kSfCol0 + stage * kSfColsPerStage;
-          // scales into TMEM: A's 4 atoms (one per K=64 step) in columns [0, 16); B's in
-          // [16, 48), the two 128-row halves of a K step side by side (8 columns per step), the
-          // layout an N=256 MMA reads its B scales from
+          const bool got = mbar_wait(&full[stage], phase, abort_flag, p.dev_status, p.wait_ns);
+          if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+          // 16 columns per store (A's four atoms; then B's K steps 0-1 and 2-3)
+        const uint4* atoms = reinterpret_cast<const uint4*>(smem + stage * kStageBytes + kOffSfa);
+        const uint32_t sft = sf_lane + stage * kSfColsPerStage;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) tmem_cp_sf_tile(sft + kk * 4, sdesc_sf_tile(st + kOffSfa + kk * 512));
+        for (int part = 0; part < 3; ++part) {
+          uint32_t v[16];
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-              tmem_cp_sf_tile(sft + 16 + kk * 8 + h * 4, sdesc_sf_tile(st + kOffSfb + h * 2048 + kk * 512));
-          // one M=128, N=256, K=64 MMA per K step: the 256-row B tile is one operand (8-row
-          // groups 1024 bytes apart, so its second half follows the first)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_mxf4nvf4(tmem, sdesc_kmajor_sw128(st + kk * 32), sdesc_kmajor_sw128(st + kOffB + kk * 32), idesc,
-                         sft + kk * 4, sft + 16 + kk * 8, (kb | kk) != 0);
-          tc_commit(&empty[stage]);
+          for (int i = 0; i < 4; ++i) {
+            // part 0: A atom i; parts 1-2: B atom (K step 2(part-1) + i/2, half i%2)
+            const int atom = part == 0 ? i : 4 + (i & 1) * 4 + (part - 1) * 2 + (i >> 1);
+            const uint4 w = atoms[atom * 32 + lane];
+            v[4 * i] = w.x; v[4 * i + 1] = w.y; v[4 * i + 2] = w.z; v[4 * i + 3] = w.w;
+          }
+          tmem_st16(sft + 16 * part, v);
+        }
+        tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sf_full[stage]);
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
-        if (!ok) break;
-        tc_commit(acc_full);
-        acc_phase ^= 1;
       }
-      // every MMA issued by this thread has finished before TMEM is released
-      tc_commit(final_bar);
-      mbar_drain(final_bar, 0);
     }
   } else {
+    setmaxnreg_inc<kRegsEpi>();
     const int q = warp & 3;                 // TMEM lane quarter this warp may access
-    const int half = (warp - 2) >> 2;       // column half of the tile
+    const int half = (warp - kEpiWarp0) >> 2;  // column half of the tile
     const int r = q * 32 + lane;            // row inside the 128-row tile
     const uint32_t tmem_row = tmem + (static_cast<uint32_t>(q * 32) << 16);
     uint32_t acc_phase = 0, sphase = 0;
     uint32_t rslot = 0, rphase = 0;
-    const int etid = threadIdx.x - 64;      // 0..255 over the epilogue warps
+    const int etid = threadIdx.x - kEpiWarp0 * 32;  // 0..255 over the epilogue warps
     while (true) {
       const int u = take_unit(rslot, rphase, false);
       if (u < 0) break;
@@ -735,6 +797,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
 template <int MODE, int ACT>
 moe_status_t launch_kernel(const GemmParams& prm, int64_t units_max, size_t smem, cudaStream_t s) {
   auto kern = grouped_gemm_kernel<MODE, ACT>;
+  // the register split is drawn from what the launch provides: refuse a build that gives less
+  cudaFuncAttributes fa;
+  MOE_CUDA(cudaFuncGetAttributes(&fa, kern));
+  if (fa.numRegs < kRegsAtLaunch) return MOE_ERR_CUDA;
   MOE_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)));
   // persistent: one CTA per SM, at most one per work unit
   const int grid = static_cast<int>(units_max < num_sms() ? units_max : num_sms());
