@@ -84,6 +84,9 @@ bool fill_phase(Phase& ph, const GemmLaunch& g) {
   ph.alpha_gate = g.alpha_gate;
   ph.out = g.out;
   ph.out_sf = g.out_sf;
+  // rows are N (a multiple of 128) BF16 values long and stored from 32-value column offsets,
+  // so a 32-byte aligned base keeps every row store 32-byte aligned
+  ph.out_v8 = (reinterpret_cast<uintptr_t>(g.out) & 31) == 0;
   ph.K = static_cast<int32_t>(g.K);
   ph.Kp = static_cast<int32_t>(g.Kp);
   ph.nkb = static_cast<int32_t>(g.Kp / kTileK);

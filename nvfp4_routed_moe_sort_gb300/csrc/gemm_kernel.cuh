@@ -72,6 +72,7 @@ struct Phase {
   void* out;
   uint8_t* out_sf;
   int32_t K, Kp, nkb, N, Np, n_tiles;
+  int32_t out_v8;         // `out` is 32-byte aligned: BF16 rows go out in 32-byte stores
 };
 
 struct GemmParams {
@@ -177,13 +178,24 @@ __device__ __forceinline__ void load_acc(uint32_t tmem_row, int half, uint32_t* 
   mbar_arrive(acc_empty);
 }
 
-__device__ __forceinline__ void store_bf16x32(uint16_t* dst, const float* v) {
+// 32 BF16 values (64 bytes) at dst: two 32-byte stores, each a whole L2 sector, when dst is
+// 32-byte aligned (v8); else four 16-byte stores
+__device__ __forceinline__ void store_bf16x32(uint16_t* dst, const float* v, bool v8) {
   uint32_t w[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-  uint4* d = reinterpret_cast<uint4*>(dst);
+  if (v8) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) d[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    for (int i = 0; i < 2; ++i)
+      asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + 16 * i), "r"(w[8 * i]),
+                   "r"(w[8 * i + 1]), "r"(w[8 * i + 2]), "r"(w[8 * i + 3]), "r"(w[8 * i + 4]), "r"(w[8 * i + 5]),
+                   "r"(w[8 * i + 6]), "r"(w[8 * i + 7])
+                   : "memory");
+  } else {
+    uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+  }
 }
 
 template <int MODE, int ACT>
@@ -202,7 +214,7 @@ __device__ __forceinline__ void epilogue_compute(const GemmParams& p, const Phas
       float v[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] = __fmul_rn(__uint_as_float(r[32 * c + i]), d2);
-      store_bf16x32(orow + 32 * c, v);
+      store_bf16x32(orow + 32 * c, v, ph.out_v8);
     }
   } else if constexpr (MODE == kG2Reduce) {
     // acc[t, :] += (y2 * w') for this row's token t, w' = fp32(w * rsf)
@@ -271,7 +283,7 @@ __device__ __forceinline__ void epilogue_compute(const GemmParams& p, const Phas
 #undef MOE_YG
       const int ic = i0 + 32 * c;
       if constexpr (MODE == kG1Act) {
-        store_bf16x32(static_cast<uint16_t*>(ph.out) + prow * I + ic, h);
+        store_bf16x32(static_cast<uint16_t*>(ph.out) + prow * I + ic, h, ph.out_v8);
       } else {
         uint8_t* dst = static_cast<uint8_t*>(ph.out) + prow * (I / 2) + ic / 2;
         const uint32_t q2 = requant32_store(h, p.g2, dst);
