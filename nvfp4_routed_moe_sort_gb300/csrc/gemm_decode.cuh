@@ -53,19 +53,30 @@ constexpr int kOffX = kWBytes;
 constexpr int kOffSfw = kOffX + kXBytes;
 constexpr int kOffSfx = kOffSfw + kSfwBytes;
 constexpr int kStageBytes = kOffSfx + kSfxBytes;  // 40 KB
-constexpr int kThreads = 192;
+// warp 0 producer, warp 1 MMA issuer, warps 2-5 epilogue, warps 6-9 scale writers (each
+// warp reaches only the TMEM lane quarter warp % 4, so each role's four warps cover all 128)
+constexpr int kThreads = 320;
 constexpr int kEpiWarps = 4;
 constexpr int kEpiThreads = kEpiWarps * 32;
+constexpr int kSfWriter0 = 2 + kEpiWarps;
+constexpr int kSfWriters = 4;
 constexpr int kTmemCols = 512;
 constexpr int kAccCols = 2 * kTokens;             // one accumulator buffer: two halves x 16 columns
 constexpr int kSfCol0 = 2 * kAccCols;             // after the two accumulator buffers
 constexpr int kSfColsPerStage = 48;               // 2 weight tiles x 16 + 16 for the tokens
 constexpr int kUnitRing = 4;
-constexpr int kRingConsumers = 1 + kEpiWarps;
-constexpr int kSmemExtra = 1024 /*align*/ + 256 /*barriers*/;
+constexpr int kRingConsumers = 1 + kEpiWarps + kSfWriters;
+constexpr int kBarBytes = 512;  // barriers, unit ring, TMEM address, flags
+constexpr int kSmemExtra = 1024 /*align*/ + kBarBytes;
 
 static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
 static_assert(kSfCol0 + kStages * kSfColsPerStage <= kTmemCols, "TMEM budget");
+// full, empty, sf_full, pre per stage; acc_full/acc_empty pairs; final; the unit ring's two
+// sets; then the ring, the TMEM address, the abort flag and the active-expert count
+static_assert((4 * kStages + 5 + 2 * kUnitRing) * 8 + kUnitRing * 4 + 12 <= kBarBytes, "barrier area");
+// the 12 scale atoms of a stage (two weight tiles x 4 K=64 steps, then the tokens' 4) are
+// contiguous, atom a feeding TMEM columns [4a, 4a+4) of the stage
+static_assert(kOffSfx == kOffSfw + 8 * 512 && kSfColsPerStage == 12 * 4, "scale atom order");
 
 // One GEMM of the launch.
 struct Phase {
@@ -207,11 +218,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm_kernel(const __grid_c
   uint64_t* unit_full = final_bar + 1;
   uint64_t* unit_empty = unit_full + kUnitRing;
   uint64_t* pre_bar = unit_empty + kUnitRing;  // [kStages] weight stages loaded before the wait
-  volatile int32_t* unit_ring = reinterpret_cast<volatile int32_t*>(pre_bar + kStages);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pre_bar + kStages) + kUnitRing;
+  uint64_t* sf_full = pre_bar + kStages;       // [kStages] the stage's scales are in TMEM
+  volatile int32_t* unit_ring = reinterpret_cast<volatile int32_t*>(sf_full + kStages);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_full + kStages) + kUnitRing;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* s_nact = const_cast<int*>(abort_flag) + 1;
-  int32_t* s_off = reinterpret_cast<int32_t*>(smem + kStages * kStageBytes + 256);
+  int32_t* s_off = reinterpret_cast<int32_t*>(smem + kStages * kStageBytes + kBarBytes);
   int32_t* s_act = s_off + roundup64(p.El + 1, 4);  // active local experts, ascending
   uint8_t* s_flag = reinterpret_cast<uint8_t*>(s_act + p.El);  // routed local experts (from the ids)
 
@@ -227,6 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm_kernel(const __grid_c
       mbar_init(&acc_empty[b], kEpiThreads);
     }
     for (int s = 0; s < kStages; ++s) mbar_init(&pre_bar[s], 1);
+    for (int s = 0; s < kStages; ++s) mbar_init(&sf_full[s], kSfWriters);
     mbar_init(final_bar, 1);
     for (int i = 0; i < kUnitRing; ++i) {
       mbar_init(&unit_full[i], 1);
@@ -499,17 +512,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm_kernel(const __grid_c
         const int nkb = p.ph[u >= units0 ? 1 : 0].nkb;
         const uint32_t acc = tmem + buf * kAccCols;
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(&full[stage], phase, abort_flag, p.dev_status, p.wait_ns)) { ok = false; break; }
+          // the stage has landed and the writer warps have put its scales in TMEM: the
+          // weight tiles' at [h*16 + kk*4, +4), the tokens' at [32 + kk*4, +4)
+          if (!mbar_wait(&sf_full[stage], phase, abort_flag, p.dev_status, p.wait_ns)) { ok = false; break; }
           tc_fence_after();
           const uint32_t st = smem_u32(smem + stage * kStageBytes);
           const uint32_t sft = tmem + kSfCol0 + stage * kSfColsPerStage;
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              tmem_cp_sf_tile(sft + h * 16 + kk * 4, sdesc_sf_tile(st + kOffSfw + h * 2048 + kk * 512));
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) tmem_cp_sf_tile(sft + 32 + kk * 4, sdesc_sf_tile(st + kOffSfx + kk * 512));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t xdesc = sdesc_kmajor_sw128(st + kOffX + kk * 32);
@@ -530,6 +538,42 @@ __global__ void __launch_bounds__(kThreads, 1) decode_gemm_kernel(const __grid_c
       }
       tc_commit(final_bar);
       mbar_drain(final_bar, 0);
+    }
+  } else if (warp >= kSfWriter0) {
+    // Scale writers: per stage, once it has landed, each writer warp stores the stage's 12
+    // scale atoms into its own TMEM lane quarter (tcgen05.st), line l of an atom to lane l,
+    // as a copy replicated over the four quarters would put it. A stage's scale columns are
+    // free once it has landed: the producer reloads a stage only after the MMAs that read it
+    // have completed.
+    const uint32_t sf_lane = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + kSfCol0;
+    uint32_t stage = 0, phase = 0;
+    uint32_t rslot = 0, rphase = 0;
+    bool ok = true;
+    while (ok) {
+      const int u = take_unit(rslot, rphase, false);
+      if (u < 0) break;
+      const int nkb = p.ph[u >= units0 ? 1 : 0].nkb;
+      for (int kb = 0; kb < nkb; ++kb) {
+        const bool got = mbar_wait(&full[stage], phase, abort_flag, p.dev_status, p.wait_ns);
+        if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
+        const uint4* atoms = reinterpret_cast<const uint4*>(smem + stage * kStageBytes + kOffSfw);
+        const uint32_t sft = sf_lane + stage * kSfColsPerStage;
+#pragma unroll
+        for (int part = 0; part < 3; ++part) {
+          uint32_t v[16];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint4 w = atoms[(4 * part + i) * 32 + lane];
+            v[4 * i] = w.x; v[4 * i + 1] = w.y; v[4 * i + 2] = w.z; v[4 * i + 3] = w.w;
+          }
+          tmem_st16(sft + 16 * part, v);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sf_full[stage]);
+        if (++stage == kStages) { stage = 0; phase ^= 1; }
+      }
     }
   } else {
     const int q = warp & 3;                 // TMEM lane quarter of this warp

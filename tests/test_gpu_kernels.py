@@ -151,14 +151,20 @@ def test_plan_duplicate_sets_status():
     assert _check_plan(ids, 8, 0, 8, allow_dup=True) & pkg.MOE_DEV_DUPLICATE_EXPERT
 
 
-@pytest.mark.parametrize("M,k,H,R", [(1, 1, 128, 4), (7, 3, 256, 30), (300, 8, 2048, 900), (64, 6, 7168, 128)])
-def test_finalize_bitexact(M, k, H, R):
+# shift = 8 values places rows and out 16 bytes past a 32-byte boundary (the API asks for
+# 16-byte alignment only); H = 384 leaves most threads of a token's block without columns
+@pytest.mark.parametrize("M,k,H,R,shift", [(1, 1, 128, 4, 0), (7, 3, 256, 30, 0), (300, 8, 2048, 900, 0),
+                                           (64, 6, 7168, 128, 0), (1000, 4, 384, 2000, 0), (1000, 4, 384, 2000, 8),
+                                           (300, 8, 2048, 900, 8)])
+def test_finalize_bitexact(M, k, H, R, shift):
     rng = np.random.default_rng(M * k)
-    rows = torch.from_numpy(rng.standard_normal((R, H)).astype(np.float32)).to(torch.bfloat16).to(DEV)
+    rows_all = torch.from_numpy(rng.standard_normal((R * H + shift,)).astype(np.float32)).to(torch.bfloat16).to(DEV)
+    rows = rows_all[shift:].view(R, H)
     t2r = rng.integers(-1, R, size=(M, k)).astype(np.int32)
     w = rng.random((M, k)).astype(np.float32)
     w[t2r < 0] = np.nan                                   # scores of masked slots are never read
-    out = torch.empty(M, H, dtype=torch.bfloat16, device=DEV)
+    out = torch.empty(M * H + shift, dtype=torch.bfloat16, device=DEV)[shift:].view(M, H)
+    assert rows.data_ptr() % 32 == out.data_ptr() % 32 == 2 * shift % 32
     pkg.moe_finalize(rows, torch.from_numpy(w).to(DEV), torch.from_numpy(t2r).to(DEV), out)
     torch.cuda.synchronize()
     ref = O.finalize(bf16_np(rows), w, t2r)
