@@ -577,16 +577,6 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
-  if (epi_warp && p.sparse) {
-    // while the previous kernel finishes: one dry pass of the sparse epilogue (expert 0),
-    // which brings its code and the scalar tables into the caches
-    if constexpr (kEpi0 == kG1Fused || is_g2(kEpi0))
-      sparse_compute<kEpi0, ACT>(p, p.ph[0], threadIdx.x - kEpiWarp0 * 32, 0, 0, 0, 1, s_stage, s_slot, s_scal,
-                                 true);
-    if constexpr (kChain)
-      sparse_compute<kEpi1, MOE_ACT_IDENTITY>(p, p.ph[1], threadIdx.x - kEpiWarp0 * 32, 0, 0, 0, 1, s_stage, s_slot,
-                                              s_scal, true);
-  }
   pdl_wait();  // the plan, activations and tile counter come from earlier kernels
   // the producer's first claim goes out now (its round trip overlaps the plan load); each
   // later claim is issued one unit early, while the current unit's loads go out
@@ -767,6 +757,18 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     }
   } else {
     setmaxnreg_inc<kRegsEpi>();
+    if (p.sparse) {
+      // before the first accumulator is ready: one dry pass of the sparse epilogue (expert 0),
+      // which brings its code and the scalar tables into the caches. (Called here, under the
+      // epilogue's register budget: a call before the role split made the compiler keep values
+      // of the epilogue loop on the stack.)
+      if constexpr (kEpi0 == kG1Fused || is_g2(kEpi0))
+        sparse_compute<kEpi0, ACT>(p, p.ph[0], threadIdx.x - kEpiWarp0 * 32, 0, 0, 0, 1, s_stage, s_slot, s_scal,
+                                   true);
+      if constexpr (kChain)
+        sparse_compute<kEpi1, MOE_ACT_IDENTITY>(p, p.ph[1], threadIdx.x - kEpiWarp0 * 32, 0, 0, 0, 1, s_stage,
+                                                s_slot, s_scal, true);
+    }
     const int q = warp & 3;                 // TMEM lane quarter this warp may access
     const int half = (warp - kEpiWarp0) >> 2;  // column half of the tile
     const int r = q * 32 + lane;            // row inside the 128-row tile
