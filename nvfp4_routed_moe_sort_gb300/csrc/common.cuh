@@ -31,8 +31,10 @@ __host__ __device__ constexpr int64_t roundup64(int64_t x, int64_t a) { return (
 // padded to 128 and whose scale columns are padded to `kcols_padded` (a multiple of 16, i.e.
 // K padded to 256). A tile of 128 rows x 4 scales is 512 contiguous bytes: byte
 // (r % 32) * 16 + ((r % 128) / 32) * 4 + c % 4. Tiles are ordered row-tile-major, then by
-// scale-column group. This is the shared-memory layout that one
-// tcgen05.cp.32x128b.warpx4 turns into the TMEM scale layout of an M=128 block-scaled MMA.
+// scale-column group. Line l of a tile (16 bytes: rows l, l+32, l+64, l+96) is what TMEM
+// lane l of every lane quarter holds in the scale layout of an M=128 block-scaled MMA (the
+// layout a replicating tcgen05.cp.32x128b.warpx4 copy of the tile produces), so the GEMMs
+// load a tile with one bulk copy and store its lines into TMEM unchanged.
 __host__ __device__ __forceinline__ int64_t sf_tile_offset(int64_t r, int64_t c, int64_t kcols_padded) {
   return ((r >> 7) * (kcols_padded >> 2) + (c >> 2)) * 512 + (r & 31) * 16 + ((r & 127) >> 5) * 4 + (c & 3);
 }
@@ -263,17 +265,6 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
   return d;
 }
 
-// Shared-memory descriptor of one 512-byte scale tile (32 rows x 16 bytes, no swizzle,
-// 8-row core matrices of 128 contiguous bytes) as the source of tcgen05.cp.32x128b.
-__device__ __forceinline__ uint64_t sdesc_sf_tile(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr & 0x3FFFF) >> 4);
-  d |= (uint64_t)(128 >> 4) << 16;
-  d |= (uint64_t)(128 >> 4) << 32;
-  d |= (uint64_t)1 << 46;
-  return d;
-}
-
 // Instruction descriptor of tcgen05.mma.kind::mxf4nvf4 with E2M1 A and B, K-major both,
 // UE4M3 scales, FP32 accumulation, shape M x N (x K=64).
 __host__ __device__ constexpr uint32_t idesc_mxf4nvf4(int M, int N) {
@@ -292,12 +283,6 @@ __device__ __forceinline__ void mma_mxf4nvf4(uint32_t d_tmem, uint64_t a_desc, u
       " tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n}\n"
       ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
-}
-
-// Copy one 512-byte scale tile from shared memory into TMEM (32 lanes x 128 bits,
-// replicated to the four lane quarters).
-__device__ __forceinline__ void tmem_cp_sf_tile(uint32_t taddr, uint64_t sdesc) {
-  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 // Each thread of the warp loads 32 consecutive 32-bit columns of its TMEM lane into r[].

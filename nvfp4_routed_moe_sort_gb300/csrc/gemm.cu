@@ -8,14 +8,17 @@
 // FlashInfer flashinfer.fused_moe.alphamoe_nvfp4_aligned_moe (capacity-sized grid that
 // skips work past the device-side valid extent).
 //
-// One persistent CTA per SM, 320 threads:
+// One persistent CTA per SM, 512 threads (setmaxnreg: 184 registers for the epilogue
+// warpgroups, 72 for the rest):
 //   warp 0       producer: per stage, two 2D TMA tile loads (A: 128 rows x 128 B, B: 256
 //                rows x 128 B, 128-byte swizzle) and three 2 KB bulk copies of 128x4 scale
 //                tiles, all completing on the stage's full barrier;
-//   warp 1       TMEM owner and MMA issuer: per stage, 12 tcgen05.cp of scale tiles into
-//                TMEM and 4 tcgen05.mma.kind::mxf4nvf4 (M=128, N=256, K=64, E2M1 x E2M1
-//                with UE4M3 scales per 16 values, FP32 accumulation in TMEM);
-//   warps 2..9   epilogue: two warps per TMEM lane quarter, one per column half; each pulls
+//   warp 1       TMEM owner and MMA issuer: per stage, 4 tcgen05.mma.kind::mxf4nvf4 (M=128,
+//                N=256, K=64, E2M1 x E2M1 with UE4M3 scales per 16 values, FP32
+//                accumulation in TMEM), once the stage's scales are in TMEM;
+//   warps 2, 3, 12, 13  scale writers, one per TMEM lane quarter: per stage, the 12 scale
+//                tiles' lines from shared memory into TMEM (tcgen05.st);
+//   warps 4..11  epilogue: two warps per TMEM lane quarter, one per column half; each pulls
 //                its 128 accumulator columns into registers (tcgen05.ld) and releases the
 //                accumulator at once, so the next tile's MMAs overlap its scaling,
 //                activation and NVFP4 requantisation (GEMM1) or BF16 rows (GEMM2); warps

@@ -11,14 +11,16 @@
 // the static FC2 input scale; GEMM2 x alpha2 / fc2_input_scale into BF16 rows or FP32
 // reductions.
 //
-// One persistent CTA per SM, 192 threads:
+// One persistent CTA per SM, 320 threads:
 //   warp 0     producer: per stage one 2D TMA load of the 256-row weight tile (128 B of K
 //              per row), one of the expert's 16 token rows, two 4 KB and one 2 KB bulk
 //              copies of scale tiles; 5 stages of 40 KB;
-//   warp 1     TMEM owner and MMA issuer: per stage 12 tcgen05.cp of scale tiles and 8
+//   warp 1     TMEM owner and MMA issuer: per stage, once its scales are in TMEM, 8
 //              tcgen05.mma.kind::mxf4nvf4 (M=128, N=16, K=64) into one of two accumulator
 //              buffers (double-buffered: the next unit's MMAs overlap this one's epilogue);
-//   warps 2-5  epilogue, one per TMEM lane quarter.
+//   warps 2-5  epilogue, one per TMEM lane quarter;
+//   warps 6-9  scale writers, one per TMEM lane quarter: per stage, the 12 scale tiles'
+//              lines from shared memory into TMEM (tcgen05.st).
 // Work units are (active expert, 256-row weight tile): GEMM1's first, then GEMM2's; a GEMM2
 // unit waits (bounded) until every GEMM1 unit of its expert has been written, after loading
 // or starting its weight tiles.

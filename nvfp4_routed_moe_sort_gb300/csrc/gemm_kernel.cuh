@@ -696,7 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             const uint32_t sft = tmem + kSfCol0 + stage * kSfColsPerStage;
             // one M=128, N=256, K=64 MMA per K step: the 256-row B tile is one operand (8-row
             // groups 1024 bytes apart, so its second half follows the first)
-  #pragma unroll
+#pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               mma_mxf4nvf4(tmem, sdesc_kmajor_sw128(st + kk * 32), sdesc_kmajor_sw128(st + kOffB + kk * 32), idesc,
                            sft + kk * 4, sft + 16 + kk * 8, (kb | kk) != 0);
@@ -733,21 +733,21 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
           const bool got = mbar_wait(&full[stage], phase, abort_flag, p.dev_status, p.wait_ns);
           if (!__all_sync(0xffffffffu, got)) { ok = false; break; }
           // 16 columns per store (A's four atoms; then B's K steps 0-1 and 2-3)
-        const uint4* atoms = reinterpret_cast<const uint4*>(smem + stage * kStageBytes + kOffSfa);
-        const uint32_t sft = sf_lane + stage * kSfColsPerStage;
+          const uint4* atoms = reinterpret_cast<const uint4*>(smem + stage * kStageBytes + kOffSfa);
+          const uint32_t sft = sf_lane + stage * kSfColsPerStage;
 #pragma unroll
-        for (int part = 0; part < 3; ++part) {
-          uint32_t v[16];
+          for (int part = 0; part < 3; ++part) {
+            uint32_t v[16];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            // part 0: A atom i; parts 1-2: B atom (K step 2(part-1) + i/2, half i%2)
-            const int atom = part == 0 ? i : 4 + (i & 1) * 4 + (part - 1) * 2 + (i >> 1);
-            const uint4 w = atoms[atom * 32 + lane];
-            v[4 * i] = w.x; v[4 * i + 1] = w.y; v[4 * i + 2] = w.z; v[4 * i + 3] = w.w;
+            for (int i = 0; i < 4; ++i) {
+              // part 0: A atom i; parts 1-2: B atom (K step 2(part-1) + i/2, half i%2)
+              const int atom = part == 0 ? i : 4 + (i & 1) * 4 + (part - 1) * 2 + (i >> 1);
+              const uint4 w = atoms[atom * 32 + lane];
+              v[4 * i] = w.x; v[4 * i + 1] = w.y; v[4 * i + 2] = w.z; v[4 * i + 3] = w.w;
+            }
+            tmem_st16(sft + 16 * part, v);
           }
-          tmem_st16(sft + 16 * part, v);
-        }
-        tmem_wait_st();
+          tmem_wait_st();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&sf_full[stage]);
