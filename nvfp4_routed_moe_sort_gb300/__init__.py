@@ -19,4 +19,4 @@ from ._lib import (  # noqa: F401
     moe_quantize_weights, moe_routed_forward, moe_routed_forward_workspace_bytes, moe_test_gemm1, status_string,
 )
 from .build import LIB as LIB_PATH  # noqa: F401
-from .moe import NVFP4RoutedMoE, quantize_weights  # noqa: F401
+from .moe import HostStaging, NVFP4RoutedMoE, quantize_weights  # noqa: F401

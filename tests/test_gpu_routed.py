@@ -181,3 +181,37 @@ def test_refresh_in_place_under_captured_graph(name):
     assert np.array_equal(got, bf16_np(p2.run_routed(True)))
     assert_close_output(got, p2.oracle_forward()["out"], f"{name} after refresh")
     assert p.layer.device_status(cfg.M, cfg.top_k, True) == 0
+
+
+@pytest.mark.parametrize("direct", [False, True])
+@pytest.mark.parametrize("name", ["decode_t8", "swiglu_ragged"])
+def test_capture_host_matches_device_path(name, direct):
+    """capture_host: one graph copies the pinned inputs in, runs the forward and copies the
+    output out (direct: the kernels read the pinned inputs and write the pinned output in
+    place). Its host output equals the device path's bit for bit, and stays so after the
+    staging buffer is refilled with new hidden states and a new routing."""
+    cfg = CASES[name]
+    p = Problem(cfg)
+    M, k, H = cfg.M, cfg.top_k, cfg.H
+    staging = pkg.HostStaging(M, H, k, DEV)
+    hout = torch.empty(M, H, dtype=torch.bfloat16).pin_memory()
+    staging.x.copy_(p.x.cpu())
+    staging.ids.copy_(torch.from_numpy(np.ascontiguousarray(p.ids, dtype=np.int32)))
+    staging.weights.copy_(torch.from_numpy(np.ascontiguousarray(p.tw, dtype=np.float32)))
+    g = p.layer.capture_host(staging, hout, direct=direct)
+    for rep in range(2):
+        if rep == 1:
+            # a second step: other tokens (the rows reversed) and another routing
+            cfg2 = cfg.with_(seed=cfg.seed + 100)
+            ids2, tw2 = mi.routing(cfg2)
+            staging.x.copy_(p.x.cpu().flip(0))
+            staging.ids.copy_(torch.from_numpy(np.ascontiguousarray(ids2, dtype=np.int32)))
+            staging.weights.copy_(torch.from_numpy(np.ascontiguousarray(tw2, dtype=np.float32)))
+        g.replay()
+        torch.cuda.synchronize()
+        got = bf16_np(hout).copy()
+        x_dev = staging.x.to(DEV)
+        ref = p.layer.forward(x_dev, staging.ids.to(DEV), staging.weights.to(DEV), do_finalize=True)
+        torch.cuda.synchronize()
+        assert np.array_equal(got, bf16_np(ref)), f"step {rep}"
+        assert p.layer.device_status(M, k, True) == 0
