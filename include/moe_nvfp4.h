@@ -331,6 +331,11 @@ MOE_API moe_status_t moe_finalize(const uint16_t* gemm2_out, const void* topk_we
  *   step_events   0 or 5 cudaEvent_t recorded before the prologue (quantise, plan, permute),
  *                 GEMM1, GEMM2, the combine, and at the end
  * Outputs must not overlap any input, the workspace or each other (MOE_ERR_OVERLAP).
+ * Host buffers: x, topk_ids, topk_weights and, with do_finalize = MOE_OUTPUT_FINALIZED, out
+ * may instead be page-locked host memory that the device addresses directly (cudaHostAlloc
+ * or cudaHostRegister, unified addressing). The kernels then read and write them in place
+ * over the CPU-GPU link, with plain loads and stores. For small batches this saves the fixed
+ * latency of separate copies. For large ones the copy engine moves the data faster.
  * ---------------------------------------------------------------------------------------- */
 MOE_API size_t moe_routed_forward_workspace_bytes(int32_t M, int32_t top_k, const moe_nvfp4_weights_t* w,
                                                   int32_t do_finalize);
