@@ -488,16 +488,17 @@ def run_e2e(layer, x, ids, tw, dev, steps, flush):
         return float(np.mean(times))
 
     graph = layer.capture_host(staging, hout)
+    direct = staging.direct
     ms = time_graph(graph)
-    other = time_graph(layer.capture_host(staging, hout, direct=not graph.direct))
+    other = time_graph(layer.capture_host(staging, hout, direct=not direct))
     kinds = {True: "in place: the kernels read the pinned inputs and write the pinned output over NVLink-C2C",
              False: "copies: one H2D copy of the staging buffer and one D2H copy of the output, in the graph"}
     in_bytes = staging.x.numel() * 2 + staging.ids.numel() * 4 + staging.weights.numel() * 4
     return {"value": M / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms,
-            "h2d_bytes_per_step": int(in_bytes if graph.direct else staging.nbytes),
+            "h2d_bytes_per_step": int(in_bytes if direct else staging.nbytes),
             "d2h_bytes_per_step": int(hout.numel() * 2),
-            "h2d_copies_per_step": 0 if graph.direct else 1, "transfer": kinds[graph.direct],
-            "other_transfer": {"transfer": kinds[not graph.direct], "ms_per_step": other},
+            "h2d_copies_per_step": 0 if direct else 1, "transfer": kinds[direct],
+            "other_transfer": {"transfer": kinds[not direct], "ms_per_step": other},
             "output": "finalized"}
 
 

@@ -250,7 +250,8 @@ class NVFP4RoutedMoE:
         direct=False: the graph copies the staging buffer to the device (one transfer), runs
         the forward and copies the output back. direct=True: the kernels read the pinned
         inputs and write the pinned output in place (over the CPU-GPU link; no copy nodes).
-        None picks direct when the host traffic is at most DIRECT_HOST_BYTES.
+        None picks direct when the host traffic is at most DIRECT_HOST_BYTES. The choice is
+        recorded in ``staging.direct``.
         """
         if not host_out.is_pinned() or host_out.dtype != torch.bfloat16 or tuple(host_out.shape) != (staging.M, staging.H):
             raise ValueError("host_out must be a pinned bf16 tensor of shape [M, H]")
@@ -272,7 +273,7 @@ class NVFP4RoutedMoE:
                 staging.device.copy_(staging.host, non_blocking=True)
                 self.routed(staging.dev_x, staging.dev_ids, staging.dev_weights, b, mode)
                 host_out.copy_(b["out"], non_blocking=True)
-        g.direct = direct
+        staging.direct = direct
         return g
 
     def device_status(self, M: int, top_k: int, do_finalize, routed: bool = True) -> int:
@@ -302,3 +303,4 @@ class HostStaging:
         self.x, self.ids, self.weights = views(self.host)
         self.dev_x, self.dev_ids, self.dev_weights = views(self.device)
         self.nbytes = total
+        self.direct = None  # set by NVFP4RoutedMoE.capture_host: in place (True) or copies (False)
